@@ -1,0 +1,334 @@
+"""CPU oracle for the QuaRot W4A4 hot path -- TEST INFRASTRUCTURE ONLY.
+
+This module is the plain, slow, obviously-correct statement of what the hot
+path computes.  It is used by the test-suite, by ``__graft_entry__.smoke()``
+and by ``bench.py``'s CPU-baseline leg, and by nothing else: the product path
+(``w4a4_rotated_quantized_gb300``) never imports, calls or links it, and this
+module imports nothing from the product.  It shares no code with the CUDA
+path; the only common module is ``workloads`` (seeded random inputs).
+
+Arithmetic is numpy float64 with explicit dense Hadamard matrices (no fast
+transform), an exact integer GEMM, and float32/float16 only where the method
+fixes the storage precision (rotated values are compared as fp32, scales are
+stored as fp16, the dequantised output is fp16).
+
+Sources (page title, section):
+  [S]  "QuaRot: Outlier-Free 4-Bit Inference in Rotated LLMs" (paper summary
+       page), section 3 "Technical Approach": Stage 1a (randomized Hadamard,
+       Kronecker sizes), Stage 1c/1d (head-wise H_dh on V, K and Q), Stage 2a/2b
+       (symmetric per-channel / per-token quantizers, dequantisation), Stage 2c
+       (KV decode procedure), "Kernel Implementation and Hardware Efficiency".
+  [G]  "QuaRot Guide: Outlier-Free 4-Bit W4A4 LLM Quantization" (blog),
+       sections "The Collapse of Naive W4A4" (INT4 grid -8..7), "Why Randomized
+       Walsh-Hadamard Transforms (RHT) Disperse Outliers" (Sylvester doubling,
+       x~_j = (1/sqrt d) sum_k D_kk H_jk x_k), "End-to-End Implementation" (abs-max
+       floor 1e-5).
+  [E]  QuaRot paper-viz explainer (romaanj.github.io): Sylvester for 2^n and a
+       Kronecker product with a Paley-12 block for 12288.
+
+Readings where the pages are silent or disagree (each also listed in the
+design notes):
+  * rotation is x~ = (x * s) @ H / sqrt(d), row-vector convention, signs first;
+  * H_12288 = H12 (+) H1024 (Kronecker, index k = a*1024 + b), H12 = Paley I
+    with q = 11: Jacobsthal Q_ij = chi(j - i), S = [[0, 1^T], [-1, Q]], H = I + S;
+  * activation scale S = max(clip * max|x~|, 1e-5) / 7, stored as fp16
+    (saturating at 65504), codes = clamp(round_half_even(x~ / S_fp16), -8, 7);
+  * two codes per byte, even index in the low nibble, two's complement;
+  * dequant epilogue Y = fp16(fp32(fp32(acc) * sx_i) * sw_j);
+  * KV: head-wise H_128 without random signs, per-(token, head) symmetric INT4
+    with an fp16 scale; decode softmax in full precision, GQA head h reads KV
+    head h // (Hq / Hkv); output optionally rotated back by the same H_128.
+"""
+from __future__ import annotations
+
+import functools
+import math
+
+import numpy as np
+
+FP16_MAX = 65504.0
+SCALE_FLOOR = 1e-5  # abs-max floor of the guide's quantize_to_int4_symmetric
+QMIN, QMAX = -8, 7  # INT4 grid, [G] "The Collapse of Naive W4A4"
+
+
+# ---------------------------------------------------------------------------
+# Hadamard matrices ([G] Sylvester doubling; [S] Stage 1a Kronecker sizes;
+# [E] Paley-12 block)
+# ---------------------------------------------------------------------------
+@functools.lru_cache(maxsize=None)
+def sylvester(n: int) -> np.ndarray:
+    """Integer Sylvester Hadamard matrix of order n = 2^k: H_1 = [1],
+    H_2m = [[H_m, H_m], [H_m, -H_m]]."""
+    if n < 1 or n & (n - 1):
+        raise ValueError(f"Sylvester order must be a power of two, got {n}")
+    h = np.ones((1, 1), dtype=np.int8)
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    h.setflags(write=False)
+    return h
+
+
+def legendre(a: int, q: int) -> int:
+    """chi(a) for prime q: 0 if a = 0 mod q, +1 for a nonzero square, -1 otherwise."""
+    a %= q
+    if a == 0:
+        return 0
+    squares = {(x * x) % q for x in range(1, q)}
+    return 1 if a in squares else -1
+
+
+@functools.lru_cache(maxsize=None)
+def paley12() -> np.ndarray:
+    """Paley construction I of order q + 1 = 12 with q = 11 (q = 3 mod 4).
+
+    Jacobsthal matrix Q_ij = chi(j - i) (antisymmetric for q = 3 mod 4),
+    S = [[0, 1^T], [-1, Q]] and H = I + S.  Not symmetric.
+    """
+    q = 11
+    Q = np.array([[legendre(j - i, q) for j in range(q)] for i in range(q)], dtype=np.int8)
+    S = np.zeros((q + 1, q + 1), dtype=np.int8)
+    S[0, 1:] = 1
+    S[1:, 0] = -1
+    S[1:, 1:] = Q
+    H = (np.eye(q + 1, dtype=np.int8) + S).astype(np.int8)
+    H.setflags(write=False)
+    return H
+
+
+@functools.lru_cache(maxsize=4)
+def hadamard(d: int) -> np.ndarray:
+    """Dense integer (+-1) Hadamard matrix of order d, as int8 [d, d].
+
+    d = 2^n: Sylvester.  d = 12 * 2^n: H12 (Kronecker) H_{2^n}, entry
+    [(a, b), (c, e)] = H12[a, c] * H_{2^n}[b, e] with row/col index a*2^n + b.
+    """
+    if d >= 1 and d & (d - 1) == 0:
+        return sylvester(d)
+    if d % 12 == 0 and (d // 12) & (d // 12 - 1) == 0:
+        H = np.kron(paley12(), sylvester(d // 12)).astype(np.int8)
+        H.setflags(write=False)
+        return H
+    raise ValueError(f"no Hadamard construction for d = {d} (need 2^n or 12*2^n)")
+
+
+def _apply_dense(xs: np.ndarray, H: np.ndarray, block: int = 1024) -> np.ndarray:
+    """xs @ H in float64, with H's columns converted to float64 a block at a time
+    (bounds memory at d = 12288; the product itself is the plain dense one)."""
+    d = H.shape[0]
+    out = np.empty((xs.shape[0], d), dtype=np.float64)
+    for j0 in range(0, d, block):
+        out[:, j0:j0 + block] = xs @ H[:, j0:j0 + block].astype(np.float64)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Online rotation ([S] Stage 1a, 1b; [G] RHT section)
+# ---------------------------------------------------------------------------
+def rotate(x: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
+    """x~ = (x * s) @ H_d / sqrt(d) for each row, exact in float64, returned as fp32.
+
+    x: [..., d] (any float dtype, fp16 in the workloads).  signs: int8 [d] of
+    +-1, or None for the plain (unsigned) Hadamard used on K, V and q.
+    """
+    x = np.asarray(x)
+    d = x.shape[-1]
+    xs = x.reshape(-1, d).astype(np.float64)
+    if signs is not None:
+        xs = xs * np.asarray(signs, dtype=np.float64)[None, :]
+    r = _apply_dense(xs, hadamard(d)) / math.sqrt(d)
+    return r.astype(np.float32).reshape(x.shape)
+
+
+def rotate_f64(x: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
+    """Same map as ``rotate`` but left in float64 (for invariance checks)."""
+    x = np.asarray(x)
+    d = x.shape[-1]
+    xs = x.reshape(-1, d).astype(np.float64)
+    if signs is not None:
+        xs = xs * np.asarray(signs, dtype=np.float64)[None, :]
+    return (_apply_dense(xs, hadamard(d)) / math.sqrt(d)).reshape(x.shape)
+
+
+# ---------------------------------------------------------------------------
+# Symmetric INT4 quantizer ([S] Stage 2a/2b; [G] quantizer formula)
+# ---------------------------------------------------------------------------
+def quant_scale(absmax: np.ndarray, clip_ratio: float = 1.0) -> np.ndarray:
+    """Per-row scale S = max(clip * absmax, 1e-5) / 7, rounded to fp16 (saturating)."""
+    s = np.maximum(clip_ratio * np.asarray(absmax, dtype=np.float64), SCALE_FLOOR) / 7.0
+    return np.minimum(s, FP16_MAX).astype(np.float16)
+
+
+def round_half_even(y: np.ndarray) -> np.ndarray:
+    """Round to nearest, ties to even (numpy's rint is IEEE roundTiesToEven)."""
+    return np.rint(y)
+
+
+def quantize_rows(xr: np.ndarray, clip_ratio: float = 1.0):
+    """Per-row symmetric INT4: returns (codes int8 [..., d], scale fp16 [...]).
+
+    The codes are computed with the stored fp16 scale:
+    q = clamp(round_half_even(x~ / S), -8, 7), the division done in float64.
+    """
+    xr = np.asarray(xr, dtype=np.float32)
+    absmax = np.max(np.abs(xr), axis=-1)
+    S = quant_scale(absmax, clip_ratio)
+    y = xr.astype(np.float64) / S.astype(np.float64)[..., None]
+    q = np.clip(round_half_even(y), QMIN, QMAX).astype(np.int8)
+    return q, S
+
+
+def pack_int4(codes: np.ndarray) -> np.ndarray:
+    """Two codes per byte: byte i = (q[2i] & 0xF) | ((q[2i+1] & 0xF) << 4)."""
+    c = np.asarray(codes).astype(np.int16)
+    if c.shape[-1] % 2:
+        raise ValueError("last dimension must be even to pack two codes per byte")
+    lo = c[..., 0::2] & 0xF
+    hi = c[..., 1::2] & 0xF
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def unpack_int4(packed: np.ndarray) -> np.ndarray:
+    """Inverse of pack_int4: signed codes int8 [..., 2 * nbytes]."""
+    p = np.asarray(packed, dtype=np.uint8).astype(np.int16)
+    lo = p & 0xF
+    hi = (p >> 4) & 0xF
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def rotate_quant(x: np.ndarray, signs: np.ndarray | None, clip_ratio: float = 1.0):
+    """Rotation followed by per-row INT4 quantize-and-pack.
+
+    Returns (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d]).
+    Applied to activations online ([S] Stage 1b/2b) and to weight rows offline
+    for per-output-channel RTN ([S] Stage 2a; [G] "Offline Weight
+    Transformation": W~ = W H^T, one scale per output row).
+    """
+    r = rotate(x, signs)
+    q, S = quantize_rows(r, clip_ratio)
+    return pack_int4(q), S, r
+
+
+# ---------------------------------------------------------------------------
+# W4A4 GEMM + dequant epilogue ([S] Stage 2b "dequantization step",
+# "Kernel Implementation"; [G] "Pure INT4 Tensor Core GEMM Execution")
+# ---------------------------------------------------------------------------
+def int_gemm(a_codes: np.ndarray, w_codes: np.ndarray) -> np.ndarray:
+    """acc[i, j] = sum_k a[i, k] * w[j, k], exact integers (int64 result)."""
+    a = np.asarray(a_codes, dtype=np.int64)
+    w = np.asarray(w_codes, dtype=np.int64)
+    return a @ w.T
+
+
+def dequant(acc: np.ndarray, sx: np.ndarray, sw: np.ndarray) -> np.ndarray:
+    """Y = fp16(fp32(fp32(acc) * sx[i]) * sw[j]) -- exact integer to fp32, two
+    fp32 products, one rounding to fp16."""
+    acc = np.asarray(acc)
+    if np.max(np.abs(acc), initial=0) > 2 ** 24:
+        raise ValueError("accumulator outside the range fp32 holds exactly")
+    a32 = acc.astype(np.float32)
+    t = a32 * np.asarray(sx, dtype=np.float16).astype(np.float32)[:, None]
+    t = t * np.asarray(sw, dtype=np.float16).astype(np.float32)[None, :]
+    return t.astype(np.float16)
+
+
+def w4a4_gemm(a_packed, a_scale, w_packed, w_scale):
+    """Returns (acc int64 [M, N], y fp16 [M, N]) from packed operands."""
+    acc = int_gemm(unpack_int4(a_packed), unpack_int4(w_packed))
+    return acc, dequant(acc, a_scale, w_scale)
+
+
+# ---------------------------------------------------------------------------
+# Rotated INT4 KV cache ([S] Stage 1c/1d, Stage 2c "KV cache operation during
+# decoding", "Append"/"Decode" routines)
+# ---------------------------------------------------------------------------
+def kv_quant(kv: np.ndarray):
+    """Head-wise rotation x~ = x @ H_d / sqrt(d) (no signs) and per-(token, head)
+    symmetric INT4.  kv: fp16 [B, T, Hkv, d] -> (packed [B, Hkv, T, d/2], scale fp16 [B, Hkv, T])."""
+    kv = np.asarray(kv)
+    B, T, H, d = kv.shape
+    r = rotate(kv, None)  # [B, T, H, d] fp32
+    q, S = quantize_rows(r, 1.0)
+    packed = pack_int4(q)  # [B, T, H, d/2]
+    return np.ascontiguousarray(packed.transpose(0, 2, 1, 3)), np.ascontiguousarray(S.transpose(0, 2, 1))
+
+
+def kv_write(k, v, t_start, k_cache, k_scale, v_cache, v_scale):
+    """Append: quantize T_new tokens of K and V and store them at positions
+    t_start .. t_start + T_new - 1 of the caches (modified in place)."""
+    T_new = np.asarray(k).shape[1]
+    kq, ks = kv_quant(k)
+    vq, vs = kv_quant(v)
+    k_cache[:, :, t_start:t_start + T_new, :] = kq
+    k_scale[:, :, t_start:t_start + T_new] = ks
+    v_cache[:, :, t_start:t_start + T_new, :] = vq
+    v_scale[:, :, t_start:t_start + T_new] = vs
+
+
+def decode_attn(q, k_cache, k_scale, v_cache, v_scale, T: int, sm_scale: float | None = None,
+                unrotate: bool = False) -> np.ndarray:
+    """One-token GQA decode attention over the first T cached tokens, float64.
+
+    q: fp16 [B, Hq, d].  Caches [B, Hkv, T_max, d/2] uint8 and [B, Hkv, T_max] fp16.
+    q~ = q @ H / sqrt(d); for head h the KV head is g = h // (Hq / Hkv);
+    k^_t = Ks[t] * codes_t, s_t = sm_scale * (q~ . k^_t), p = softmax(s),
+    o = sum_t p_t * Vs[t] * vcodes_t; optionally o <- o @ H / sqrt(d).
+    Returns float64 [B, Hq, d].
+    """
+    q = np.asarray(q)
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    grp = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if sm_scale is None or sm_scale <= 0 else float(sm_scale)
+    qr = rotate_f64(q, None)  # [B, Hq, d]
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    if T == 0:
+        return out
+    for b in range(B):
+        for g in range(Hkv):
+            kd = unpack_int4(k_cache[b, g, :T]).astype(np.float64) * k_scale[b, g, :T].astype(np.float64)[:, None]
+            vd = unpack_int4(v_cache[b, g, :T]).astype(np.float64) * v_scale[b, g, :T].astype(np.float64)[:, None]
+            qs = qr[b, g * grp:(g + 1) * grp]  # [grp, d]
+            s = scale * (qs @ kd.T)  # [grp, T]
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p /= p.sum(axis=1, keepdims=True)
+            out[b, g * grp:(g + 1) * grp] = p @ vd
+    if unrotate:
+        out = rotate_f64(out, None)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Tolerance helpers for parity (the bars stated for the hot path)
+# ---------------------------------------------------------------------------
+def boundary_mask(xr: np.ndarray, scale: np.ndarray, eps: float = 1e-4) -> np.ndarray:
+    """True where |x~ / S| lies within eps of a .5 rounding boundary (codes may
+    legitimately differ there between two correct implementations)."""
+    y = np.abs(np.asarray(xr, dtype=np.float64) / np.asarray(scale, dtype=np.float16).astype(np.float64)[..., None])
+    frac = y - np.floor(y)
+    return np.abs(frac - 0.5) < eps
+
+
+def rotation_error(r_test: np.ndarray, r_ref: np.ndarray) -> float:
+    """max_j |r_test - r_ref| / max(|r_ref_j|, rms(row)), the relative bar for
+    rotated values floored at the row RMS."""
+    r_ref = np.asarray(r_ref, dtype=np.float64)
+    r_test = np.asarray(r_test, dtype=np.float64)
+    rms = np.sqrt(np.mean(r_ref ** 2, axis=-1, keepdims=True))
+    den = np.maximum(np.abs(r_ref), np.maximum(rms, 1e-30))
+    return float(np.max(np.abs(r_test - r_ref) / den)) if r_ref.size else 0.0
+
+
+def rel_fro(test: np.ndarray, ref: np.ndarray) -> float:
+    """||test - ref||_F / ||ref||_F in float64."""
+    ref = np.asarray(ref, dtype=np.float64)
+    test = np.asarray(test, dtype=np.float64)
+    n = np.linalg.norm(ref)
+    return float(np.linalg.norm(test - ref) / n) if n > 0 else float(np.linalg.norm(test))
