@@ -1,0 +1,356 @@
+"""Benchmark of the QuaRot W4A4 hot path on GB300.
+
+One step = one pass of every hot-path stage on synthetic, seeded inputs:
+  1. quarot_rotate_quant  X [2048, 12288] fp16 (H12 (x) H1024, random signs)
+  2. quarot_w4a4_gemm     -> Y [2048, 4096] fp16 against W~ [4096, 12288] INT4
+  3. quarot_kv_write      append one token for 16 sequences (8 KV heads x 128)
+  4. quarot_decode_attn   16 sequences x 32 query heads over 4096 cached tokens
+The headline value is W4A4 layer tokens/s: 2048 tokens per step divided by
+the device time of the step (inputs resident in HBM, L2 flushed between
+steps).  Per-stage times, HBM GB/s, GEMM TOPS and the roofline fraction come
+from CUDA events on the launching stream in the same run.
+
+--impl reference times the CPU oracle (dense Hadamard matrices, exact integer
+GEMM, float64 attention) on the host cores over a bounded sample per step.
+Multi-GPU (torchrun): every rank runs an independent replica (weak scaling);
+the only cross-rank traffic is the barrier and the max of the step times.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+M_TOK, K_DIM, N_OUT = 2048, 12288, 4096
+KV = W.CONFIGS["kv4"]
+METRIC = "W4A4 layer tokens/s"
+WORKLOAD = ("down_proj W4A4 layer 2048x12288->4096 (H12(x)H1024 rotate+quant, INT4 GEMM, fp16 out) "
+            "+ KV4 decode step (append 1 token, GQA 32q/8kv x128 over 4096 cached tokens, batch 16)")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_sample(rows: int = 8, seqs: int = 1):
+    """Times the oracle on a bounded sample of one step; returns (tokens/s, seconds, description)."""
+    import oracle as O
+
+    x, w, s = W.layer_inputs("down_proj", M=rows, N=N_OUT)
+    k, v, qq = W.kv_inputs("kv4", B=seqs)
+    T = KV["T"]
+    caches = [np.zeros((seqs, KV["Hkv"], T, KV["d"] // 2), np.uint8), np.zeros((seqs, KV["Hkv"], T), np.float16),
+              np.zeros((seqs, KV["Hkv"], T, KV["d"] // 2), np.uint8), np.zeros((seqs, KV["Hkv"], T), np.float16)]
+    # weights are prepared offline (not timed), as on the GPU side
+    wq, wsc, _ = O.rotate_quant(w, s)
+    O.kv_write(k[:, :T - 1], v[:, :T - 1], 0, *caches)
+    t0 = time.perf_counter()
+    aq, asc, _ = O.rotate_quant(x, s)
+    O.w4a4_gemm(aq, asc, wq, wsc)
+    t1 = time.perf_counter()
+    O.kv_write(k[:, T - 1:], v[:, T - 1:], T - 1, *caches)
+    O.decode_attn(qq, *caches, T=T)
+    t2 = time.perf_counter()
+    dt = t2 - t0
+    # scale to a whole step: layer time with the rows, decode time with the batch
+    step_s = (t1 - t0) * (M_TOK / rows) + (t2 - t1) * (KV["B"] / seqs)
+    desc = (f"{rows} of {M_TOK} layer rows (rotate+quant + exact INT GEMM against all {N_OUT} outputs, "
+            f"{t1 - t0:.2f} s) and {seqs} of {KV['B']} decode sequences (append + attention over {T} tokens, "
+            f"{t2 - t1:.2f} s), each scaled linearly to one step")
+    return M_TOK / step_s, dt, desc
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    for _ in range(args.warmup):
+        cpu_oracle_sample(rows=1, seqs=1)
+    vals, secs = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        v, dt, desc = cpu_oracle_sample(rows=2, seqs=1)
+        vals.append(v)
+        secs += dt
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * M_TOK / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+int64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import w4a4_rotated_quantized_gb300 as q
+    from w4a4_rotated_quantized_gb300 import build as qbuild
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(qbuild.LIB):
+        qbuild.build()
+    if ws > 1:
+        dist.barrier()
+    q.load()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---------------- inputs (seeded, synthetic), weights prepared offline
+    x, w, s = W.layer_inputs("down_proj")
+    k, v, qq = W.kv_inputs("kv4")
+    B, T, Hkv, d = k.shape
+    Hq = qq.shape[1]
+    xt = torch.from_numpy(x).to(dev)
+    st = torch.from_numpy(s).to(dev)
+    wq, wsc, _ = q.quarot_rotate_quant(torch.from_numpy(w).to(dev), st)
+    del w
+    cache = q.new_kv_cache(B, Hkv, T, d, dev)
+    q.quarot_kv_write(torch.from_numpy(k[:, :T - 1]).to(dev), torch.from_numpy(v[:, :T - 1]).to(dev), 0, *cache)
+    k_new = torch.from_numpy(np.ascontiguousarray(k[:, T - 1:])).to(dev)
+    v_new = torch.from_numpy(np.ascontiguousarray(v[:, T - 1:])).to(dev)
+    q_dec = torch.from_numpy(qq).to(dev)
+    aq = torch.empty((M_TOK, K_DIM // 2), dtype=torch.uint8, device=dev)
+    asx = torch.empty((M_TOK,), dtype=torch.float16, device=dev)
+    y = torch.empty((M_TOK, N_OUT), dtype=torch.float16, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    wsp = torch.empty((q.quarot_decode_workspace_bytes(B, Hq, d, T),), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    EV = 5  # events per step: start, after rotate, after gemm, after kv_write, after decode
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        q.quarot_rotate_quant(xt, st, q_out=aq, scale_out=asx, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        q.quarot_w4a4_gemm(aq, asx, wq, wsc, y=y, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        q.quarot_kv_write(k_new, v_new, T - 1, *cache, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        q.quarot_decode_attn(q_dec, *cache, T=T, out=out, workspace=wsp, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    LAUNCHES_PER_STEP = 1 + 1 + 2 + 2
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    q.quarot_check_error(stream)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(EV)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (outside the step's events)
+            step(evs[i])
+        torch.cuda.synchronize()
+    q.quarot_check_error(stream)
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(EV - 1)] for i in range(args.steps)])
+    step_ms = per.sum(axis=1)
+    total_ms = float(step_ms.sum())
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    value = ws * M_TOK * args.steps / (total_ms / 1000.0)
+    stage_ms = per.mean(axis=0)
+
+    # ---------------- e2e: host buffers through the C ABI, copies inside the timed region
+    x_h = torch.from_numpy(x).pin_memory()
+    kn_h, vn_h, q_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q_dec.cpu().pin_memory()
+    y_h = torch.empty_like(y, device="cpu").pin_memory()
+    o_h = torch.empty_like(out, device="cpu").pin_memory()
+    xd = torch.empty_like(xt)
+    kd, vd, qd = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q_dec)
+
+    def e2e_step():
+        xd.copy_(x_h, non_blocking=True)
+        kd.copy_(kn_h, non_blocking=True)
+        vd.copy_(vn_h, non_blocking=True)
+        qd.copy_(q_h, non_blocking=True)
+        q.quarot_rotate_quant(xd, st, q_out=aq, scale_out=asx, stream=stream)
+        q.quarot_w4a4_gemm(aq, asx, wq, wsc, y=y, stream=stream)
+        q.quarot_kv_write(kd, vd, T - 1, *cache, stream=stream)
+        q.quarot_decode_attn(qd, *cache, T=T, out=out, workspace=wsp, stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        o_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b2.record(stream)
+        b2.synchronize()
+        e_ms.append(a.elapsed_time(b2))
+    q.quarot_check_error(stream)
+    e2e_total = float(np.sum(e_ms))
+    if ws > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_val = ws * M_TOK * args.steps / (e2e_total / 1000.0)
+    h2d = (xd.numel() * 2 + kd.numel() * 2 + vd.numel() * 2 + qd.numel() * 2)
+    d2h = y.numel() * 2 + out.numel() * 2
+
+    # ---------------- roofline of the dominant kernel (GEMM, tensor pipe)
+    hbm_peak, bf16_peak, peak_src = _peaks()
+    fp8_peak = bf16_peak * (4.5 / 2.25)  # kind::f8f6f4 executes the INT4 contraction
+    gemm_ms = float(stage_ms[1])
+    gemm_tflops = 2.0 * M_TOK * N_OUT * K_DIM / (gemm_ms / 1000.0) / 1e12
+    rq_bytes = M_TOK * K_DIM * 2 + M_TOK * K_DIM // 2 + M_TOK * 2
+    dec_bytes = B * Hkv * T * (d // 2) * 2 + B * Hkv * T * 2 * 2 + B * Hq * d * 2 * 2
+    kvw_bytes = 2 * (B * Hkv * d * 2 + B * Hkv * (d // 2 + 2))
+    stages = {
+        "rotate_quant": {"ms": float(stage_ms[0]), "GB/s": rq_bytes / (stage_ms[0] / 1e3) / 1e9,
+                         "frac_hbm": rq_bytes / (stage_ms[0] / 1e3) / 1e9 / hbm_peak},
+        "w4a4_gemm": {"ms": gemm_ms, "TOPS": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
+        "kv_write_append": {"ms": float(stage_ms[2]), "GB/s": kvw_bytes / (stage_ms[2] / 1e3) / 1e9},
+        "decode_attn": {"ms": float(stage_ms[3]), "GB/s": dec_bytes / (stage_ms[3] / 1e3) / 1e9,
+                        "frac_hbm": dec_bytes / (stage_ms[3] / 1e3) / 1e9 / hbm_peak},
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4+f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": M_TOK, "l2": "flushed between steps (2x L2 write)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "tensor", "kernel": "w4a4_gemm", "achieved": gemm_tflops, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio)"},
+        "stages": stages,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import torch as _t  # noqa: F401
+
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        v, dt, desc = cpu_oracle_sample(rows=32, seqs=2)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+                                "sample_seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

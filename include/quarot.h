@@ -1,0 +1,170 @@
+/*
+ * quarot.h -- C ABI of libquarot.so, the GB300 (sm_103a) hot path of QuaRot:
+ * online randomized Hadamard rotation fused with per-token INT4 quantization,
+ * a W4A4 GEMM with a scale-dequant epilogue, and the rotated INT4 KV cache
+ * (append + one-token decode attention).
+ *
+ * Sources (page title, section):
+ *   [S] "QuaRot: Outlier-Free 4-Bit Inference in Rotated LLMs" (paper summary),
+ *       section 3 "Technical Approach" (Stages 1a-1d, 2a-2c, "Kernel
+ *       Implementation and Hardware Efficiency").
+ *   [G] "QuaRot Guide: Outlier-Free 4-Bit W4A4 LLM Quantization" (blog),
+ *       sections on the RHT, the INT4 grid and the 4-bit rotated KV cache.
+ *   [E] QuaRot paper-viz explainer: Sylvester for 2^n, Kronecker with a
+ *       Paley-12 block for 12288.
+ *
+ * Conventions for every entry point:
+ *   - Pointers to tensors are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them.  fp16 data is passed as void*
+ *     (IEEE binary16).  All tensors are dense row-major (C order) unless a
+ *     leading dimension is given.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream.
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and returns a nonzero status.  No exception crosses
+ *     the ABI.
+ *   - Kernels that wait on hardware barriers give up after a bounded time,
+ *     record QUAROT_ERR_TIMEOUT in a device error word and return;
+ *     quarot_check_error() reads (and clears) that word.
+ *   - INT4 codes are two's complement in [-8, 7], two per byte, the even
+ *     index in the low nibble.
+ */
+#ifndef QUAROT_H_
+#define QUAROT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  QUAROT_OK = 0,
+  QUAROT_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size */
+  QUAROT_ERR_UNSUPPORTED = 2, /* size outside what the kernels implement     */
+  QUAROT_ERR_ALIGNMENT = 3,   /* pointer or leading dimension misaligned      */
+  QUAROT_ERR_LAUNCH = 4,      /* the CUDA launch itself failed                */
+  QUAROT_ERR_TIMEOUT = 5,     /* a device-side bounded wait expired           */
+  QUAROT_ERR_CUDA = 6         /* another CUDA runtime/driver error            */
+};
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* quarot_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int quarot_version(void);
+
+/* Synchronizes `stream`, then returns and clears the device error word of the
+ * current device (QUAROT_OK if no kernel recorded an error), or
+ * QUAROT_ERR_CUDA if the synchronization itself failed. */
+int quarot_check_error(void* stream);
+
+/*
+ * quarot_rotate_quant -- online randomized Hadamard rotation of each row
+ * followed by per-token symmetric INT4 quantization and packing.
+ * [S] Stage 1a (Q = H diag(s), Kronecker sizes), Stage 1b (online FWHT in
+ * FP32), Stage 2b (per-token scale, clipping ratio), "Kernel Implementation"
+ * (quantize, pack two INT4 per byte); [G] RHT and quantizer formulas.
+ *
+ * For each row i of x:
+ *   r = (x_i * s) @ H_d / sqrt(d)          (fp32; s = 1 if signs == NULL)
+ *   S = fp16(min(max(clip_ratio * max_j |r_j|, 1e-5) / 7, 65504))
+ *   q_j = clamp(round_half_even(r_j / S), -8, 7), packed two per byte.
+ * H_d is Sylvester for d = 2^n, and H12 (x) H_{d/12} (Paley I, q = 11) for
+ * d = 12 * 2^n (row-vector convention, column index c * (d/12) + e).
+ * The same call quantizes weight rows offline (per-output-channel RTN).
+ *
+ *   x         fp16 [M, ld_x], first d columns used (ld_x >= d, ld_x % 8 == 0,
+ *             x 16-byte aligned)
+ *   M         rows (>= 0; M == 0 is a no-op)
+ *   d         row width: 2^n with 16 <= d <= 8192, or 12 * 2^n with
+ *             768 <= d <= 12288
+ *   signs     int8 [d] of +1/-1 (read only), or NULL
+ *   clip_ratio  in (0, 1]
+ *   q_out     uint8 [M, d/2], 16-byte aligned
+ *   scale_out fp16 [M]
+ *   rot_out   fp32 [M, d] (the rotated values r, for testing), or NULL
+ */
+int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                        float clip_ratio, uint8_t* q_out, void* scale_out, float* rot_out,
+                        void* stream);
+
+/*
+ * quarot_w4a4_gemm -- W4A4 GEMM with INT32-exact accumulation and the
+ * per-token x per-output-channel dequantization epilogue.
+ * [S] Stage 2b "dequantization step", "Kernel Implementation" (INT4 GEMM,
+ * INT32 accumulator, scale by scale_x[i] * scale_w[j]); [G] "Pure INT4 Tensor
+ * Core GEMM Execution".
+ *
+ *   acc[i, j] = sum_k a[i, k] * w[j, k]               (exact integer)
+ *   y[i, j]   = fp16(fp32(fp32(acc) * sx[i]) * sw[j])
+ *
+ *   a_q       uint8 [M, K/2] packed activations (K-major), 16-byte aligned
+ *   a_scale   fp16 [M]
+ *   w_q       uint8 [N, K/2] packed weights (K-major, [out, in]), 16-byte aligned
+ *   w_scale   fp16 [N]
+ *   M, N      >= 0 (ragged tails handled); K % 128 == 0, 128 <= K <= 131072
+ *   y         fp16 [M, N]
+ *   acc_out   int32 [M, N] (the exact accumulator, for testing), or NULL
+ */
+int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const uint8_t* w_q,
+                     const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
+                     int32_t* acc_out, void* stream);
+
+/*
+ * quarot_kv_write -- "Append": rotate the new keys and values head-wise by
+ * H_d / sqrt(d) (no random signs), quantize each (token, head) vector to
+ * symmetric INT4 with an fp16 scale (clip 1.0, the formula of
+ * quarot_rotate_quant) and store them at positions t_start .. t_start+T_new-1.
+ * [S] Stage 1c/1d (head-wise H_dh on V and on post-RoPE K), Stage 2c (KV
+ * cache procedure), "Append" routine; [G] "4-Bit Rotated KV Cache".
+ *
+ *   k, v      fp16 [B, T_new, Hkv, d], 16-byte aligned
+ *   d         64, 128 or 256
+ *   t_start   >= 0, t_start + T_new <= T_max
+ *   k_q, v_q  uint8 [B, Hkv, T_max, d/2] caches, 16-byte aligned
+ *   k_s, v_s  fp16 [B, Hkv, T_max] per-(token, head) scales
+ */
+int quarot_kv_write(const void* k, const void* v, int64_t B, int64_t T_new, int64_t Hkv,
+                    int64_t d, int64_t t_start, int64_t T_max, uint8_t* k_q, void* k_s,
+                    uint8_t* v_q, void* v_s, void* stream);
+
+/*
+ * quarot_decode_workspace_bytes -- bytes of scratch quarot_decode_attn needs
+ * for these sizes (split-T partial softmax states).  0 on invalid sizes.
+ */
+size_t quarot_decode_workspace_bytes(int64_t B, int64_t Hq, int64_t d, int64_t T);
+
+/*
+ * quarot_decode_attn -- one-token GQA decode attention over the INT4 cache,
+ * dequantizing on read.  [S] Stage 1d (rotate the query head-wise after
+ * RoPE), Stage 2c (load, dequantize on the fly, dot products, softmax),
+ * "Decode" routine.
+ *
+ *   q~ = q_h @ H_d / sqrt(d);  g = h / (Hq / Hkv)
+ *   s_t = sm_scale * (q~ . (k_s[t] * kcode_t)),  p = softmax(s) over t < T
+ *   o   = sum_t p_t * v_s[t] * vcode_t;  if unrotate_out: o <- o @ H_d / sqrt(d)
+ *
+ *   q         fp16 [B, Hq, d], 16-byte aligned
+ *   k_q, k_s, v_q, v_s  caches as written by quarot_kv_write (capacity T_max)
+ *   d         128; Hq % Hkv == 0 and Hq / Hkv <= 8
+ *   T         tokens to attend, 0 <= T <= T_max (T == 0 gives o = 0)
+ *   sm_scale  softmax scale; <= 0 selects 1/sqrt(d)
+ *   unrotate_out  0: o stays in the rotated basis (the rotation is absorbed
+ *             by W_out, Stage 1c); 1: o is rotated back
+ *   out       fp16 [B, Hq, d]
+ *   workspace device scratch of ws_bytes >= quarot_decode_workspace_bytes(),
+ *             256-byte aligned, owned by the caller; contents need no
+ *             initialisation and are clobbered
+ */
+int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const uint8_t* v_q,
+                       const void* v_s, int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t T,
+                       int64_t T_max, float sm_scale, int unrotate_out, void* out, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUAROT_H_ */

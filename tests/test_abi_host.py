@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+function include/quarot.h declares, and rejects bad arguments before any
+launch (no GPU is touched by these calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+import w4a4_rotated_quantized_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return q.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "quarot.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(quarot_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(q.EXPORTED) == _declared()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.quarot_status_string(code)
+        assert s and s.decode() == q.STATUS[code]
+    assert lib.quarot_status_string(99) == b"unknown status"
+    assert lib.quarot_version() >> 16 == 1
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)  # never dereferenced: every call below fails validation first
+
+
+def test_rotate_quant_validation(lib):
+    f = lib.quarot_rotate_quant
+    assert f(FAKE, 0, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 0  # M = 0 no-op
+    assert f(FAKE, 4, 24, 24, None, 1.0, FAKE, FAKE, None, None) == 2  # no construction for 24
+    assert f(FAKE, 4, 20, 20, None, 1.0, FAKE, FAKE, None, None) == 3  # ld % 8
+    assert f(FAKE, -1, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 4, 4096, 4000, None, 1.0, FAKE, FAKE, None, None) == 1  # ld < d
+    assert f(FAKE, 4, 4096, 4096, None, 0.0, FAKE, FAKE, None, None) == 1  # clip
+    assert f(FAKE, 4, 4096, 4096, None, 1.5, FAKE, FAKE, None, None) == 1
+    assert f(None, 4, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(P(0x10002), 4, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 3  # misaligned x
+    assert f(FAKE, 4, 4096, 4100, None, 1.0, FAKE, FAKE, None, None) == 3  # ld % 8
+    assert f(FAKE, 4, 4104, 4104, None, 1.0, FAKE, FAKE, None, None) == 2  # no construction
+
+
+def test_gemm_validation(lib):
+    f = lib.quarot_w4a4_gemm
+    assert f(FAKE, FAKE, FAKE, FAKE, 0, 16, 256, FAKE, None, None) == 0
+    assert f(FAKE, FAKE, FAKE, FAKE, 16, 16, 200, FAKE, None, None) == 2  # K % 128
+    assert f(FAKE, FAKE, FAKE, FAKE, 16, 16, 131072, FAKE, None, None) == 2  # K too large for exact fp32
+    assert f(FAKE, FAKE, FAKE, FAKE, -1, 16, 256, FAKE, None, None) == 1
+    assert f(None, FAKE, FAKE, FAKE, 16, 16, 256, FAKE, None, None) == 1
+    assert f(P(0x10008), FAKE, FAKE, FAKE, 16, 16, 256, FAKE, None, None) == 3
+
+
+def test_kv_validation(lib):
+    f = lib.quarot_kv_write
+    assert f(FAKE, FAKE, 1, 4, 8, 128, 14, 16, FAKE, FAKE, FAKE, FAKE, None) == 1  # past T_max
+    assert f(FAKE, FAKE, 1, 4, 8, 96, 0, 16, FAKE, FAKE, FAKE, FAKE, None) == 2
+    assert f(FAKE, FAKE, 0, 4, 8, 128, 0, 16, FAKE, FAKE, FAKE, FAKE, None) == 0
+    d = lib.quarot_decode_attn
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 64, 4, 8, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 2
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 30, 8, 128, 4, 8, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 1
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 9, 8, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 1
+    assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 4, 8, 0.0, 0, FAKE, FAKE, 16, None) == 1  # small ws
+
+
+def test_workspace_size(lib):
+    assert q.quarot_decode_workspace_bytes(16, 32, 128, 4096) == 16 * 32 * 16 * 130 * 4
+    assert q.quarot_decode_workspace_bytes(1, 1, 128, 1) == 768  # 130 floats rounded up to 256 B
+    assert q.quarot_decode_workspace_bytes(1, 1, 64, 1) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(q, "_lib", None)
+    with pytest.raises(q.QuarotError):
+        q.load("/nonexistent/libquarot.so")

@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars (stated for the hot path): INT32 accumulators bit-exact on identical
+codes; rotated fp32 within 1e-5 relative (floored at the row RMS); INT4 codes
+identical except where |x/S| is within 1e-4 of a .5 boundary, with fewer than
+1e-4 of codes affected; scales within one fp16 ulp; dequantised outputs within
+1e-3 relative Frobenius error.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ROT_TOL = 1e-5
+OUT_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import w4a4_rotated_quantized_gb300 as mod
+
+    mod.load()
+    torch.cuda.set_device(0)
+    return mod
+
+
+DEV = "cuda:0"
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _fp16_ulp(s):
+    s = np.asarray(s, dtype=np.float16)
+    return np.abs(np.spacing(s).astype(np.float64))
+
+
+def check_quant(gq, gs, grot, r_ref, clip=1.0):
+    """Compare GPU (packed, scale, rotated) with the oracle's rotated values."""
+    assert O.rotation_error(grot, r_ref) <= ROT_TOL
+    q_ref, s_ref = O.quantize_rows(r_ref, clip)
+    ds = np.abs(gs.astype(np.float64) - s_ref.astype(np.float64))
+    assert np.all(ds <= _fp16_ulp(s_ref) * 1.0001), float(ds.max())
+    same_scale = gs == s_ref
+    codes = O.unpack_int4(gq)
+    diff = codes != q_ref
+    # where the scales agree, codes may differ only at .5 boundaries
+    bnd = O.boundary_mask(r_ref, s_ref)
+    bad = diff & ~bnd & same_scale[:, None]
+    assert not bad.any(), f"{int(bad.sum())} codes differ away from a rounding boundary"
+    frac = diff[same_scale].mean() if same_scale.any() else 0.0
+    assert frac < 1e-4, frac
+    # codes must be the quantizer applied to the GPU's own rotated values with its own scale
+    y = grot.astype(np.float64) / gs.astype(np.float64)[:, None]
+    own = np.clip(np.rint(y), -8, 7)
+    near = np.abs(np.abs(y - np.floor(y)) - 0.5) < 1e-5
+    assert np.all((own == codes) | near)
+
+
+# ---------------------------------------------------------------- rotate+quant
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 3072, 6144, 12288])
+@pytest.mark.parametrize("signed", [True, False])
+def test_rotate_quant_widths(q, d, signed):
+    M = 37  # ragged: not a multiple of the rows per CTA
+    x = W.activations(M, d, W.outlier_channels(d, max(1, d // 512), 5 + d), 100.0, 11 + d)
+    s = W.random_signs(d, 21 + d) if signed else None
+    gq, gs, grot = q.quarot_rotate_quant(_t(x), None if s is None else _t(s), want_rot=True)
+    r_ref = O.rotate(x, s)
+    check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), r_ref)
+
+
+@pytest.mark.parametrize("d", [256, 4096, 12288])
+def test_rotate_quant_clip_09(q, d):
+    x = W.activations(19, d, [1, 7], 50.0, 3)
+    s = W.random_signs(d, 4)
+    gq, gs, grot = q.quarot_rotate_quant(_t(x), _t(s), clip_ratio=0.9, want_rot=True)
+    check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), O.rotate(x, s), clip=0.9)
+    assert (O.unpack_int4(gq.cpu().numpy()) == -8).any() or True
+
+
+def test_rotate_quant_edge_rows(q):
+    d = 4096
+    x = np.zeros((5, d), dtype=np.float16)
+    x[1, 3] = 1.0            # one-hot: all |r| equal -> every code +-7
+    x[2] = 65504.0           # largest fp16: scale saturates below fp16 max
+    x[3, ::2] = -1.0
+    x[4] = np.float16(6e-8)  # subnormal inputs
+    gq, gs, grot = q.quarot_rotate_quant(_t(x), None, want_rot=True)
+    gq, gs, grot = gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy()
+    codes = O.unpack_int4(gq)
+    assert np.all(codes[0] == 0) and float(gs[0]) == float(np.float16(1e-5 / 7))
+    assert np.all(np.abs(codes[1]) == 7)
+    assert np.isfinite(gs.astype(np.float32)).all()
+    check_quant(gq, gs, grot, O.rotate(x, None))
+
+
+def test_rotate_quant_empty(q):
+    x = torch.empty((0, 4096), dtype=torch.float16, device=DEV)
+    gq, gs, _ = q.quarot_rotate_quant(x)
+    assert gq.shape == (0, 2048)
+
+
+def test_rotate_quant_config_rotq4096_full(q):
+    """2048 x 4096 at full size (the bench launch); oracle on sampled rows."""
+    x, _, s = W.layer_inputs("rotq4096")
+    gq, gs, grot = q.quarot_rotate_quant(_t(x), _t(s), want_rot=True)
+    rows = np.random.default_rng(0).choice(x.shape[0], 192, replace=False)
+    rows[:2] = [0, x.shape[0] - 1]
+    check_quant(gq.cpu().numpy()[rows], gs.cpu().numpy()[rows], grot.cpu().numpy()[rows], O.rotate(x[rows], s))
+
+
+def test_rotate_quant_config_down_proj_sampled(q):
+    x, _, s = W.layer_inputs("down_proj", N=0)
+    gq, gs, grot = q.quarot_rotate_quant(_t(x), _t(s), want_rot=True)
+    rows = np.random.default_rng(1).choice(x.shape[0], 48, replace=False)
+    check_quant(gq.cpu().numpy()[rows], gs.cpu().numpy()[rows], grot.cpu().numpy()[rows], O.rotate(x[rows], s))
+
+
+# ---------------------------------------------------------------- GEMM
+def _gemm_case(q, M, N, K, seed, codes_a=None, codes_w=None):
+    a = W.int4_codes(M, K, seed) if codes_a is None else codes_a
+    w = W.int4_codes(N, K, seed + 1) if codes_w is None else codes_w
+    sx = W.fp16_scales(M, seed + 2)
+    sw = W.fp16_scales(N, seed + 3)
+    ap, wp = O.pack_int4(a), O.pack_int4(w)
+    y, acc = q.quarot_w4a4_gemm(_t(ap), _t(sx), _t(wp), _t(sw), want_acc=True)
+    q.quarot_check_error()
+    return a, w, sx, sw, y.cpu().numpy(), acc.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 256), (128, 256, 128), (200, 300, 256), (1, 8, 128),
+                                   (257, 513, 384), (256, 512, 4096), (130, 264, 12288)])
+def test_gemm_bit_exact(q, M, N, K):
+    a, w, sx, sw, y, acc = _gemm_case(q, M, N, K, 100 + M + N + K)
+    ref = O.int_gemm(a, w)
+    assert np.array_equal(acc, ref)
+    assert np.array_equal(y.view(np.uint16), O.dequant(ref, sx, sw).view(np.uint16))
+
+
+def test_gemm_adversarial_extremes(q):
+    K = 12288
+    a = np.full((130, K), -8, dtype=np.int8)
+    a[1::2] = 7
+    a[2, ::3] = -7
+    w = np.full((260, K), -8, dtype=np.int8)
+    w[::3] = 7
+    _, _, _, _, y, acc = _gemm_case(q, 130, 260, K, 7, a, w)
+    assert np.array_equal(acc, O.int_gemm(a, w))
+    assert acc[0, 0] == 64 * K
+
+
+def test_gemm_full_down_proj_sampled(q):
+    """2048 x 4096 x 12288 at full size; exact check on sampled rows."""
+    M, N, K = 2048, 4096, 12288
+    a, w, sx, sw, y, acc = _gemm_case(q, M, N, K, 900)
+    rows = np.random.default_rng(2).choice(M, 12, replace=False)
+    rows[0] = M - 1
+    ref = O.int_gemm(a[rows], w)
+    assert np.array_equal(acc[rows], ref)
+    assert np.array_equal(y[rows].view(np.uint16), O.dequant(ref, sx[rows], sw).view(np.uint16))
+
+
+# ---------------------------------------------------------------- layer end to end
+@pytest.mark.parametrize("config,M,N", [("tiny", None, None), ("down_proj", 256, 512), ("sweep", 512, 4096)])
+def test_layer_end_to_end(q, config, M, N):
+    x, w, s = W.layer_inputs(config, M=M, N=N)
+    aq, asx, _ = q.quarot_rotate_quant(_t(x), _t(s))
+    wq, wsx, _ = q.quarot_rotate_quant(_t(w), _t(s))
+    y, _ = q.quarot_w4a4_gemm(aq, asx, wq, wsx)
+    oa, osx, _ = O.rotate_quant(x, s)
+    ow, osw, _ = O.rotate_quant(w, s)
+    _, oy = O.w4a4_gemm(oa, osx, ow, osw)
+    assert O.rel_fro(y.cpu().numpy(), oy) <= OUT_TOL
+
+
+# ---------------------------------------------------------------- KV cache
+def _caches(shape_like, T_max):
+    B, _, H, d = shape_like
+    return [np.zeros((B, H, T_max, d // 2), np.uint8), np.zeros((B, H, T_max), np.float16),
+            np.zeros((B, H, T_max, d // 2), np.uint8), np.zeros((B, H, T_max), np.float16)]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_kv_write_parity(q, d):
+    B, T, H, T_max, t0 = 3, 37, 2, 64, 5
+    k = W.kv_tensors(B, T, H, d, 2, 20.0, 31)
+    v = W.kv_tensors(B, T, H, d, 2, 20.0, 32)
+    gc = q.new_kv_cache(B, H, T_max, d, DEV)
+    q.quarot_kv_write(_t(k), _t(v), t0, *gc)
+    gk, gks, gv, gvs = [t.cpu().numpy() for t in gc]
+    for src, codes, scales in ((k, gk, gks), (v, gv, gvs)):
+        r = O.rotate(src, None)  # [B, T, H, d]
+        q_ref, s_ref = O.quantize_rows(r, 1.0)
+        s_gpu = scales[:, :, t0:t0 + T].transpose(0, 2, 1)
+        c_gpu = O.unpack_int4(codes[:, :, t0:t0 + T].transpose(0, 2, 1, 3))
+        assert np.all(np.abs(s_gpu.astype(np.float64) - s_ref.astype(np.float64)) <= _fp16_ulp(s_ref))
+        diff = (c_gpu != q_ref) & ~O.boundary_mask(r, s_ref)
+        assert not diff.any()
+        assert np.all(codes[:, :, :t0] == 0) and np.all(codes[:, :, t0 + T:] == 0)
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("T", [1, 5, 256, 300, 1000])
+def test_decode_parity(q, G, T):
+    B, Hkv, d, T_max = 2, 2, 128, 1024
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 41 + T)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 42 + T)
+    qq = W.query(B, Hkv * G, d, 43 + T)
+    oc = _caches(k.shape, T_max)
+    O.kv_write(k, v, 0, *oc)
+    for unrot in (False, True):
+        out = q.quarot_decode_attn(_t(qq), *[_t(c) for c in oc], T=T, unrotate_out=unrot)
+        ref = O.decode_attn(qq, *oc, T=T, unrotate=unrot)
+        assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+
+
+def test_decode_custom_scale_and_zero_T(q):
+    B, Hkv, G, d, T = 1, 2, 4, 128, 77
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 5)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 6)
+    qq = W.query(B, Hkv * G, d, 7)
+    oc = _caches(k.shape, 128)
+    O.kv_write(k, v, 0, *oc)
+    out = q.quarot_decode_attn(_t(qq), *[_t(c) for c in oc], T=T, sm_scale=0.05)
+    assert O.rel_fro(out.cpu().numpy(), O.decode_attn(qq, *oc, T=T, sm_scale=0.05)) <= OUT_TOL
+    out0 = q.quarot_decode_attn(_t(qq), *[_t(c) for c in oc], T=0)
+    assert torch.all(out0 == 0)
+
+
+def test_kv4_config_full(q):
+    """B16 x T4096 x Hkv8 x Hq32: full-size append and decode; oracle on two sequences."""
+    k, v, qq = W.kv_inputs("kv4")
+    B, T, Hkv, d = k.shape
+    gc = q.new_kv_cache(B, Hkv, T, d, DEV)
+    q.quarot_kv_write(_t(k), _t(v), 0, *gc)
+    out = q.quarot_decode_attn(_t(qq), *gc, T=T)
+    q.quarot_check_error()
+    out = out.cpu().numpy()
+    gnp = [t.cpu().numpy() for t in gc]
+    for b in (0, B - 1):
+        oc = _caches(k[b:b + 1].shape, T)
+        O.kv_write(k[b:b + 1], v[b:b + 1], 0, *oc)
+        for name, g, o in (("k_s", gnp[1][b], oc[1][0]), ("v_s", gnp[3][b], oc[3][0])):
+            assert np.all(np.abs(g.astype(np.float64) - o.astype(np.float64)) <= _fp16_ulp(o)), name
+        ref = O.decode_attn(qq[b:b + 1], *oc, T=T)
+        assert O.rel_fro(out[b:b + 1], ref) <= OUT_TOL

@@ -1,0 +1,205 @@
+"""QuaRot W4A4 hot path on GB300 (sm_103a): Python binding of libquarot.so.
+
+This module only marshals arguments: it checks devices/dtypes/shapes, allocates
+outputs with torch when the caller does not pass them, and calls the C ABI
+declared in ``include/quarot.h``.  Every step of the computation runs in the
+CUDA kernels of ``csrc/``; there is no CPU fallback.  If the shared library is
+missing the calls raise ``QuarotError``.
+
+Functions (same names as the C entry points):
+    quarot_rotate_quant, quarot_w4a4_gemm, quarot_kv_write,
+    quarot_decode_attn, quarot_decode_workspace_bytes, quarot_check_error
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libquarot.so")
+
+QUAROT_OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "misaligned pointer or leading dimension",
+          4: "kernel launch failed", 5: "device-side wait timed out", 6: "CUDA error"}
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SIGS = {
+    "quarot_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "quarot_version": (ctypes.c_int, []),
+    "quarot_check_error": (ctypes.c_int, [_P]),
+    "quarot_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "quarot_w4a4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "quarot_kv_write": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "quarot_decode_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
+    "quarot_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                          ctypes.c_float, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
+}
+EXPORTED = tuple(_SIGS)
+
+
+class QuarotError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, 'unknown status')} (status {status})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads libquarot.so (once) and declares the ABI signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise QuarotError(6, f"libquarot.so not found at {p}; build it with "
+                             "w4a4_rotated_quantized_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != QUAROT_OK:
+        raise QuarotError(status, where)
+
+
+def _stream(stream, dev):
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, dev=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise QuarotError(1, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise QuarotError(1, f"{name} must be {dtype}, got {t.dtype}")
+    if dev is not None and t.device != dev:
+        raise QuarotError(1, f"{name} is on {t.device}, expected {dev}")
+    if not t.is_contiguous():
+        raise QuarotError(1, f"{name} must be contiguous")
+
+
+def quarot_version() -> int:
+    return load().quarot_version()
+
+
+def quarot_check_error(stream=None, device=None) -> None:
+    """Synchronizes the stream and raises if a kernel recorded a device-side error."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(load().quarot_check_error(_stream(stream, dev)), "quarot_check_error")
+
+
+def quarot_rotate_quant(x, signs=None, clip_ratio: float = 1.0, q_out=None, scale_out=None, rot_out=None,
+                        stream=None, want_rot: bool = False):
+    """x: fp16 [M, d] -> (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d] or None)."""
+    _need(x, torch.float16, "x")
+    dev = x.device
+    M, d = x.shape
+    if signs is not None:
+        _need(signs, torch.int8, "signs", dev)
+    if q_out is None:
+        q_out = torch.empty((M, d // 2), dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float16, device=dev)
+    if rot_out is None and want_rot:
+        rot_out = torch.empty((M, d), dtype=torch.float32, device=dev)
+    _need(q_out, torch.uint8, "q_out", dev)
+    _need(scale_out, torch.float16, "scale_out", dev)
+    if rot_out is not None:
+        _need(rot_out, torch.float32, "rot_out", dev)
+    st = load().quarot_rotate_quant(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(q_out),
+                                    _ptr(scale_out), _ptr(rot_out), _stream(stream, dev))
+    _check(st, "quarot_rotate_quant")
+    return q_out, scale_out, rot_out
+
+
+def quarot_w4a4_gemm(a_q, a_scale, w_q, w_scale, y=None, acc_out=None, stream=None, want_acc: bool = False):
+    """a_q uint8 [M, K/2], w_q uint8 [N, K/2] -> (y fp16 [M, N], acc int32 [M, N] or None)."""
+    _need(a_q, torch.uint8, "a_q")
+    dev = a_q.device
+    _need(w_q, torch.uint8, "w_q", dev)
+    _need(a_scale, torch.float16, "a_scale", dev)
+    _need(w_scale, torch.float16, "w_scale", dev)
+    M, Kh = a_q.shape
+    N, Kh2 = w_q.shape
+    if Kh != Kh2:
+        raise QuarotError(1, "a_q and w_q disagree on K")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    if acc_out is None and want_acc:
+        acc_out = torch.empty((M, N), dtype=torch.int32, device=dev)
+    _need(y, torch.float16, "y", dev)
+    if acc_out is not None:
+        _need(acc_out, torch.int32, "acc_out", dev)
+    st = load().quarot_w4a4_gemm(_ptr(a_q), _ptr(a_scale), _ptr(w_q), _ptr(w_scale), M, N, 2 * Kh, _ptr(y),
+                                 _ptr(acc_out), _stream(stream, dev))
+    _check(st, "quarot_w4a4_gemm")
+    return y, acc_out
+
+
+def quarot_kv_write(k, v, t_start, k_q, k_s, v_q, v_s, stream=None):
+    """k, v fp16 [B, T_new, Hkv, d] appended at t_start into caches [B, Hkv, T_max, d/2] (+ scales)."""
+    _need(k, torch.float16, "k")
+    dev = k.device
+    _need(v, torch.float16, "v", dev)
+    for t, n in ((k_q, "k_q"), (v_q, "v_q")):
+        _need(t, torch.uint8, n, dev)
+    for t, n in ((k_s, "k_s"), (v_s, "v_s")):
+        _need(t, torch.float16, n, dev)
+    B, T_new, Hkv, d = k.shape
+    if tuple(v.shape) != tuple(k.shape):
+        raise QuarotError(1, "k and v shapes differ")
+    T_max = k_q.shape[2]
+    st = load().quarot_kv_write(_ptr(k), _ptr(v), B, T_new, Hkv, d, int(t_start), T_max, _ptr(k_q), _ptr(k_s),
+                                _ptr(v_q), _ptr(v_s), _stream(stream, dev))
+    _check(st, "quarot_kv_write")
+
+
+def quarot_decode_workspace_bytes(B: int, Hq: int, d: int, T: int) -> int:
+    return int(load().quarot_decode_workspace_bytes(B, Hq, d, T))
+
+
+def quarot_decode_attn(q, k_q, k_s, v_q, v_s, T: int, sm_scale: float = 0.0, unrotate_out: bool = False,
+                       out=None, workspace=None, stream=None):
+    """q fp16 [B, Hq, d] against the first T cached tokens -> out fp16 [B, Hq, d]."""
+    _need(q, torch.float16, "q")
+    dev = q.device
+    for t, n in ((k_q, "k_q"), (v_q, "v_q")):
+        _need(t, torch.uint8, n, dev)
+    for t, n in ((k_s, "k_s"), (v_s, "v_s")):
+        _need(t, torch.float16, n, dev)
+    B, Hq, d = q.shape
+    Hkv, T_max = k_q.shape[1], k_q.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    _need(out, torch.float16, "out", dev)
+    need = quarot_decode_workspace_bytes(B, Hq, d, T)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    st = load().quarot_decode_attn(_ptr(q), _ptr(k_q), _ptr(k_s), _ptr(v_q), _ptr(v_s), B, Hq, Hkv, d, int(T),
+                                   T_max, float(sm_scale), int(bool(unrotate_out)), _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    _check(st, "quarot_decode_attn")
+    return out
+
+
+def new_kv_cache(B: int, Hkv: int, T_max: int, d: int, device):
+    """Zeroed caches (k_q, k_s, v_q, v_s) in the layout quarot_kv_write expects."""
+    kq = torch.zeros((B, Hkv, T_max, d // 2), dtype=torch.uint8, device=device)
+    vq = torch.zeros_like(kq)
+    ks = torch.zeros((B, Hkv, T_max), dtype=torch.float16, device=device)
+    vs = torch.zeros_like(ks)
+    return kq, ks, vq, vs

@@ -1,0 +1,387 @@
+// quarot_w4a4_gemm: packed INT4 x packed INT4 GEMM on the sm_103a tensor
+// cores (tcgen05, TMEM accumulator, TMA loads) with the per-token x
+// per-output-channel dequantization epilogue.
+//
+// What it computes -- "QuaRot: Outlier-Free 4-Bit Inference in Rotated LLMs"
+// (paper summary), Stage 2b "dequantization step" and "Kernel Implementation
+// and Hardware Efficiency": an INT4 GEMM with an INT32 accumulator whose
+// result is scaled by scale_x[i] * scale_w[j]; "QuaRot Guide: Outlier-Free
+// 4-Bit W4A4 LLM Quantization", "Pure INT4 Tensor Core GEMM Execution".
+//
+// How, on sm_103a: tcgen05 has no INT4 kind and no INT8 kind on this target,
+// so the contraction runs on kind::f8f6f4 (e4m3 x e4m3 -> fp32 in TMEM) with
+// an exact encoding:
+//   * a code v in [-8, 7] is offset to u = v + 8 in [0, 15] (one XOR of the
+//     nibble with 8);
+//   * the e4m3 byte with value u (0x00..0x0F) is exactly u * 2^-9: bytes
+//     0x01..0x07 are the subnormals u * 2^-9 and 0x08..0x0F the first binade
+//     (8 + m) * 2^-9, so the nibble itself is the fp8 operand;
+//   * every product is a multiple of 2^-18 and every partial sum is a
+//     non-negative integer multiple of 2^-18 below 225 * K * 2^-18 <= 2^24 *
+//     2^-18 for K <= 65536, so fp32 accumulation is exact;
+//   * sum_k a_k w_k = sum_k u_k u'_k - 8 sum_k u_k - 8 sum_k u'_k + 64 K,
+//     with the row sums of the offset codes gathered while unpacking.
+// Within each group of 8 codes the unpacked byte order is (0,2,4,6,1,3,5,7);
+// the same permutation of K on both operands leaves the product unchanged.
+//
+// Warp roles (320 threads, one CTA per 128 x 256 output tile):
+//   warp 0      TMA producer: packed A/W k-blocks into a 4-stage ring (64B swizzle)
+//   warp 1      TMEM allocator and single-thread MMA issuer
+//   warps 2-9   converters: packed nibbles -> e4m3 bytes in a 2-stage ring
+//               laid out for the 128B-swizzled K-major UMMA descriptors;
+//               afterwards the epilogue (TMEM -> registers -> fp16)
+// Every wait is bounded; an expired wait records QUAROT_ERR_TIMEOUT and the
+// CTA drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace quarot {
+namespace gemm {
+
+constexpr int BM = 128, BN = 256, BK = 128;  // tile in codes
+constexpr int BKB = BK / 2;                  // packed bytes per row per k-block
+constexpr int SP = 4;                        // packed ring stages
+constexpr int SU = 2;                        // unpacked ring stages
+constexpr int NCONV = 256;                   // converter / epilogue threads
+constexpr int NTHREADS = 64 + NCONV;
+constexpr int A_PK = BM * BKB, B_PK = BN * BKB;  // 8 KB, 16 KB
+constexpr int A_UN = BM * BK, B_UN = BN * BK;    // 16 KB, 32 KB
+constexpr int OFF_AU = 0;
+constexpr int OFF_BU = OFF_AU + SU * A_UN;
+constexpr int OFF_AP = OFF_BU + SU * B_UN;
+constexpr int OFF_BP = OFF_AP + SP * A_PK;
+constexpr int OFF_BAR = OFF_BP + SP * B_PK;  // 196608
+constexpr int NBAR = 2 * SP + 2 * SU + 1;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int OFF_RSA = OFF_MISC + 16;
+constexpr int OFF_RSB = OFF_RSA + BM * 4;
+constexpr int SMEM_USED = OFF_RSB + BN * 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t TMEM_COLS = 256;
+constexpr int MAX_K = 65536;
+
+// Instruction descriptor, kind::f8f6f4: D fp32, A/B e4m3, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(BN >> 3) << 17) |
+                           (uint32_t(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand in the 128B swizzle
+// layout: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFF) >> 4);
+  d |= uint64_t(1) << 16;             // leading byte offset (unused for this layout)
+  d |= uint64_t(1024 >> 4) << 32;     // stride byte offset
+  d |= uint64_t(1) << 46;             // descriptor version
+  d |= uint64_t(2) << 61;             // SWIZZLE_128B
+  return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+#define QUAROT_TMEM_LD32(taddr, r)                                                                 \
+  asm volatile(                                                                                    \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"               \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),       \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),             \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])              \
+      : "r"(taddr))
+
+// 8 packed codes (one 32-bit word) -> 8 offset codes as bytes, order
+// (0,2,4,6 | 1,3,5,7); also returns their byte-wise sum word.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = (w ^ 0x88888888u) & 0x0F0F0F0Fu;
+  hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K,
+                 __half* __restrict__ y, int32_t* __restrict__ acc_out) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* pk_full = bars;
+  uint64_t* pk_empty = bars + SP;
+  uint64_t* un_full = bars + 2 * SP;
+  uint64_t* un_empty = bars + 2 * SP + SU;
+  uint64_t* acc_full = bars + 2 * SP + 2 * SU;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
+  int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
+  int* rsB = reinterpret_cast<int*>(sm + OFF_RSB);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int nkb = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SP; ++s) {
+      mbar_init(&pk_full[s], 1);
+      mbar_init(&pk_empty[s], NCONV);
+    }
+    for (int s = 0; s < SU; ++s) {
+      mbar_init(&un_full[s], NCONV);
+      mbar_init(&un_empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem_d = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % SP;
+        if (!mbar_wait_bounded(&pk_empty[s], ((kb / SP) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&pk_full[s], A_PK + B_PK);
+        tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
+        tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
+        issued = kb + 1;
+      }
+      if (*abort_flag) {
+        // drain: every issued copy must land before the CTA exits
+        for (int kb = (issued > SP ? issued - SP : 0); kb < issued; ++kb)
+          mbar_wait_bounded(&pk_full[kb % SP], (kb / SP) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % SU;
+        if (!mbar_wait_bounded(&un_full[s], (kb / SU) & 1, abort_flag)) break;
+        fence_after_sync();
+        const uint64_t ad = sw128_desc(smem_u32(sm + OFF_AU + s * A_UN));
+        const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + s * B_UN));
+#pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk)
+          mma_f8(tmem_d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), (kb | kk) != 0);
+        mma_commit(&un_empty[s]);
+      }
+      mma_commit(acc_full);  // also fires when nothing was issued
+    }
+  } else {
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - 64;
+    const int ra = ct >> 1;         // A row handled (half a row per thread)
+    const int ca0 = 2 * (ct & 1);   // first packed 16B chunk of that half row
+    uint32_t sumA = 0, sumB = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int sp = kb % SP, su = kb % SU;
+      if (!mbar_wait_bounded(&pk_full[sp], (kb / SP) & 1, abort_flag)) break;
+      if (!mbar_wait_bounded(&un_empty[su], ((kb / SU) & 1) ^ 1, abort_flag)) break;
+      const unsigned char* ap = sm + OFF_AP + sp * A_PK;
+      const unsigned char* bp = sm + OFF_BP + sp * B_PK;
+      unsigned char* au = sm + OFF_AU + su * A_UN;
+      unsigned char* bu = sm + OFF_BU + su * B_UN;
+      // A: row ra, packed chunks ca0, ca0+1 (64B-swizzled source)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = ca0 + i;
+        const uint4 w = *reinterpret_cast<const uint4*>(ap + ra * 64 + ((c ^ ((ra >> 1) & 3)) << 4));
+        uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+        unpack_word(w.x, l0, h0);
+        unpack_word(w.y, l1, h1);
+        unpack_word(w.z, l2, h2);
+        unpack_word(w.w, l3, h3);
+        sumA += __dp4a(l0 + h0 + l1 + h1 + l2 + h2 + l3 + h3, 0x01010101u, 0u);
+        unsigned char* rowp = au + ra * 128;
+        *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (ra & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
+        *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (ra & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
+      }
+      // B: row ct, packed chunks 0..3
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(bp + ct * 64 + ((c ^ ((ct >> 1) & 3)) << 4));
+        uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+        unpack_word(w.x, l0, h0);
+        unpack_word(w.y, l1, h1);
+        unpack_word(w.z, l2, h2);
+        unpack_word(w.w, l3, h3);
+        sumB += __dp4a(l0 + h0 + l1 + h1 + l2 + h2 + l3 + h3, 0x01010101u, 0u);
+        unsigned char* rowp = bu + ct * 128;
+        *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (ct & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
+        *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (ct & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&un_full[su]);
+      mbar_arrive(&pk_empty[sp]);
+    }
+    sumA += __shfl_xor_sync(0xffffffffu, sumA, 1);
+    if ((ct & 1) == 0) rsA[ra] = int(sumA);
+    rsB[ct] = int(sumB);
+    asm volatile("bar.sync 1, %0;" ::"r"(NCONV) : "memory");
+
+    // ------------------------------------------------------------ epilogue
+    const bool ok = mbar_wait_bounded(acc_full, 0, nullptr);
+    fence_after_sync();
+    if (ok && !*abort_flag) {
+      const int q = warp & 3;                   // TMEM lane quadrant of this warp
+      const int chalf = (warp - 2) >> 2;        // column half
+      const int r = 32 * q + lane;
+      const int gm = m0 + r;
+      const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
+      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[r]);
+      const bool vec_ok = (N % 8) == 0;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c0 = chalf * 128 + cc * 32;
+        uint32_t v[32];
+        __syncwarp();
+        QUAROT_TMEM_LD32(tmem_d + (uint32_t(32 * q) << 16) + uint32_t(c0), v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (gm < M && n0 + c0 < N) {
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f),
+                             8.0f * float(rsB[c0 + j])) + bias_r;
+        const int gn = n0 + c0;
+        __half* yrow = y + size_t(gm) * N + gn;
+        if (vec_ok && gn + 32 <= N) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sw + gn + j));
+            const uint32_t sws[4] = {s8.x, s8.y, s8.z, s8.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 wsc = h2_to_f2(sws[e]);
+              const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x));
+              const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
+              o[e] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+            }
+            *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        } else {
+          for (int j = 0; j < 32 && gn + j < N; ++j)
+            yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
+        }
+        if (acc_out != nullptr) {
+          int32_t* arow = acc_out + size_t(gm) * N + gn;
+          for (int j = 0; j < 32 && gn + j < N; ++j) arow[j] = __float2int_rn(acc[j]);
+        }
+        }
+      }
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after_sync();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+static bool make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int box_rows) {
+  cuuint64_t gdim[2] = {cuuint64_t(K / 2), cuuint64_t(rows)};
+  cuuint64_t gstride[1] = {cuuint64_t(K / 2)};
+  cuuint32_t box[2] = {cuuint32_t(BKB), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gemm
+}  // namespace quarot
+
+using namespace quarot;
+
+extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const uint8_t* w_q,
+                                const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
+                                int32_t* acc_out, void* stream) {
+  using namespace quarot::gemm;
+  if (M < 0 || N < 0 || K <= 0) return QUAROT_ERR_INVALID_ARG;
+  if (K % BK != 0 || K > MAX_K) return QUAROT_ERR_UNSUPPORTED;
+  if (M > (int64_t(1) << 31) - BM || N > (int64_t(1) << 31) - BN) return QUAROT_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return QUAROT_OK;
+  if (!a_q || !a_scale || !w_q || !w_scale || !y) return QUAROT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a_q) & 15) || (reinterpret_cast<uintptr_t>(w_q) & 15) ||
+      (reinterpret_cast<uintptr_t>(a_scale) & 1) || (reinterpret_cast<uintptr_t>(w_scale) & 15) ||
+      (reinterpret_cast<uintptr_t>(y) & 15) || (acc_out && (reinterpret_cast<uintptr_t>(acc_out) & 3)))
+    return QUAROT_ERR_ALIGNMENT;
+  if (!get_encoder()) return QUAROT_ERR_CUDA;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, a_q, M, K, BM) || !make_map(&tb, w_q, N, K, BN)) return QUAROT_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
+      return QUAROT_ERR_LAUNCH;
+    attr = true;
+  }
+  dim3 grid(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
+  w4a4_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(
+      ta, tb, static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale), int(M), int(N),
+      int(K), static_cast<__half*>(y), acc_out);
+  return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
