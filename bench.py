@@ -240,6 +240,15 @@ def run_ours(args):
             flush.zero_()  # L2 flush between timed steps (outside the step's events)
             step(evs[i])
         torch.cuda.synchronize()
+        timed_samples = len(clocks.lines)
+        # a short timed region may end before nvidia-smi reports: keep the same
+        # load running (untimed) until a few samples exist
+        t_end = time.time() + 3.0
+        while len(clocks.lines) < timed_samples + 5 and time.time() < t_end:
+            for _ in range(50):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
     q.quarot_check_error(stream)
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(EV - 1)] for i in range(args.steps)])
     step_ms = per.sum(axis=1)
@@ -321,7 +330,7 @@ def run_ours(args):
         "stages": stages,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), samples_in_timed_region=timed_samples),
     }
     if rank == 0 and not args.no_cpu_baseline:
         import torch as _t  # noqa: F401
@@ -340,7 +349,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

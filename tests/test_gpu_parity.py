@@ -43,7 +43,8 @@ def _t(a):
 
 def _fp16_ulp(s):
     s = np.asarray(s, dtype=np.float16)
-    return np.abs(np.spacing(s).astype(np.float64))
+    with np.errstate(over="ignore"):
+        return np.abs(np.spacing(s).astype(np.float64))
 
 
 def check_quant(gq, gs, grot, r_ref, clip=1.0):
@@ -86,7 +87,6 @@ def test_rotate_quant_clip_09(q, d):
     s = W.random_signs(d, 4)
     gq, gs, grot = q.quarot_rotate_quant(_t(x), _t(s), clip_ratio=0.9, want_rot=True)
     check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), O.rotate(x, s), clip=0.9)
-    assert (O.unpack_int4(gq.cpu().numpy()) == -8).any() or True
 
 
 def test_rotate_quant_edge_rows(q):
@@ -157,7 +157,7 @@ def test_gemm_adversarial_extremes(q):
     w[::3] = 7
     _, _, _, _, y, acc = _gemm_case(q, 130, 260, K, 7, a, w)
     assert np.array_equal(acc, O.int_gemm(a, w))
-    assert acc[0, 0] == 64 * K
+    assert acc[0, 0] == -56 * K and acc[0, 1] == 64 * K and acc[1, 0] == 49 * K
 
 
 def test_gemm_full_down_proj_sampled(q):
