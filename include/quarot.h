@@ -163,6 +163,34 @@ int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const
                        int64_t T_max, float sm_scale, int unrotate_out, void* out, void* workspace,
                        size_t ws_bytes, void* stream);
 
+/*
+ * quarot_decode_attn_static -- quarot_decode_attn for callers that cannot
+ * allocate device memory when they run decode (a plain C host without an
+ * allocator, a serving loop that forbids cudaMalloc/cudaFree after start-up
+ * because they synchronise the device or may fail, a plug-in that only
+ * receives its input and output buffers).  The QuaRot pages have no
+ * counterpart: this is a deployment variant of the "Decode" entry above.
+ *
+ * Same arguments and result as quarot_decode_attn, without the workspace:
+ * the split-T scratch is a fixed array of QUAROT_DECODE_STATIC_SCRATCH_BYTES
+ * inside the library, present on every GPU that loads it until process exit.
+ * The call allocates nothing.
+ *   - Returns QUAROT_ERR_UNSUPPORTED, before touching the device, when
+ *     quarot_decode_workspace_bytes(B, Hq, d, T) exceeds that maximum.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.  A failed lookup returns QUAROT_ERR_CUDA.
+ *   - Every call on a device shares the one array.  No part of it needs to
+ *     start at zero (each call writes every slot it later reads), but two
+ *     calls whose executions overlap on the GPU (different streams, no
+ *     ordering between them) race on it and give undefined results.
+ */
+#define QUAROT_DECODE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+int quarot_decode_attn_static(const void* q, const uint8_t* k_q, const void* k_s, const uint8_t* v_q,
+                              const void* v_s, int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t T,
+                              int64_t T_max, float sm_scale, int unrotate_out, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

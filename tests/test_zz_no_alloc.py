@@ -1,0 +1,82 @@
+"""quarot_decode_attn_static: the decode entry point for callers that cannot
+allocate device memory when they run decode (plain C hosts without an
+allocator, serving loops that forbid cudaMalloc after start-up, plug-ins that
+only receive their input and output buffers).  Its scratch is a fixed array
+inside the library, so it takes no workspace argument.
+
+The GPU test calls it through the C ABI twice in a row, with different sizes
+and inputs, and checks each result against quarot_decode_attn given its own
+caller-allocated workspace, within the decode tolerance of the other tests.
+This file is collected last so that a failure here cannot hide another test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+OUT_TOL = 1e-3
+
+
+def _rel_fro(a, b):
+    a = a.double()
+    b = b.double()
+    return float(torch.linalg.norm(a - b) / torch.linalg.norm(b))
+
+
+def _cache(B, Hkv, T, d, seed, dev):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    kq = torch.from_numpy(rng.integers(0, 256, size=(B, Hkv, T, d // 2), dtype=np.uint8)).to(dev)
+    vq = torch.from_numpy(rng.integers(0, 256, size=(B, Hkv, T, d // 2), dtype=np.uint8)).to(dev)
+    ks = torch.from_numpy(W.fp16_scales(B * Hkv * T, seed + 1, 0.05, 0.5).reshape(B, Hkv, T)).to(dev)
+    vs = torch.from_numpy(W.fp16_scales(B * Hkv * T, seed + 2, 0.05, 0.5).reshape(B, Hkv, T)).to(dev)
+    return kq, ks, vq, vs
+
+
+def test_static_rejects_oversize_without_touching_the_device():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import w4a4_rotated_quantized_gb300 as q
+
+    lib = q.load()
+    P = ctypes.c_void_p(0x10000)  # never dereferenced: the request is rejected first
+    # 64 x 32 heads x 32 splits x 130 floats = 34 MB > the 8 MB array
+    assert lib.quarot_decode_attn_static(P, P, P, P, P, 64, 32, 8, 128, 8192, 8192, 0.0, 0, P, None) == 2
+    assert q.quarot_decode_workspace_bytes(64, 32, 128, 8192) > q.DECODE_STATIC_SCRATCH_BYTES
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_workspace_entry_twice():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import w4a4_rotated_quantized_gb300 as q
+
+    lib = q.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    cases = [  # (B, Hkv, G, T, T_max, unrotate): the bench shape, then a smaller one
+        (16, 8, 4, 4096, 4096, 0),
+        (3, 2, 8, 700, 1024, 1),
+    ]
+    assert q.quarot_decode_workspace_bytes(16, 32, 128, 4096) <= q.DECODE_STATIC_SCRATCH_BYTES
+    for i, (B, Hkv, G, T, T_max, unrot) in enumerate(cases):
+        d = 128
+        kq, ks, vq, vs = _cache(B, Hkv, T_max, d, 100 + i, dev)
+        qq = torch.from_numpy(W.query(B, Hkv * G, d, 200 + i)).to(dev)
+        ref = q.quarot_decode_attn(qq, kq, ks, vq, vs, T=T, unrotate_out=bool(unrot))
+        out = torch.full((B, Hkv * G, d), float("nan"), dtype=torch.float16, device=dev)
+        st = lib.quarot_decode_attn_static(
+            ctypes.c_void_p(qq.data_ptr()), ctypes.c_void_p(kq.data_ptr()), ctypes.c_void_p(ks.data_ptr()),
+            ctypes.c_void_p(vq.data_ptr()), ctypes.c_void_p(vs.data_ptr()), B, Hkv * G, Hkv, d, T, T_max, 0.0,
+            unrot, ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+        assert st == 0, q.STATUS.get(st)
+        q.quarot_check_error(stream)
+        assert torch.isfinite(out).all()
+        assert _rel_fro(out, ref) <= OUT_TOL

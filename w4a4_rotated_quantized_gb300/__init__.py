@@ -38,7 +38,10 @@ _SIGS = {
     "quarot_decode_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "quarot_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                           ctypes.c_float, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
+    "quarot_decode_attn_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                                 ctypes.c_float, ctypes.c_int, _P, _P]),
 }
+DECODE_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024  # QUAROT_DECODE_STATIC_SCRATCH_BYTES
 EXPORTED = tuple(_SIGS)
 
 
@@ -193,6 +196,30 @@ def quarot_decode_attn(q, k_q, k_s, v_q, v_s, T: int, sm_scale: float = 0.0, unr
                                    T_max, float(sm_scale), int(bool(unrotate_out)), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check(st, "quarot_decode_attn")
+    return out
+
+
+def quarot_decode_attn_static(q, k_q, k_s, v_q, v_s, T: int, sm_scale: float = 0.0, unrotate_out: bool = False,
+                              out=None, stream=None):
+    """quarot_decode_attn without a workspace argument: the scratch is the
+    library's fixed device array, so the call itself allocates nothing (pass
+    ``out`` to avoid the only torch allocation here).  For callers that cannot
+    allocate device memory when they run decode."""
+    _need(q, torch.float16, "q")
+    dev = q.device
+    for t, n in ((k_q, "k_q"), (v_q, "v_q")):
+        _need(t, torch.uint8, n, dev)
+    for t, n in ((k_s, "k_s"), (v_s, "v_s")):
+        _need(t, torch.float16, n, dev)
+    B, Hq, d = q.shape
+    Hkv, T_max = k_q.shape[1], k_q.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    _need(out, torch.float16, "out", dev)
+    st = load().quarot_decode_attn_static(_ptr(q), _ptr(k_q), _ptr(k_s), _ptr(v_q), _ptr(v_s), B, Hq, Hkv, d,
+                                          int(T), T_max, float(sm_scale), int(bool(unrotate_out)), _ptr(out),
+                                          _stream(stream, dev))
+    _check(st, "quarot_decode_attn_static")
     return out
 
 
