@@ -225,7 +225,7 @@ def run_ours(args):
         if ev is not None:
             ev[4].record(stream)
 
-    LAUNCHES_PER_STEP = 1 + 1 + 2 + 2
+    LAUNCHES_PER_STEP = 1 + 1 + 1 + 2
     for _ in range(args.warmup):
         flush.zero_()
         step()

@@ -79,7 +79,7 @@ int quarot_check_error(void* stream);
  *             x 16-byte aligned)
  *   M         rows (>= 0; M == 0 is a no-op)
  *   d         row width: 2^n with 16 <= d <= 8192, or 12 * 2^n with
- *             768 <= d <= 12288
+ *             3072 <= d <= 12288
  *   signs     int8 [d] of +1/-1 (read only), or NULL
  *   clip_ratio  in (0, 1]
  *   q_out     uint8 [M, d/2], 16-byte aligned
@@ -104,7 +104,8 @@ int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, const
  *   a_scale   fp16 [M]
  *   w_q       uint8 [N, K/2] packed weights (K-major, [out, in]), 16-byte aligned
  *   w_scale   fp16 [N]
- *   M, N      >= 0 (ragged tails handled); K % 128 == 0, 128 <= K <= 131072
+ *   M, N      >= 0 (ragged tails handled); K % 128 == 0, 128 <= K <= 65536
+ *             (the bound keeps every partial sum exact in fp32 on the tensor cores)
  *   y         fp16 [M, N]
  *   acc_out   int32 [M, N] (the exact accumulator, for testing), or NULL
  */
@@ -148,7 +149,7 @@ size_t quarot_decode_workspace_bytes(int64_t B, int64_t Hq, int64_t d, int64_t T
  *
  *   q         fp16 [B, Hq, d], 16-byte aligned
  *   k_q, k_s, v_q, v_s  caches as written by quarot_kv_write (capacity T_max)
- *   d         128; Hq % Hkv == 0 and Hq / Hkv <= 8
+ *   d         128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8}
  *   T         tokens to attend, 0 <= T <= T_max (T == 0 gives o = 0)
  *   sm_scale  softmax scale; <= 0 selects 1/sqrt(d)
  *   unrotate_out  0: o stays in the rotated basis (the rotation is absorbed

@@ -24,14 +24,18 @@
 // Within each group of 8 codes the unpacked byte order is (0,2,4,6,1,3,5,7);
 // the same permutation of K on both operands leaves the product unchanged.
 //
-// Warp roles (320 threads, one CTA per 128 x 256 output tile):
-//   warp 0      TMA producer: packed A/W k-blocks into a 4-stage ring (64B swizzle)
-//   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2-9   converters: packed nibbles -> e4m3 bytes in a 2-stage ring
-//               laid out for the 128B-swizzled K-major UMMA descriptors;
-//               afterwards the epilogue (TMEM -> registers -> fp16)
-// Every wait is bounded; an expired wait records QUAROT_ERR_TIMEOUT and the
-// CTA drains its copies and MMAs, frees TMEM and returns.
+// Persistent kernel, one CTA per SM, 576 threads in five roles:
+//   warp 0        TMA producer: packed A/W k-blocks into a 4-stage ring (64B swizzle)
+//   warp 1        TMEM allocator and single-thread MMA issuer
+//   warps 2-13    converters: packed nibbles -> e4m3 bytes in a 2-stage ring laid
+//                 out for the 128B-swizzled K-major UMMA descriptors, plus the
+//                 offset-code row sums of the tile
+//   warps 14-17   epilogue: TMEM -> registers -> integer correction -> fp16
+// Tiles are 128 x BN (BN in {128..256} chosen per shape so the tiles split
+// evenly over the SMs); two TMEM accumulators let the epilogue of one tile
+// overlap the main loop of the next.  Every wait is bounded; an expired wait
+// records QUAROT_ERR_TIMEOUT and the CTA drains its copies and MMAs, frees
+// TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,32 +46,33 @@
 namespace quarot {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 128;  // tile in codes
-constexpr int BKB = BK / 2;                  // packed bytes per row per k-block
-constexpr int SP = 4;                        // packed ring stages
-constexpr int SU = 2;                        // unpacked ring stages
-constexpr int NCONV = 256;                   // converter / epilogue threads
-constexpr int NTHREADS = 64 + NCONV;
-constexpr int A_PK = BM * BKB, B_PK = BN * BKB;  // 8 KB, 16 KB
-constexpr int A_UN = BM * BK, B_UN = BN * BK;    // 16 KB, 32 KB
+constexpr int BM = 128, BN_MAX = 256, BK = 128;  // tile in codes
+constexpr int BKB = BK / 2;                      // packed bytes per row per k-block
+constexpr int SP = 4;                            // packed ring stages
+constexpr int SU = 2;                            // unpacked ring stages
+constexpr int NCONV = 384;                       // converter threads (12 warps)
+constexpr int NEPI = 128;                        // epilogue threads (4 warps)
+constexpr int EPI_WARP0 = 2 + NCONV / 32;        // 14
+constexpr int NTHREADS = 64 + NCONV + NEPI;      // 576
+constexpr int A_PK = BM * BKB, B_PK = BN_MAX * BKB;  // 8 KB, 16 KB
+constexpr int A_UN = BM * BK, B_UN = BN_MAX * BK;    // 16 KB, 32 KB
 constexpr int OFF_AU = 0;
 constexpr int OFF_BU = OFF_AU + SU * A_UN;
 constexpr int OFF_AP = OFF_BU + SU * B_UN;
 constexpr int OFF_BP = OFF_AP + SP * A_PK;
 constexpr int OFF_BAR = OFF_BP + SP * B_PK;  // 196608
-constexpr int NBAR = 2 * SP + 2 * SU + 1;
+constexpr int NBAR = 2 * SP + 2 * SU + 8 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int OFF_RSA = OFF_MISC + 16;
-constexpr int OFF_RSB = OFF_RSA + BM * 4;
-constexpr int SMEM_USED = OFF_RSB + BN * 4;
+constexpr int OFF_RSA = OFF_MISC + 16;             // int [2][BM]
+constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;      // int [2][BN_MAX]
+constexpr int SMEM_USED = OFF_RSB + 2 * BN_MAX * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;           // two accumulators of up to 256 columns
 constexpr int MAX_K = 65536;
 
 // Instruction descriptor, kind::f8f6f4: D fp32, A/B e4m3, both K-major,
-// N = 256, M = 128.
-constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(BN >> 3) << 17) |
-                           (uint32_t(BM >> 4) << 24);
+// M = 128; N (bits 17-22, N >> 3) is filled in at run time.
+constexpr uint32_t IDESC_BASE = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(BM >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major operand in the 128B swizzle
 // layout: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -89,13 +94,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate));
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -129,9 +134,31 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& lo, uint32_t& 
   hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;
 }
 
+// One packed 64-byte row chunk set (4 x 16 B, 64B-swizzled source) -> 128
+// e4m3 bytes (128B-swizzled destination); returns the byte sum of the offset
+// codes.
+__device__ __forceinline__ uint32_t convert_row(const unsigned char* src_row, int r, unsigned char* dst_row) {
+  uint4 w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(src_row + ((c ^ ((r >> 1) & 3)) << 4));
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+    unpack_word(w[c].x, l0, h0);
+    unpack_word(w[c].y, l1, h1);
+    unpack_word(w[c].z, l2, h2);
+    unpack_word(w[c].w, l3, h3);
+    acc = __dp4a((l0 + h0) + (l1 + h1) + (l2 + h2) + (l3 + h3), 0x01010101u, acc);
+    *reinterpret_cast<uint4*>(dst_row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
+    *reinterpret_cast<uint4*>(dst_row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
+  }
+  return acc;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K,
+                 const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K, int BN,
                  __half* __restrict__ y, int32_t* __restrict__ acc_out) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -141,15 +168,22 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   uint64_t* pk_empty = bars + SP;
   uint64_t* un_full = bars + 2 * SP;
   uint64_t* un_empty = bars + 2 * SP + SU;
-  uint64_t* acc_full = bars + 2 * SP + 2 * SU;
+  uint64_t* acc_full = bars + 2 * SP + 2 * SU;   // [2]
+  uint64_t* acc_empty = acc_full + 2;            // [2]
+  uint64_t* rs_full = acc_full + 4;              // [2]
+  uint64_t* rs_empty = acc_full + 6;             // [2]
+  uint64_t* drain = acc_full + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
   int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
   int* rsB = reinterpret_cast<int*>(sm + OFF_RSB);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int nkb = K / BK;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + BM - 1) / BM) * n_tiles_n;
+  const uint32_t idesc = IDESC_BASE | (uint32_t(BN >> 3) << 17);
+  const int b_bytes = BN * BKB;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SP; ++s) {
@@ -160,7 +194,13 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       mbar_init(&un_full[s], NCONV);
       mbar_init(&un_empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], NEPI);
+      mbar_init(&rs_full[s], NCONV);
+      mbar_init(&rs_empty[s], NEPI);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -174,145 +214,154 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  const uint32_t tmem_d = *tmem_slot;
+  const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % SP;
-        if (!mbar_wait_bounded(&pk_empty[s], ((kb / SP) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&pk_full[s], A_PK + B_PK);
-        tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
-        tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
-        issued = kb + 1;
+      long issued = 0;
+      long it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = int(it % SP);
+          if (!mbar_wait_bounded(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(&pk_full[s], A_PK + b_bytes);
+          tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
+          tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
+          issued = it + 1;
+        }
       }
       if (*abort_flag) {
         // drain: every issued copy must land before the CTA exits
-        for (int kb = (issued > SP ? issued - SP : 0); kb < issued; ++kb)
-          mbar_wait_bounded(&pk_full[kb % SP], (kb / SP) & 1, nullptr);
+        for (long j = (issued > SP ? issued - SP : 0); j < issued; ++j)
+          mbar_wait_bounded(&pk_full[j % SP], uint32_t((j / SP) & 1), nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % SU;
-        if (!mbar_wait_bounded(&un_full[s], (kb / SU) & 1, abort_flag)) break;
+      long it = 0;
+      int ti = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
+        const int a = ti & 1;
+        if (!mbar_wait_bounded(&acc_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
         fence_after_sync();
-        const uint64_t ad = sw128_desc(smem_u32(sm + OFF_AU + s * A_UN));
-        const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + s * B_UN));
+        const uint32_t tmem_d = tmem_base + uint32_t(a * BN_MAX);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = int(it % SU);
+          if (!mbar_wait_bounded(&un_full[s], uint32_t((it / SU) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          const uint64_t ad = sw128_desc(smem_u32(sm + OFF_AU + s * A_UN));
+          const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + s * B_UN));
 #pragma unroll
-        for (int kk = 0; kk < BK / 32; ++kk)
-          mma_f8(tmem_d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), (kb | kk) != 0);
-        mma_commit(&un_empty[s]);
+          for (int kk = 0; kk < BK / 32; ++kk)
+            mma_f8(tmem_d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
+          mma_commit(&un_empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[a]);
       }
-      mma_commit(acc_full);  // also fires when nothing was issued
+      // every issued MMA must finish before TMEM is freed
+      mma_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ converters
+    const int ct = threadIdx.x - 64;  // 0..383
+    const bool is_a = ct < BM;
+    const int r = is_a ? ct : ct - BM;
+    long it = 0;
+    int ti = 0;
+    for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
+      uint32_t sum = 0;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int sp = int(it % SP), su = int(it % SU);
+        if (!mbar_wait_bounded(&pk_full[sp], uint32_t((it / SP) & 1), abort_flag) ||
+            !mbar_wait_bounded(&un_empty[su], uint32_t((it / SU) & 1) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (is_a) {
+          sum += convert_row(sm + OFF_AP + sp * A_PK + r * 64, r, sm + OFF_AU + su * A_UN + r * 128);
+        } else if (r < BN) {
+          sum += convert_row(sm + OFF_BP + sp * B_PK + r * 64, r, sm + OFF_BU + su * B_UN + r * 128);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&un_full[su]);
+        mbar_arrive(&pk_empty[sp]);
+      }
+      if (!ok) break;
+      const int a = ti & 1;
+      if (!mbar_wait_bounded(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+      if (is_a) rsA[a * BM + r] = int(sum);
+      else rsB[a * BN_MAX + r] = int(sum);
+      mbar_arrive(&rs_full[a]);
     }
   } else {
-    // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 64;
-    const int ra = ct >> 1;         // A row handled (half a row per thread)
-    const int ca0 = 2 * (ct & 1);   // first packed 16B chunk of that half row
-    uint32_t sumA = 0, sumB = 0;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int sp = kb % SP, su = kb % SU;
-      if (!mbar_wait_bounded(&pk_full[sp], (kb / SP) & 1, abort_flag)) break;
-      if (!mbar_wait_bounded(&un_empty[su], ((kb / SU) & 1) ^ 1, abort_flag)) break;
-      const unsigned char* ap = sm + OFF_AP + sp * A_PK;
-      const unsigned char* bp = sm + OFF_BP + sp * B_PK;
-      unsigned char* au = sm + OFF_AU + su * A_UN;
-      unsigned char* bu = sm + OFF_BU + su * B_UN;
-      // A: row ra, packed chunks ca0, ca0+1 (64B-swizzled source)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int c = ca0 + i;
-        const uint4 w = *reinterpret_cast<const uint4*>(ap + ra * 64 + ((c ^ ((ra >> 1) & 3)) << 4));
-        uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
-        unpack_word(w.x, l0, h0);
-        unpack_word(w.y, l1, h1);
-        unpack_word(w.z, l2, h2);
-        unpack_word(w.w, l3, h3);
-        sumA += __dp4a(l0 + h0 + l1 + h1 + l2 + h2 + l3 + h3, 0x01010101u, 0u);
-        unsigned char* rowp = au + ra * 128;
-        *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (ra & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
-        *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (ra & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
-      }
-      // B: row ct, packed chunks 0..3
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(bp + ct * 64 + ((c ^ ((ct >> 1) & 3)) << 4));
-        uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
-        unpack_word(w.x, l0, h0);
-        unpack_word(w.y, l1, h1);
-        unpack_word(w.z, l2, h2);
-        unpack_word(w.w, l3, h3);
-        sumB += __dp4a(l0 + h0 + l1 + h1 + l2 + h2 + l3 + h3, 0x01010101u, 0u);
-        unsigned char* rowp = bu + ct * 128;
-        *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (ct & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
-        *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (ct & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&un_full[su]);
-      mbar_arrive(&pk_empty[sp]);
-    }
-    sumA += __shfl_xor_sync(0xffffffffu, sumA, 1);
-    if ((ct & 1) == 0) rsA[ra] = int(sumA);
-    rsB[ct] = int(sumB);
-    asm volatile("bar.sync 1, %0;" ::"r"(NCONV) : "memory");
-
     // ------------------------------------------------------------ epilogue
-    const bool ok = mbar_wait_bounded(acc_full, 0, nullptr);
-    fence_after_sync();
-    if (ok && !*abort_flag) {
-      const int q = warp & 3;                   // TMEM lane quadrant of this warp
-      const int chalf = (warp - 2) >> 2;        // column half
-      const int r = 32 * q + lane;
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int r = 32 * q + lane;
+    const bool vec_ok = (N % 8) == 0;
+    int ti = 0;
+    for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
+      const int a = ti & 1;
+      const uint32_t par = uint32_t((ti >> 1) & 1);
+      if (!mbar_wait_bounded(&acc_full[a], par, abort_flag) || !mbar_wait_bounded(&rs_full[a], par, abort_flag))
+        break;
+      fence_after_sync();
+      const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
       const int gm = m0 + r;
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
-      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[r]);
-      const bool vec_ok = (N % 8) == 0;
+      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[a * BM + r]);
+      const int* rsb = rsB + a * BN_MAX;
+      const uint32_t tmem_row = tmem_base + uint32_t(a * BN_MAX) + (uint32_t(32 * q) << 16);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const int c0 = chalf * 128 + cc * 32;
+      for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
         __syncwarp();
-        QUAROT_TMEM_LD32(tmem_d + (uint32_t(32 * q) << 16) + uint32_t(c0), v);
+        QUAROT_TMEM_LD32(tmem_row + uint32_t(c0), v);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (gm < M && n0 + c0 < N) {
-        float acc[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f),
-                             8.0f * float(rsB[c0 + j])) + bias_r;
         const int gn = n0 + c0;
-        __half* yrow = y + size_t(gm) * N + gn;
-        if (vec_ok && gn + 32 <= N) {
+        if (gm < M && gn < N) {
+          float acc[32];
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sw + gn + j));
-            const uint32_t sws[4] = {s8.x, s8.y, s8.z, s8.w};
-            uint32_t o[4];
+          for (int j = 0; j < 32; ++j)
+            acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(rsb[c0 + j])) + bias_r;
+          __half* yrow = y + size_t(gm) * N + gn;
+          if (vec_ok && gn + 32 <= N) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 wsc = h2_to_f2(sws[e]);
-              const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x));
-              const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
-              o[e] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+            for (int j = 0; j < 32; j += 8) {
+              const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sw + gn + j));
+              const uint32_t sws[4] = {s8.x, s8.y, s8.z, s8.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 wsc = h2_to_f2(sws[e]);
+                const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x));
+                const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
+                o[e] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+              }
+              *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
+          } else {
+            for (int j = 0; j < 32 && gn + j < N; ++j)
+              yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
           }
-        } else {
-          for (int j = 0; j < 32 && gn + j < N; ++j)
-            yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
-        }
-        if (acc_out != nullptr) {
-          int32_t* arow = acc_out + size_t(gm) * N + gn;
-          for (int j = 0; j < 32 && gn + j < N; ++j) arow[j] = __float2int_rn(acc[j]);
-        }
+          if (acc_out != nullptr) {
+            int32_t* arow = acc_out + size_t(gm) * N + gn;
+            for (int j = 0; j < 32 && gn + j < N; ++j) arow[j] = __float2int_rn(acc[j]);
+          }
         }
       }
+      fence_before_sync();
+      mbar_arrive(&acc_empty[a]);
+      mbar_arrive(&rs_empty[a]);
     }
   }
 
@@ -320,7 +369,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   __syncthreads();
   if (warp == 1) {
     fence_after_sync();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(TMEM_COLS)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                  : "memory");
   }
 }
@@ -351,6 +400,31 @@ static bool make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tile width for the N dimension: the candidate with the smallest per-SM
+// makespan (tiles per SM x width), larger widths first on ties.
+static int pick_bn(int64_t M, int64_t N, int sms) {
+  const int cands[5] = {256, 224, 192, 160, 128};
+  int best = 256;
+  int64_t best_cost = -1;
+  const int64_t mt = (M + BM - 1) / BM;
+  for (int bn : cands) {
+    const int64_t tiles = mt * ((N + bn - 1) / bn);
+    const int64_t cost = ((tiles + sms - 1) / sms) * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 }  // namespace gemm
 }  // namespace quarot
 
@@ -362,7 +436,7 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   using namespace quarot::gemm;
   if (M < 0 || N < 0 || K <= 0) return QUAROT_ERR_INVALID_ARG;
   if (K % BK != 0 || K > MAX_K) return QUAROT_ERR_UNSUPPORTED;
-  if (M > (int64_t(1) << 31) - BM || N > (int64_t(1) << 31) - BN) return QUAROT_ERR_UNSUPPORTED;
+  if (M > (int64_t(1) << 31) - BM || N > (int64_t(1) << 31) - BN_MAX) return QUAROT_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return QUAROT_OK;
   if (!a_q || !a_scale || !w_q || !w_scale || !y) return QUAROT_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(a_q) & 15) || (reinterpret_cast<uintptr_t>(w_q) & 15) ||
@@ -370,8 +444,11 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
       (reinterpret_cast<uintptr_t>(y) & 15) || (acc_out && (reinterpret_cast<uintptr_t>(acc_out) & 3)))
     return QUAROT_ERR_ALIGNMENT;
   if (!get_encoder()) return QUAROT_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms <= 0) return QUAROT_ERR_CUDA;
+  const int bn = pick_bn(M, N, sms);
   CUtensorMap ta, tb;
-  if (!make_map(&ta, a_q, M, K, BM) || !make_map(&tb, w_q, N, K, BN)) return QUAROT_ERR_CUDA;
+  if (!make_map(&ta, a_q, M, K, BM) || !make_map(&tb, w_q, N, K, bn)) return QUAROT_ERR_CUDA;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
@@ -379,9 +456,10 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
       return QUAROT_ERR_LAUNCH;
     attr = true;
   }
-  dim3 grid(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const unsigned grid = unsigned(tiles < sms ? tiles : sms);
   w4a4_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(
       ta, tb, static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale), int(M), int(N),
-      int(K), static_cast<__half*>(y), acc_out);
+      int(K), bn, static_cast<__half*>(y), acc_out);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }

@@ -40,9 +40,14 @@ __device__ __forceinline__ void fwht32(float* v) {
 
 template <int D>
 __global__ void __launch_bounds__(256)
-kv_write_kernel(const __half* __restrict__ src, int64_t B, int64_t T_new, int64_t Hkv, int64_t t_start,
-                int64_t T_max, uint8_t* __restrict__ cq, __half* __restrict__ cs) {
+kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_src, int64_t B, int64_t T_new,
+                int64_t Hkv, int64_t t_start, int64_t T_max, uint8_t* __restrict__ k_q, __half* __restrict__ k_s,
+                uint8_t* __restrict__ v_q, __half* __restrict__ v_s) {
   constexpr int TPV = D / 32;
+  // blockIdx.y selects the tensor: 0 = keys, 1 = values
+  const __half* __restrict__ src = blockIdx.y == 0 ? k_src : v_src;
+  uint8_t* __restrict__ cq = blockIdx.y == 0 ? k_q : v_q;
+  __half* __restrict__ cs = blockIdx.y == 0 ? k_s : v_s;
   const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nvec = B * Hkv * T_new;
   const int64_t vi = gt / TPV;
@@ -316,10 +321,9 @@ extern "C" int quarot_kv_write(const void* k, const void* v, int64_t B, int64_t 
   const int64_t blocks = (threads + 255) / 256;
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   auto go = [&](auto kern) {
-    kern<<<unsigned(blocks), 256, 0, st>>>(static_cast<const __half*>(k), B, T_new, Hkv, t_start, T_max, k_q,
-                                           static_cast<__half*>(k_s));
-    kern<<<unsigned(blocks), 256, 0, st>>>(static_cast<const __half*>(v), B, T_new, Hkv, t_start, T_max, v_q,
-                                           static_cast<__half*>(v_s));
+    kern<<<dim3(unsigned(blocks), 2), 256, 0, st>>>(static_cast<const __half*>(k), static_cast<const __half*>(v),
+                                                    B, T_new, Hkv, t_start, T_max, k_q, static_cast<__half*>(k_s),
+                                                    v_q, static_cast<__half*>(v_s));
   };
   if (d == 64) go(kv::kv_write_kernel<64>);
   else if (d == 128) go(kv::kv_write_kernel<128>);
