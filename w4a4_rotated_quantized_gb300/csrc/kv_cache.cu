@@ -116,35 +116,93 @@ __host__ __device__ inline int64_t num_splits(int64_t T) {
   return s < 1 ? 1 : s;
 }
 
-// Nibble n (0..15) of a two's complement code -> float value, exactly:
-// 2^23 + (n ^ 8) as fp32 bits, minus 2^23 + 8.
-__device__ __forceinline__ float code_f(uint32_t n) {
-  return __int_as_float(0x4B000000 | ((n ^ 8u) & 0xFu)) - 8388616.0f;
+// ------------------------------------------------------------------ tensor-core helpers
+// The INT4 codes are exact in fp16.  A byte holding codes (lo, hi) becomes an
+// fp16x2 pair with the magic-number trick: 0x6400 | (n ^ 8) is 1024 + (v + 8)
+// for the low nibble, 0x6400 | ((n ^ 8) << 4) is 1024 + 16 (v + 8) for the
+// high nibble; one fused multiply-add per pair recovers v exactly.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t x, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(m), "r"(c));
+  return d;
+}
+constexpr uint32_t H2_ONE = 0x3C003C00u;       // (1, 1)
+constexpr uint32_t H2_M1032 = 0xE408E408u;     // (-1032, -1032)
+constexpr uint32_t H2_SIXTEENTH = 0x2C002C00u; // (1/16, 1/16)
+constexpr uint32_t H2_M72 = 0xD480D480u;       // (-72, -72)
+constexpr uint32_t H2_ONE_SIXTEENTH = 0x2C003C00u;  // (lo 1, hi 1/16)
+constexpr uint32_t H2_M1032_M72 = 0xD480E408u;      // (lo -1032, hi -72)
+
+// Byte `p` of `w` -> (code_lo, code_hi) as fp16x2.
+__device__ __forceinline__ uint32_t byte_pair(uint32_t w, int p) {
+  const uint32_t x = prmt(w, 0u, uint32_t(p) | (4u << 4) | (uint32_t(p) << 8) | (4u << 12));
+  const uint32_t h = (x & 0x00F0000Fu) ^ 0x64806408u;
+  return hfma2_u32(h, H2_ONE_SIXTEENTH, H2_M1032_M72);
+}
+// Byte `p` of `wa` and byte `p` of `wb` -> low nibbles (lo_a, lo_b) and high
+// nibbles (hi_a, hi_b) as fp16x2.
+__device__ __forceinline__ void byte_cross(uint32_t wa, uint32_t wb, int p, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = prmt(wa, wb, uint32_t(p) | (uint32_t(p + 4) << 8));
+  lo = hfma2_u32((x & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
+  hi = hfma2_u32((x & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
 }
 
-// One CTA per (split, b, g): partial softmax state of the GQA group's heads
-// over one chunk of tokens.  Scores use exp2 with log2(e) folded into q~.
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
+  return uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+}
+
+// One CTA per (split, b, g): the partial softmax state of the group's G query
+// heads over CHUNK tokens, on tensor cores.  Four warps take 16-token tiles in
+// turn.  Per tile:
+//   scores  S^T[16 tok x 2G] = Kcodes[16 x 128] . Q~^T, m16n8k16 with the
+//           query split into fp16 hi and lo halves (the 2G columns), so the
+//           product keeps fp32-level precision; the key scale multiplies the
+//           fp32 result.  Head dims are permuted identically on both
+//           operands so that each thread's fragment bytes are one 16-byte load.
+//   softmax online per head, warp-uniform running max, exp2 (log2 e folded
+//           into q~).
+//   output  O^T[128 x 2G] += Vcodes^T[128 x 16 tok] . P'^T, with P' = p * v_scale
+//           split into fp16 hi and lo columns; the output dims are permuted so
+//           each thread's value bytes are one 8-byte load per token.
 template <int G>
 __global__ void __launch_bounds__(DT)
-decode_partial_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq,
-                      const __half* __restrict__ ks, const uint8_t* __restrict__ vq,
-                      const __half* __restrict__ vs, int Hq, int Hkv, int T, int T_max,
-                      float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits) {
+decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, const __half* __restrict__ ks,
+                  const uint8_t* __restrict__ vq, const __half* __restrict__ vs, int Hq, int Hkv, int T,
+                  int T_max, float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits) {
+  constexpr int NT = (2 * G + 7) / 8;  // n8 tiles of (head, hi/lo) columns
+  constexpr int NW = DT / 32;
   __shared__ float qs[G][HD];
-  __shared__ float sc[CHUNK][G];          // scores, then p * v_scale
-  __shared__ __align__(16) uint8_t vcode[CHUNK][HD / 2];
-  __shared__ float red[DT / 32][G];
-  __shared__ float mrow[G], lrow[G];
+  __shared__ float wm[NW][G], wl[NW][G];
+  __shared__ float wo[NW][G][HD];
 
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
   const int b = bg / Hkv, g = bg % Hkv;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int r = lane >> 2, c = lane & 3;
   const int t0 = split * CHUNK;
-  const int tn = min(CHUNK, T - t0);      // tokens in this chunk (may be <= 0)
-  const int64_t cache_row = (int64_t(b) * Hkv + g) * T_max;
+  const int tn = min(CHUNK, T - t0);
+  const int64_t cache_row = (int64_t(b) * Hkv + g) * T_max + t0;
+  const uint8_t* kbase = kq + cache_row * (HD / 2);
+  const uint8_t* vbase = vq + cache_row * (HD / 2);
+  const __half* ksb = ks + cache_row;
+  const __half* vsb = vs + cache_row;
 
-  // q~ = q H / sqrt(d) * qscale, head-wise FWHT in shared memory
+  // ---- q~ = q H / sqrt(d) * qscale (FWHT in shared memory)
   for (int i = tid; i < G * HD; i += DT) {
     const int hh = i / HD, e = i % HD;
     qs[hh][e] = __half2float(q[(int64_t(b) * Hq + g * G + hh) * HD + e]);
@@ -154,115 +212,174 @@ decode_partial_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ 
     for (int i = tid; i < G * HD / 2; i += DT) {
       const int hh = i / (HD / 2), pr = i % (HD / 2);
       const int lo = (pr / hspan) * 2 * hspan + (pr % hspan);
-      const float a = qs[hh][lo], c = qs[hh][lo + hspan];
-      qs[hh][lo] = a + c;
-      qs[hh][lo + hspan] = a - c;
+      const float a = qs[hh][lo], cc = qs[hh][lo + hspan];
+      qs[hh][lo] = a + cc;
+      qs[hh][lo + hspan] = a - cc;
     }
     __syncthreads();
   }
-  for (int i = tid; i < G * HD; i += DT) (&qs[0][0])[i] *= qscale;
-  // stage the chunk's value codes
-  for (int i = tid; i < CHUNK * (HD / 2) / 16; i += DT) {
-    const int tok = i / (HD / 32), part = i % (HD / 32);
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (tok < tn) val = __ldcs(reinterpret_cast<const uint4*>(vq + (cache_row + t0 + tok) * (HD / 2)) + part);
-    *reinterpret_cast<uint4*>(&vcode[tok][part * 16]) = val;
-  }
-  __syncthreads();
 
-  // scores: one thread per token
-  float lmax[G];
+  // ---- B fragments of Q~^T: column n = lane/4 of n-tile nt is head (4 nt + n/2),
+  // hi half for even n, lo half for odd n.  Step j uses head dims
+  // 32c + 4j + {0,1} (b0) and 32c + 4j + {2,3} (b1).
+  uint32_t qb[NT][8][2];
 #pragma unroll
-  for (int hh = 0; hh < G; ++hh) lmax[hh] = -INFINITY;
-  for (int tok = tid; tok < tn; tok += DT) {
-    const uint4* kp = reinterpret_cast<const uint4*>(kq + (cache_row + t0 + tok) * (HD / 2));
-    float acc[G];
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = nt * 4 + (r >> 1);
+    const bool lo_part = (r & 1) != 0;
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) acc[hh] = 0.f;
+    for (int j = 0; j < 8; ++j) {
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      const uint4 r = __ldcs(kp + c);
-      const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+      for (int half = 0; half < 2; ++half) {
+        __half e2[2];
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi)
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-          const float kv = code_f(wv[wi] >> (4 * n));
-          const int e = c * 32 + wi * 8 + n;
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) acc[hh] = fmaf(qs[hh][e], kv, acc[hh]);
+        for (int e = 0; e < 2; ++e) {
+          const float x = hh < G ? qs[hh][32 * c + 4 * j + 2 * half + e] * qscale : 0.f;
+          const __half hi = __float2half_rn(x);
+          e2[e] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
         }
-    }
-    const float ksc = __half2float(ks[cache_row + t0 + tok]);
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float s = acc[hh] * ksc;
-      sc[tok][hh] = s;
-      lmax[hh] = fmaxf(lmax[hh], s);
+        qb[nt][j][half] = pack_h2(e2[0], e2[1]);
+      }
     }
   }
-  // chunk max per head
+
+  float o[NT][8][4];
 #pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    float m = lmax[hh];
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[wid][hh] = m;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][i][e] = 0.f;
+  float m_run[NT], l_run[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt] = -INFINITY;
+    l_run[nt] = 0.f;
   }
-  __syncthreads();
-  if (tid < G) {
-    float m = red[0][tid];
+
+  for (int tt = wid * 16; tt < tn; tt += NW * 16) {
+    // ---- loads: keys of tokens tt+r, tt+r+8 (bytes 16c..16c+15); values of
+    // tokens tt+2c, +1, +8, +9 (bytes 8r..8r+7); their scales
+    const int tr0 = tt + r, tr1 = tt + r + 8;
+    uint4 k0 = make_uint4(0, 0, 0, 0), k1 = make_uint4(0, 0, 0, 0);
+    if (tr0 < tn) k0 = __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr0) * (HD / 2)) + c);
+    if (tr1 < tn) k1 = __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr1) * (HD / 2)) + c);
+    const float ks0 = tr0 < tn ? __half2float(ksb[tr0]) : 0.f;
+    const float ks1 = tr1 < tn ? __half2float(ksb[tr1]) : 0.f;
+    const int tv[4] = {tt + 2 * c, tt + 2 * c + 1, tt + 2 * c + 8, tt + 2 * c + 9};
+    uint2 vw[4];
+    float vsc[4];
 #pragma unroll
-    for (int w = 1; w < DT / 32; ++w) m = fmaxf(m, red[w][tid]);
-    mrow[tid] = m;
-  }
-  __syncthreads();
-  // p = exp2(s - m); keep p * v_scale for the PV sweep, sum p for l
-  float lsum[G];
+    for (int u = 0; u < 4; ++u) {
+      vw[u] = tv[u] < tn ? __ldcs(reinterpret_cast<const uint2*>(vbase + int64_t(tv[u]) * (HD / 2)) + r)
+                         : make_uint2(0, 0);
+      vsc[u] = tv[u] < tn ? __half2float(vsb[tv[u]]) : 0.f;
+    }
+
+    // ---- scores
+    const uint32_t kw0[4] = {k0.x, k0.y, k0.z, k0.w};
+    const uint32_t kw1[4] = {k1.x, k1.y, k1.z, k1.w};
+    float sacc[NT][4];
 #pragma unroll
-  for (int hh = 0; hh < G; ++hh) lsum[hh] = 0.f;
-  for (int tok = tid; tok < tn; tok += DT) {
-    const float vsc = __half2float(vs[cache_row + t0 + tok]);
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float p = exp2f(sc[tok][hh] - mrow[hh]);
-      lsum[hh] += p;
-      sc[tok][hh] = p * vsc;
+      for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int wi = j >> 1, p0 = 2 * (j & 1);
+      const uint32_t a0 = byte_pair(kw0[wi], p0), a2 = byte_pair(kw0[wi], p0 + 1);
+      const uint32_t a1 = byte_pair(kw1[wi], p0), a3 = byte_pair(kw1[wi], p0 + 1);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816(sacc[nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+    }
+
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      // thread holds head 4 nt + c for tokens tr0 (sacc 0 + 1) and tr1 (sacc 2 + 3)
+      const float s0 = tr0 < tn ? (sacc[nt][0] + sacc[nt][1]) * ks0 : -INFINITY;
+      const float s1 = tr1 < tn ? (sacc[nt][2] + sacc[nt][3]) * ks1 : -INFINITY;
+      float mt = fmaxf(s0, s1);
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+      const float m_new = fmaxf(m_run[nt], mt);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m_run[nt] - m_use);
+      m_run[nt] = m_new;
+      const float P0 = exp2f(s0 - m_use), P1 = exp2f(s1 - m_use);
+      l_run[nt] = l_run[nt] * alpha + P0 + P1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][i][e] *= alpha;
+
+      // B fragment of P'^T: column n = r is head 4 nt + r/2 (hi for even r, lo
+      // for odd r); rows are tokens 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1).
+      const int src0 = 8 * c + (r >> 1), src1 = 8 * c + 4 + (r >> 1);
+      const float pv[4] = {__shfl_sync(0xffffffffu, P0, src0) * vsc[0], __shfl_sync(0xffffffffu, P0, src1) * vsc[1],
+                           __shfl_sync(0xffffffffu, P1, src0) * vsc[2], __shfl_sync(0xffffffffu, P1, src1) * vsc[3]};
+      __half ph[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __half hi = __float2half_rn(pv[u]);
+        ph[u] = (r & 1) ? __float2half_rn(pv[u] - __half2float(hi)) : hi;
+      }
+      const uint32_t pb0 = pack_h2(ph[0], ph[1]), pb1 = pack_h2(ph[2], ph[3]);
+      // ---- O^T += V^T P'^T over 8 m-tiles of 16 dims: m-tile i, row r is dim
+      // 16r + 2i, row r + 8 is dim 16r + 2i + 1 (byte i of the 8-byte chunk)
+      const uint32_t va[2] = {vw[0].x, vw[0].y}, vb[2] = {vw[1].x, vw[1].y};
+      const uint32_t vc[2] = {vw[2].x, vw[2].y}, vd[2] = {vw[3].x, vw[3].y};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t a0, a1, a2, a3;
+        byte_cross(va[i >> 2], vb[i >> 2], i & 3, a0, a1);
+        byte_cross(vc[i >> 2], vd[i >> 2], i & 3, a2, a3);
+        mma16816(o[nt][i], a0, a1, a2, a3, pb0, pb1);
+      }
     }
   }
+
+  // ---- merge the warps of the CTA, then write the split's partial state
 #pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    float l = lsum[hh];
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = nt * 4 + c;
+    float l = l_run[nt];
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    if (hh < G) {
+      if (r == 0) {
+        wm[wid][hh] = m_run[nt];
+        wl[wid][hh] = l;
+      }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) red[wid][hh] = l;
+      for (int i = 0; i < 8; ++i) {
+        wo[wid][hh][16 * r + 2 * i] = o[nt][i][0] + o[nt][i][1];
+        wo[wid][hh][16 * r + 2 * i + 1] = o[nt][i][2] + o[nt][i][3];
+      }
+    }
   }
   __syncthreads();
-  if (tid < G) {
-    float l = 0.f;
-#pragma unroll
-    for (int w = 0; w < DT / 32; ++w) l += red[w][tid];
-    lrow[tid] = l;
-  }
-  // PV: thread = output dim
-  float o[G];
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) o[hh] = 0.f;
-  const int e = tid;
-  for (int tok = 0; tok < tn; ++tok) {
-    const float vv = code_f(uint32_t(vcode[tok][e >> 1]) >> (4 * (e & 1)));
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) o[hh] = fmaf(sc[tok][hh], vv, o[hh]);
-  }
-  __syncthreads();
+  const int e = tid;  // output dim
   const int64_t base = (int64_t(b) * Hq + g * G) * splits + split;
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) m = fmaxf(m, wm[w][hh]);
+    const float m_use = m == -INFINITY ? 0.f : m;
+    float l = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = exp2f(wm[w][hh] - m_use);
+      l += f * wl[w][hh];
+      acc += f * wo[w][hh][e];
+    }
     const int64_t slot = base + int64_t(hh) * splits;
-    ws_o[slot * HD + e] = o[hh];
+    ws_o[slot * HD + e] = acc;
     if (tid == 0) {
-      ws_ml[slot * 2 + 0] = mrow[hh];
-      ws_ml[slot * 2 + 1] = lrow[hh];
+      ws_ml[slot * 2 + 0] = m;
+      ws_ml[slot * 2 + 1] = l;
     }
   }
 }
@@ -371,10 +488,10 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
                                   qscale, ws_o, ws_ml, splits);
   };
   switch (G) {
-    case 1: args(kv::decode_partial_kernel<1>); break;
-    case 2: args(kv::decode_partial_kernel<2>); break;
-    case 4: args(kv::decode_partial_kernel<4>); break;
-    case 8: args(kv::decode_partial_kernel<8>); break;
+    case 1: args(kv::decode_mma_kernel<1>); break;
+    case 2: args(kv::decode_mma_kernel<2>); break;
+    case 4: args(kv::decode_mma_kernel<4>); break;
+    case 8: args(kv::decode_mma_kernel<8>); break;
     default: return QUAROT_ERR_UNSUPPORTED;
   }
   kv::decode_combine_kernel<<<unsigned(B * Hq), kv::HD, 0, st>>>(ws_o, ws_ml, splits, unrotate_out,
