@@ -108,7 +108,7 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
 // ------------------------------------------------------------------ decode
 constexpr int HD = 128;       // head_dim of the decode kernel
 constexpr int MAXG = 8;       // query heads per KV head
-constexpr int CHUNK = 256;    // tokens per split
+constexpr int CHUNK = 256;    // smallest split; the workspace is sized for T / CHUNK splits
 constexpr int DT = 128;       // threads per CTA
 
 __host__ __device__ inline int64_t num_splits(int64_t T) {
@@ -166,7 +166,7 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 }
 
 // One CTA per (split, b, g): the partial softmax state of the group's G query
-// heads over CHUNK tokens, on tensor cores.  Four warps take 16-token tiles in
+// heads over `chunk` tokens (a multiple of 16), on tensor cores.  Four warps take 16-token tiles in
 // turn.  Per tile:
 //   scores  S^T[16 tok x 2G] = Kcodes[16 x 128] . Q~^T, m16n8k16 with the
 //           query split into fp16 hi and lo halves (the 2G columns), so the
@@ -179,23 +179,26 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 //           split into fp16 hi and lo columns; the output dims are permuted so
 //           each thread's value bytes are one 8-byte load per token.
 template <int G>
-__global__ void __launch_bounds__(DT)
+__global__ void __launch_bounds__(DT, 4)
 decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, const __half* __restrict__ ks,
                   const uint8_t* __restrict__ vq, const __half* __restrict__ vs, int Hq, int Hkv, int T,
-                  int T_max, float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits) {
+                  int T_max, float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits,
+                  int chunk) {
   constexpr int NT = (2 * G + 7) / 8;  // n8 tiles of (head, hi/lo) columns
   constexpr int NW = DT / 32;
-  __shared__ float qs[G][HD];
+  constexpr int QS = HD + 16;          // padded q~ row: dim d at d + 4 (d >> 5)
+  constexpr int WO = HD + 4;           // padded merge row
+  __shared__ __align__(16) float qs[G * QS];
   __shared__ float wm[NW][G], wl[NW][G];
-  __shared__ float wo[NW][G][HD];
+  __shared__ __align__(16) float wo[NW * G * WO];
 
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
   const int b = bg / Hkv, g = bg % Hkv;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int r = lane >> 2, c = lane & 3;
-  const int t0 = split * CHUNK;
-  const int tn = min(CHUNK, T - t0);
+  const int t0 = split * chunk;
+  const int tn = min(chunk, T - t0);
   const int64_t cache_row = (int64_t(b) * Hkv + g) * T_max + t0;
   const uint8_t* kbase = kq + cache_row * (HD / 2);
   const uint8_t* vbase = vq + cache_row * (HD / 2);
@@ -203,25 +206,26 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   const __half* vsb = vs + cache_row;
 
   // ---- q~ = q H / sqrt(d) * qscale (FWHT in shared memory)
+  auto qidx = [](int hh, int d) { return hh * QS + d + 4 * (d >> 5); };
   for (int i = tid; i < G * HD; i += DT) {
     const int hh = i / HD, e = i % HD;
-    qs[hh][e] = __half2float(q[(int64_t(b) * Hq + g * G + hh) * HD + e]);
+    qs[qidx(hh, e)] = __half2float(q[(int64_t(b) * Hq + g * G + hh) * HD + e]);
   }
   __syncthreads();
   for (int hspan = 1; hspan < HD; hspan <<= 1) {
     for (int i = tid; i < G * HD / 2; i += DT) {
       const int hh = i / (HD / 2), pr = i % (HD / 2);
       const int lo = (pr / hspan) * 2 * hspan + (pr % hspan);
-      const float a = qs[hh][lo], cc = qs[hh][lo + hspan];
-      qs[hh][lo] = a + cc;
-      qs[hh][lo + hspan] = a - cc;
+      const float a = qs[qidx(hh, lo)], cc = qs[qidx(hh, lo + hspan)];
+      qs[qidx(hh, lo)] = a + cc;
+      qs[qidx(hh, lo + hspan)] = a - cc;
     }
     __syncthreads();
   }
 
   // ---- B fragments of Q~^T: column n = lane/4 of n-tile nt is head (4 nt + n/2),
   // hi half for even n, lo half for odd n.  Step j uses head dims
-  // 32c + 4j + {0,1} (b0) and 32c + 4j + {2,3} (b1).
+  // 32c + 4j + {0,1} (b0) and 32c + 4j + {2,3} (b1): one 16-byte load.
   uint32_t qb[NT][8][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -229,17 +233,17 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     const bool lo_part = (r & 1) != 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
+      float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hh < G) x4 = *reinterpret_cast<const float4*>(&qs[qidx(hh, 32 * c + 4 * j)]);
+      const float xs[4] = {x4.x * qscale, x4.y * qscale, x4.z * qscale, x4.w * qscale};
+      __half e4[4];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        __half e2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float x = hh < G ? qs[hh][32 * c + 4 * j + 2 * half + e] * qscale : 0.f;
-          const __half hi = __float2half_rn(x);
-          e2[e] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
-        }
-        qb[nt][j][half] = pack_h2(e2[0], e2[1]);
+      for (int e = 0; e < 4; ++e) {
+        const __half hi = __float2half_rn(xs[e]);
+        e4[e] = lo_part ? __float2half_rn(xs[e] - __half2float(hi)) : hi;
       }
+      qb[nt][j][0] = pack_h2(e4[0], e4[1]);
+      qb[nt][j][1] = pack_h2(e4[2], e4[3]);
     }
   }
 
@@ -257,24 +261,37 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     l_run[nt] = 0.f;
   }
 
-  for (int tt = wid * 16; tt < tn; tt += NW * 16) {
-    // ---- loads: keys of tokens tt+r, tt+r+8 (bytes 16c..16c+15); values of
-    // tokens tt+2c, +1, +8, +9 (bytes 8r..8r+7); their scales
+  // ---- tiles of 16 tokens, warp-strided; the next tile's codes and scales
+  // are loaded while the current one is processed
+  auto load_tile = [&](int tt, uint4& k0, uint4& k1, float& ks0, float& ks1, uint2* vw, float* vsc) {
     const int tr0 = tt + r, tr1 = tt + r + 8;
-    uint4 k0 = make_uint4(0, 0, 0, 0), k1 = make_uint4(0, 0, 0, 0);
-    if (tr0 < tn) k0 = __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr0) * (HD / 2)) + c);
-    if (tr1 < tn) k1 = __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr1) * (HD / 2)) + c);
-    const float ks0 = tr0 < tn ? __half2float(ksb[tr0]) : 0.f;
-    const float ks1 = tr1 < tn ? __half2float(ksb[tr1]) : 0.f;
-    const int tv[4] = {tt + 2 * c, tt + 2 * c + 1, tt + 2 * c + 8, tt + 2 * c + 9};
+    k0 = tr0 < tn ? __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr0) * (HD / 2)) + c) : make_uint4(0, 0, 0, 0);
+    k1 = tr1 < tn ? __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr1) * (HD / 2)) + c) : make_uint4(0, 0, 0, 0);
+    ks0 = tr0 < tn ? __half2float(ksb[tr0]) : 0.f;
+    ks1 = tr1 < tn ? __half2float(ksb[tr1]) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int tv = tt + 2 * c + (u & 1) + 8 * (u >> 1);
+      vw[u] = tv < tn ? __ldcs(reinterpret_cast<const uint2*>(vbase + int64_t(tv) * (HD / 2)) + r) : make_uint2(0, 0);
+      vsc[u] = tv < tn ? __half2float(vsb[tv]) : 0.f;
+    }
+  };
+  uint4 nk0, nk1;
+  float nks0, nks1, nvsc[4];
+  uint2 nvw[4];
+  load_tile(wid * 16, nk0, nk1, nks0, nks1, nvw, nvsc);
+  for (int tt = wid * 16; tt < tn; tt += NW * 16) {
+    const int tr0 = tt + r, tr1 = tt + r + 8;
+    const uint4 k0 = nk0, k1 = nk1;
+    const float ks0 = nks0, ks1 = nks1;
     uint2 vw[4];
     float vsc[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      vw[u] = tv[u] < tn ? __ldcs(reinterpret_cast<const uint2*>(vbase + int64_t(tv[u]) * (HD / 2)) + r)
-                         : make_uint2(0, 0);
-      vsc[u] = tv[u] < tn ? __half2float(vsb[tv[u]]) : 0.f;
+      vw[u] = nvw[u];
+      vsc[u] = nvsc[u];
     }
+    if (tt + NW * 16 < tn) load_tile(tt + NW * 16, nk0, nk1, nks0, nks1, nvw, nvsc);
 
     // ---- scores
     const uint32_t kw0[4] = {k0.x, k0.y, k0.z, k0.w};
@@ -352,11 +369,10 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
         wm[wid][hh] = m_run[nt];
         wl[wid][hh] = l;
       }
+      float* wrow = wo + (wid * G + hh) * WO + 16 * r;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        wo[wid][hh][16 * r + 2 * i] = o[nt][i][0] + o[nt][i][1];
-        wo[wid][hh][16 * r + 2 * i + 1] = o[nt][i][2] + o[nt][i][3];
-      }
+      for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<float2*>(wrow + 2 * i) = make_float2(o[nt][i][0] + o[nt][i][1], o[nt][i][2] + o[nt][i][3]);
     }
   }
   __syncthreads();
@@ -373,7 +389,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     for (int w = 0; w < NW; ++w) {
       const float f = exp2f(wm[w][hh] - m_use);
       l += f * wl[w][hh];
-      acc += f * wo[w][hh][e];
+      acc += f * wo[(w * G + hh) * WO + e];
     }
     const int64_t slot = base + int64_t(hh) * splits;
     ws_o[slot * HD + e] = acc;
@@ -475,7 +491,16 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
       mis(workspace, 256))
     return QUAROT_ERR_ALIGNMENT;
   if (B * Hkv > 65535 || T > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
-  const int splits = int(kv::num_splits(T));
+  // Splits: enough CTAs to fill the GPU (about 4 per SM), never more than the
+  // workspace bound of one split per kv::CHUNK tokens; chunks are multiples of 16.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t max_splits = kv::num_splits(T);
+  int64_t want = (int64_t(4) * sms + B * Hkv - 1) / (B * Hkv);
+  want = want < 1 ? 1 : (want > max_splits ? max_splits : want);
+  int64_t chunk = (T + want - 1) / want;
+  chunk = (chunk + 15) / 16 * 16;
+  const int splits = int((T + chunk - 1) / chunk);
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(float(d));
   const float qscale = scale * 1.4426950408889634f / sqrtf(float(d));  // 1/sqrt(d) of H, log2(e)
   float* ws_o = static_cast<float*>(workspace);
@@ -485,7 +510,7 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   auto args = [&](auto kern) {
     kern<<<grid, kv::DT, 0, st>>>(static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q,
                                   static_cast<const __half*>(v_s), int(Hq), int(Hkv), int(T), int(T_max),
-                                  qscale, ws_o, ws_ml, splits);
+                                  qscale, ws_o, ws_ml, splits, int(chunk));
   };
   switch (G) {
     case 1: args(kv::decode_mma_kernel<1>); break;

@@ -234,6 +234,247 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
   }
 }
 
+// ===================================================================== d = m x 1024
+// Segment kernel for the hot widths d = 4096 (m = 4, Sylvester: H4 (x) H1024)
+// and d = 12288 (m = 12, H12 (x) H1024).  Four warps own a row; warp w owns
+// segments a = w * m/4 .. of 1024 elements.
+//   round 1  lane l loads 16-byte chunks l + 32 i (i = 0..3) of its segment:
+//            element bits {0,1,2} (within the chunk) and {8,9} (i) are local;
+//            sign flip on the fp16 bits, 32-point FWHT in registers, store to
+//            a swizzled fp32 segment in shared memory;
+//   round 2  lane l re-reads the 32 elements whose bits {0,1,2,8,9} equal l and
+//            runs the 32-point FWHT over bits 3..7, stores back;
+//   round 3  thread t takes elements 8t .. 8t+7 of every segment, applies the
+//            m-point transform across segments (H4, or Paley-12 in the form
+//            y_0 = x_0 - T, y_{j+1} = 2 (z_j + A_j) + y_0 with z = x_1..x_11,
+//            T = sum z and A_j = sum of z_{j-r} over the quadratic residues r
+//            of 11), then abs-max, fp16 scale, round, clamp and pack: one
+//            32-bit store per segment.
+// Packed fp32x2 arithmetic (__fadd2_rn / __ffma2_rn) carries the butterflies.
+// Shared-memory layout: float4 slot V of a segment lives at
+// V ^ (((V >> 6) & 3) << 1) ^ ((V >> 3) & 1), which keeps the 16-byte
+// stores of round 1, the strided scalar loads of round 2 and the 16-byte loads
+// of round 3 free of bank conflicts.
+__device__ __forceinline__ int seg_swz(int V) { return V ^ (((V >> 6) & 3) << 1) ^ ((V >> 3) & 1); }
+
+__device__ __forceinline__ void bfly2(float2& a, float2& b) {
+  const float2 s = __fadd2_rn(a, b);
+  b = __ffma2_rn(b, make_float2(-1.f, -1.f), a);
+  a = s;
+}
+__device__ __forceinline__ void bfly_in(float2& a) {  // (x, y) -> (x + y, x - y)
+  const float x = a.x, y = a.y;
+  a = make_float2(x + y, x - y);
+}
+
+// 32-point FWHT of p[16] holding elements (2n, 2n+1) in p[n]: bit 0 inside
+// each pair, bits 1..4 across pairs.
+__device__ __forceinline__ void fwht32_pairs(float2* p) {
+#pragma unroll
+  for (int n = 0; n < 16; ++n) bfly_in(p[n]);
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+      if ((n & h) == 0) bfly2(p[n], p[n + h]);
+}
+
+template <int MSEG>
+struct SegPlan {
+  static constexpr int D = MSEG * 1024;
+  static constexpr int TPR = 128;
+  static constexpr int SPW = MSEG / 4;  // segments per warp
+  static constexpr int RPC = MSEG == 4 ? 2 : 1;
+  static constexpr int NT = TPR * RPC;
+  static constexpr size_t SMEM = size_t(RPC) * D * 4 + 64 * 4;
+};
+
+template <int MSEG>
+__global__ void __launch_bounds__(SegPlan<MSEG>::NT)
+rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
+                        float clip_ratio, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
+                        float* __restrict__ rot_out) {
+  using PL = SegPlan<MSEG>;
+  constexpr int D = PL::D;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* red = reinterpret_cast<float*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int r_local = tid / PL::TPR;
+  const int t = tid % PL::TPR;
+  const int lane = t & 31, w = t >> 5;
+  float4* buf = reinterpret_cast<float4*>(smem_raw + 64 * 4) + size_t(r_local) * (D / 4);
+  const int64_t row = int64_t(blockIdx.x) * PL::RPC + r_local;
+  const bool valid = row < M;
+  const __half* xr = x + (valid ? row : 0) * ld_x;
+
+  // ---- round 1
+#pragma unroll 1
+  for (int sgi = 0; sgi < PL::SPW; ++sgi) {
+    const int a = w * PL::SPW + sgi;
+    float2 p[16];  // p[4 i + jj] = elements (2 jj, 2 jj + 1) of chunk lane + 32 i
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int chunk = lane + 32 * i;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (valid) raw = __ldcs(reinterpret_cast<const uint4*>(xr + a * 1024 + 8 * chunk));
+      if (signs != nullptr) {
+        const uint2 sg = __ldg(reinterpret_cast<const uint2*>(signs + a * 1024 + 8 * chunk));
+        // sign bit of byte k of the sign word -> bit 15 / 31 of the fp16 pair
+        raw.x ^= __byte_perm(sg.x, 0u, 0x1404) & 0x80008000u;
+        raw.y ^= __byte_perm(sg.x, 0u, 0x3424) & 0x80008000u;
+        raw.z ^= __byte_perm(sg.y, 0u, 0x1404) & 0x80008000u;
+        raw.w ^= __byte_perm(sg.y, 0u, 0x3424) & 0x80008000u;
+      }
+      p[4 * i + 0] = h2_to_f2(raw.x);
+      p[4 * i + 1] = h2_to_f2(raw.y);
+      p[4 * i + 2] = h2_to_f2(raw.z);
+      p[4 * i + 3] = h2_to_f2(raw.w);
+    }
+    fwht32_pairs(p);  // pair index n = 4 i + jj: bits 1,2 = jj, bits 3,4 = i
+    float4* seg = buf + a * 256;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int V0 = 2 * (lane + 32 * i);
+      seg[seg_swz(V0)] = make_float4(p[4 * i].x, p[4 * i].y, p[4 * i + 1].x, p[4 * i + 1].y);
+      seg[seg_swz(V0 + 1)] = make_float4(p[4 * i + 2].x, p[4 * i + 2].y, p[4 * i + 3].x, p[4 * i + 3].y);
+    }
+  }
+  __syncwarp();
+
+  // ---- round 2: bits 3..7; element e = (lane & 7) + 8 k + 256 (lane >> 3)
+  {
+    const int lh = lane >> 3;
+    const int base0 = ((lane & 7) >> 2) | (lh << 6);  // float4 slot bits 0 and 6,7
+    int addr[2][4];
+#pragma unroll
+    for (int par = 0; par < 2; ++par)
+#pragma unroll
+      for (int kl = 0; kl < 4; ++kl) addr[par][kl] = ((base0 ^ par) + 2 * (kl ^ lh)) * 4 + (lane & 3);
+#pragma unroll 1
+    for (int sgi = 0; sgi < PL::SPW; ++sgi) {
+      const int a = w * PL::SPW + sgi;
+      float* seg = reinterpret_cast<float*>(buf + a * 256);
+      float2 p[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        // slot of element k: ((base0 ^ (k >> 2 & 1)) + 2 ((k & 3) ^ lh) + 8 (k >> 2)) * 4 + (lane & 3)
+        const float v0 = seg[addr[(k >> 2) & 1][k & 3] + 32 * (k >> 2)];
+        const float v1 = seg[addr[(k >> 2) & 1][(k + 1) & 3] + 32 * (k >> 2)];
+        p[k >> 1] = make_float2(v0, v1);
+      }
+      fwht32_pairs(p);
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        seg[addr[(k >> 2) & 1][k & 3] + 32 * (k >> 2)] = p[k >> 1].x;
+        seg[addr[(k >> 2) & 1][(k + 1) & 3] + 32 * (k >> 2)] = p[k >> 1].y;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- round 3: cross-segment transform on elements 8t .. 8t+7
+  float2 v[MSEG][4];
+#pragma unroll
+  for (int a = 0; a < MSEG; ++a) {
+    const float4 lo = buf[a * 256 + seg_swz(2 * t)];
+    const float4 hi = buf[a * 256 + seg_swz(2 * t + 1)];
+    v[a][0] = make_float2(lo.x, lo.y);
+    v[a][1] = make_float2(lo.z, lo.w);
+    v[a][2] = make_float2(hi.x, hi.y);
+    v[a][3] = make_float2(hi.z, hi.w);
+  }
+  if constexpr (MSEG == 4) {
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      bfly2(v[0][jj], v[1][jj]);
+      bfly2(v[2][jj], v[3][jj]);
+      bfly2(v[0][jj], v[2][jj]);
+      bfly2(v[1][jj], v[3][jj]);
+    }
+  } else {
+    // Paley-12: z_j = v[1 + j], T = sum z, A_j = z_{j-1} + z_{j-3} + z_{j-4} + z_{j-5} + z_{j-9}
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      float2 z[11];
+#pragma unroll
+      for (int j = 0; j < 11; ++j) z[j] = v[1 + j][jj];
+      float2 T = z[0];
+#pragma unroll
+      for (int j = 1; j < 11; ++j) T = __fadd2_rn(T, z[j]);
+      const float2 y0 = __ffma2_rn(T, make_float2(-1.f, -1.f), v[0][jj]);
+      v[0][jj] = y0;
+#pragma unroll
+      for (int j = 0; j < 11; ++j) {
+        float2 A = __fadd2_rn(z[(j + 10) % 11], z[(j + 8) % 11]);
+        A = __fadd2_rn(A, z[(j + 7) % 11]);
+        A = __fadd2_rn(A, z[(j + 6) % 11]);
+        A = __fadd2_rn(A, z[(j + 2) % 11]);
+        A = __fadd2_rn(A, z[j]);
+        v[1 + j][jj] = __ffma2_rn(A, make_float2(2.f, 2.f), y0);
+      }
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int a = 0; a < MSEG; ++a)
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) amax = fmaxf(amax, fmaxf(fabsf(v[a][jj].x), fabsf(v[a][jj].y)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[r_local * 4 + w] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[r_local * 4], red[r_local * 4 + 1]), fmaxf(red[r_local * 4 + 2], red[r_local * 4 + 3]));
+  // 1/sqrt(d): 1/64 for 4096; the correctly rounded quotient for 12288
+  const float inv_sqrt_d = MSEG == 4 ? (1.0f / 64.0f) : 1.0f / sqrtf(float(D));
+  const __half S = quant_scale_fp16(amax * inv_sqrt_d, clip_ratio);
+  const float f = inv_sqrt_d * (1.0f / __half2float(S));
+  if (valid && t == 0) scale_out[row] = S;
+  if (valid) {
+    uint32_t* qrow = reinterpret_cast<uint32_t*>(q_out + row * (D / 2));
+    const float2 fv = make_float2(f, f);
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
+#pragma unroll
+    for (int a = 0; a < MSEG; ++a) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        float2 yv = __fmul2_rn(v[a][jj], fv);
+        yv.x = fminf(fmaxf(yv.x, -8.0f), 7.0f);
+        yv.y = fminf(fmaxf(yv.y, -8.0f), 7.0f);
+        const float2 rr = __fadd2_rn(yv, magic);
+        word |= (uint32_t(__float_as_int(rr.x)) & 0xFu) << (8 * jj);
+        word |= (uint32_t(__float_as_int(rr.y)) & 0xFu) << (8 * jj + 4);
+      }
+      __stcs(qrow + a * 128 + t, word);
+      if (rot_out != nullptr) {
+        float4* ro = reinterpret_cast<float4*>(rot_out + row * D + a * 1024 + 8 * t);
+        ro[0] = make_float4(v[a][0].x * inv_sqrt_d, v[a][0].y * inv_sqrt_d, v[a][1].x * inv_sqrt_d,
+                            v[a][1].y * inv_sqrt_d);
+        ro[1] = make_float4(v[a][2].x * inv_sqrt_d, v[a][2].y * inv_sqrt_d, v[a][3].x * inv_sqrt_d,
+                            v[a][3].y * inv_sqrt_d);
+      }
+    }
+  }
+}
+
+template <int MSEG>
+static int launch_seg(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, uint8_t* q,
+                      void* s, float* rot, cudaStream_t st) {
+  using PL = SegPlan<MSEG>;
+  auto kern = rotate_quant_seg_kernel<MSEG>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PL::SMEM)) != cudaSuccess)
+      return QUAROT_ERR_LAUNCH;
+    attr_set = true;
+  }
+  const int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
+  if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
+  kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(static_cast<const __half*>(x), M, ld_x, signs, clip,
+                                                                q, static_cast<__half*>(s), rot);
+  return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
 template <int LOGP, bool M12>
 static int launch_rq(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip,
                      uint8_t* q, void* s, float* rot, cudaStream_t st) {
@@ -278,11 +519,11 @@ extern "C" int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t 
     case 512: return launch_rq<9, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 1024: return launch_rq<10, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 2048: return launch_rq<11, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 4096: return launch_rq<12, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
+    case 4096: return launch_seg<4>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 8192: return launch_rq<13, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 3072: return launch_rq<8, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 6144: return launch_rq<9, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 12288: return launch_rq<10, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
+    case 12288: return launch_seg<12>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     default: return QUAROT_ERR_UNSUPPORTED;
   }
 }
