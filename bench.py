@@ -207,38 +207,65 @@ def run_ours(args):
     flush = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    EV = 5  # events per step: start, after rotate, after gemm, after kv_write, after decode
+    # The four stages of a step.  Each is launched through the C ABI on the
+    # current stream; the timed loop replays them from CUDA graphs so that the
+    # device time is not diluted by Python launch gaps.
+    def s_rot():
+        q.quarot_rotate_quant(xt, st, q_out=aq, scale_out=asx)
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        q.quarot_rotate_quant(xt, st, q_out=aq, scale_out=asx, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        q.quarot_w4a4_gemm(aq, asx, wq, wsc, y=y, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        q.quarot_kv_write(k_new, v_new, T - 1, *cache, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
-        q.quarot_decode_attn(q_dec, *cache, T=T, out=out, workspace=wsp, stream=stream)
-        if ev is not None:
-            ev[4].record(stream)
+    def s_gemm():
+        q.quarot_w4a4_gemm(aq, asx, wq, wsc, y=y)
 
+    def s_kvw():
+        q.quarot_kv_write(k_new, v_new, T - 1, *cache)
+
+    def s_dec():
+        q.quarot_decode_attn(q_dec, *cache, T=T, out=out, workspace=wsp)
+
+    stages_fn = [s_rot, s_gemm, s_kvw, s_dec]
     LAUNCHES_PER_STEP = 1 + 1 + 1 + 2
+
+    def step():
+        for f in stages_fn:
+            f()
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
     q.quarot_check_error(stream)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(EV)] for _ in range(args.steps)]
+    graphs = None
+    try:
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            step()
+        g_stage = []
+        for f in stages_fn:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                f()
+            g_stage.append(g)
+        graphs = (g_step, g_stage)
+    except Exception as exc:  # graph capture unavailable: time direct launches
+        print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
+    run_step = graphs[0].replay if graphs else step
+    run_stage = [g.replay for g in graphs[1]] if graphs else stages_fn
+    for _ in range(2):
+        flush.zero_()
+        run_step()
+    torch.cuda.synchronize()
+    q.quarot_check_error(stream)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.zero_()  # L2 flush between timed steps (outside the step's events)
-            step(evs[i])
+            evs[i][0].record(stream)
+            run_step()
+            evs[i][1].record(stream)
         torch.cuda.synchronize()
         timed_samples = len(clocks.lines)
         # a short timed region may end before nvidia-smi reports: keep the same
@@ -247,11 +274,10 @@ def run_ours(args):
         while len(clocks.lines) < timed_samples + 5 and time.time() < t_end:
             for _ in range(50):
                 flush.zero_()
-                step()
+                run_step()
             torch.cuda.synchronize()
     q.quarot_check_error(stream)
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(EV - 1)] for i in range(args.steps)])
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([a.elapsed_time(b) for a, b in evs])
     total_ms = float(step_ms.sum())
     if ws > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -259,7 +285,20 @@ def run_ours(args):
         total_ms = float(t.item())
         dist.barrier()
     value = ws * M_TOK * args.steps / (total_ms / 1000.0)
-    stage_ms = per.mean(axis=0)
+
+    # per-stage device times (same cold-L2 protocol, each stage replayed alone)
+    reps = max(10, min(args.steps, 100))
+    stage_ms = []
+    for f in run_stage:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            f()
+            b.record(stream)
+        torch.cuda.synchronize()
+        stage_ms.append(float(np.mean([a.elapsed_time(b) for a, b in ev])))
+    stage_ms = np.array(stage_ms)
 
     # ---------------- e2e: host buffers through the C ABI, copies inside the timed region
     x_h = torch.from_numpy(x).pin_memory()
@@ -323,7 +362,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int4+f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens_per_step": M_TOK, "l2": "flushed between steps (2x L2 write)",
-                   "parallelism": f"replicas x{ws}"},
+                   "parallelism": f"replicas x{ws}", "launch": "CUDA graph per step" if graphs else "direct"},
         "roofline": {"bound": "tensor", "kernel": "w4a4_gemm", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": None,
                      "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio)"},
