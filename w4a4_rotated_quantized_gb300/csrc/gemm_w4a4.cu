@@ -27,13 +27,17 @@
 // Persistent kernel, one CTA per SM, 576 threads in five roles:
 //   warp 0        TMA producer: packed A/W k-blocks into a 4-stage ring (64B swizzle)
 //   warp 1        TMEM allocator and single-thread MMA issuer
-//   warps 2-13    converters: packed nibbles -> e4m3 bytes in a 2-stage ring laid
-//                 out for the 128B-swizzled K-major UMMA descriptors, plus the
-//                 offset-code row sums of the tile
+//   warps 2-5     A converters: packed nibbles -> e4m3 bytes written straight
+//                 into tensor memory (tcgen05.st), the MMA's A operand, 2 stages
+//   warps 6-13    W converters: packed nibbles -> e4m3 bytes in a 2-stage
+//                 shared-memory ring laid out for the 128B-swizzled K-major
+//                 UMMA descriptor; both converter groups also sum the offset
+//                 codes of their rows
 //   warps 14-17   epilogue: TMEM -> registers -> integer correction -> fp16
-// Tiles are 128 x BN (BN in {128..256} chosen per shape so the tiles split
-// evenly over the SMs); two TMEM accumulators let the epilogue of one tile
-// overlap the main loop of the next.  Every wait is bounded; an expired wait
+// Tiles are 128 x BN (BN in {128..224} chosen per shape so the tiles split
+// evenly over the SMs).  Tensor memory holds two accumulators (columns
+// [0, BN) and [BN, 2 BN)), so the epilogue of one tile overlaps the main loop
+// of the next, and the two A stages (columns 448.. and 480..).  Every wait is bounded; an expired wait
 // records QUAROT_ERR_TIMEOUT and the CTA drains its copies and MMAs, frees
 // TMEM and returns.
 #include <cuda.h>
@@ -46,28 +50,30 @@
 namespace quarot {
 namespace gemm {
 
-constexpr int BM = 128, BN_MAX = 256, BK = 128;  // tile in codes
+constexpr int BM = 128, BN_MAX = 224, BK = 128;  // tile in codes
 constexpr int BKB = BK / 2;                      // packed bytes per row per k-block
-constexpr int SP = 4;                            // packed ring stages
-constexpr int SU = 2;                            // unpacked ring stages
+constexpr int SP = 6;                            // packed ring stages
+constexpr int SU = 2;                            // unpacked ring stages (A in TMEM, W in smem)
 constexpr int NCONV = 384;                       // converter threads (12 warps)
 constexpr int NEPI = 128;                        // epilogue threads (4 warps)
 constexpr int EPI_WARP0 = 2 + NCONV / 32;        // 14
 constexpr int NTHREADS = 64 + NCONV + NEPI;      // 576
-constexpr int A_PK = BM * BKB, B_PK = BN_MAX * BKB;  // 8 KB, 16 KB
-constexpr int A_UN = BM * BK, B_UN = BN_MAX * BK;    // 16 KB, 32 KB
-constexpr int OFF_AU = 0;
-constexpr int OFF_BU = OFF_AU + SU * A_UN;
+constexpr int A_PK = BM * BKB, B_PK = BN_MAX * BKB;  // 8 KB, 14 KB
+constexpr int B_UN = BN_MAX * BK;                    // 28 KB
+constexpr int OFF_BU = 0;
 constexpr int OFF_AP = OFF_BU + SU * B_UN;
 constexpr int OFF_BP = OFF_AP + SP * A_PK;
-constexpr int OFF_BAR = OFF_BP + SP * B_PK;  // 196608
+constexpr int OFF_BAR = OFF_BP + SP * B_PK;
 constexpr int NBAR = 2 * SP + 2 * SU + 8 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int OFF_RSA = OFF_MISC + 16;             // int [2][BM]
 constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;      // int [2][BN_MAX]
 constexpr int SMEM_USED = OFF_RSB + 2 * BN_MAX * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
-constexpr uint32_t TMEM_COLS = 512;           // two accumulators of up to 256 columns
+constexpr uint32_t TMEM_COLS = 512;           // two accumulators of up to 224 columns + A stages
+constexpr uint32_t TMEM_A_COL = 448;          // A stage s at column 448 + 32 s (128 bytes per row)
+constexpr int NCONV_WARPS = NCONV / 32;       // arrivals per converter barrier phase
+constexpr int NEPI_WARPS = NEPI / 32;
 constexpr int MAX_K = 65536;
 
 // Instruction descriptor, kind::f8f6f4: D fp32, A/B e4m3, both K-major,
@@ -103,6 +109,15 @@ __device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+__device__ __forceinline__ void mma_f8_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
@@ -126,6 +141,17 @@ __device__ __forceinline__ void fence_after_sync() {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),             \
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])              \
       : "r"(taddr))
+
+#define QUAROT_TMEM_ST32(taddr, r)                                                                 \
+  asm volatile(                                                                                    \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),       \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),     \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), \
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),          \
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),          \
+      "r"(r[30]), "r"(r[31])                                                                       \
+      : "memory")
 
 // 8 packed codes (one 32-bit word) -> 8 offset codes as bytes, order
 // (0,2,4,6 | 1,3,5,7); also returns their byte-wise sum word.
@@ -152,6 +178,28 @@ __device__ __forceinline__ uint32_t convert_row(const unsigned char* src_row, in
     acc = __dp4a((l0 + h0) + (l1 + h1) + (l2 + h2) + (l3 + h3), 0x01010101u, acc);
     *reinterpret_cast<uint4*>(dst_row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
     *reinterpret_cast<uint4*>(dst_row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
+  }
+  return acc;
+}
+
+static_assert(OFF_AP % 1024 == 0 && OFF_BP % 1024 == 0 && OFF_BAR % 8 == 0, "stage alignment");
+
+// The A-side variant: the 128 converted bytes of the row go to 32 registers
+// (K order identical to convert_row) for one tcgen05.st.
+__device__ __forceinline__ uint32_t convert_row_regs(const unsigned char* src_row, int r, uint32_t* o) {
+  uint4 w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(src_row + ((c ^ ((r >> 1) & 3)) << 4));
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    unpack_word(w[c].x, o[8 * c + 0], o[8 * c + 1]);
+    unpack_word(w[c].y, o[8 * c + 2], o[8 * c + 3]);
+    unpack_word(w[c].z, o[8 * c + 4], o[8 * c + 5]);
+    unpack_word(w[c].w, o[8 * c + 6], o[8 * c + 7]);
+    acc = __dp4a((o[8 * c] + o[8 * c + 1]) + (o[8 * c + 2] + o[8 * c + 3]) + (o[8 * c + 4] + o[8 * c + 5]) +
+                     (o[8 * c + 6] + o[8 * c + 7]),
+                 0x01010101u, acc);
   }
   return acc;
 }
@@ -188,17 +236,17 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   if (threadIdx.x == 0) {
     for (int s = 0; s < SP; ++s) {
       mbar_init(&pk_full[s], 1);
-      mbar_init(&pk_empty[s], NCONV);
+      mbar_init(&pk_empty[s], NCONV_WARPS);
     }
     for (int s = 0; s < SU; ++s) {
-      mbar_init(&un_full[s], NCONV);
+      mbar_init(&un_full[s], NCONV_WARPS);
       mbar_init(&un_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], NEPI);
-      mbar_init(&rs_full[s], NCONV);
-      mbar_init(&rs_empty[s], NEPI);
+      mbar_init(&acc_empty[s], NEPI_WARPS);
+      mbar_init(&rs_full[s], NCONV_WARPS);
+      mbar_init(&rs_empty[s], NEPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -247,7 +295,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int a = ti & 1;
         if (!mbar_wait_bounded(&acc_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
         fence_after_sync();
-        const uint32_t tmem_d = tmem_base + uint32_t(a * BN_MAX);
+        const uint32_t tmem_d = tmem_base + uint32_t(a * BN);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = int(it % SU);
@@ -256,11 +304,11 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             break;
           }
           fence_after_sync();
-          const uint64_t ad = sw128_desc(smem_u32(sm + OFF_AU + s * A_UN));
+          const uint32_t ta = tmem_base + TMEM_A_COL + uint32_t(32 * s);
           const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + s * B_UN));
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)
-            mma_f8(tmem_d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
+            mma_f8_ts(tmem_d, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
           mma_commit(&un_empty[s]);
         }
         if (!ok) break;
@@ -272,9 +320,11 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
   } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 64;  // 0..383
-    const bool is_a = ct < BM;
-    const int r = is_a ? ct : ct - BM;
+    // warps 2-5: A rows 32 * (warp % 4) + lane (the TMEM lane quadrant the warp
+    // may access); warps 6-13: W rows 0..255
+    const bool is_a = warp < 6;
+    const int r = is_a ? 32 * (warp & 3) + lane : int(threadIdx.x) - 64 - BM;
+    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16);
     long it = 0;
     int ti = 0;
     for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
@@ -288,20 +338,28 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           break;
         }
         if (is_a) {
-          sum += convert_row(sm + OFF_AP + sp * A_PK + r * 64, r, sm + OFF_AU + su * A_UN + r * 128);
-        } else if (r < BN) {
-          sum += convert_row(sm + OFF_BP + sp * B_PK + r * 64, r, sm + OFF_BU + su * B_UN + r * 128);
+          uint32_t o[32];
+          sum += convert_row_regs(sm + OFF_AP + sp * A_PK + r * 64, r, o);
+          QUAROT_TMEM_ST32(tmem_a_row + uint32_t(32 * su), o);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          fence_before_sync();
+        } else {
+          if (r < BN) sum += convert_row(sm + OFF_BP + sp * B_PK + r * 64, r, sm + OFF_BU + su * B_UN + r * 128);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&un_full[su]);
-        mbar_arrive(&pk_empty[sp]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&un_full[su]);
+          mbar_arrive(&pk_empty[sp]);
+        }
       }
       if (!ok) break;
       const int a = ti & 1;
       if (!mbar_wait_bounded(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
       if (is_a) rsA[a * BM + r] = int(sum);
-      else rsB[a * BN_MAX + r] = int(sum);
-      mbar_arrive(&rs_full[a]);
+      else if (r < BN_MAX) rsB[a * BN_MAX + r] = int(sum);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs_full[a]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -320,7 +378,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
       const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[a * BM + r]);
       const int* rsb = rsB + a * BN_MAX;
-      const uint32_t tmem_row = tmem_base + uint32_t(a * BN_MAX) + (uint32_t(32 * q) << 16);
+      const uint32_t tmem_row = tmem_base + uint32_t(a * BN) + (uint32_t(32 * q) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
@@ -360,8 +418,11 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
       }
       fence_before_sync();
-      mbar_arrive(&acc_empty[a]);
-      mbar_arrive(&rs_empty[a]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&acc_empty[a]);
+        mbar_arrive(&rs_empty[a]);
+      }
     }
   }
 
@@ -403,8 +464,8 @@ static bool make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K,
 // Tile width for the N dimension: the candidate with the smallest per-SM
 // makespan (tiles per SM x width), larger widths first on ties.
 static int pick_bn(int64_t M, int64_t N, int sms) {
-  const int cands[5] = {256, 224, 192, 160, 128};
-  int best = 256;
+  const int cands[4] = {224, 192, 160, 128};
+  int best = 224;
   int64_t best_cost = -1;
   const int64_t mt = (M + BM - 1) / BM;
   for (int bn : cands) {
