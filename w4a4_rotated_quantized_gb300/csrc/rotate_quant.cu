@@ -279,22 +279,36 @@ __device__ __forceinline__ void fwht32_pairs(float2* p) {
       if ((n & h) == 0) bfly2(p[n], p[n + h]);
 }
 
-template <int MSEG>
+template <int MSEG, bool STAGED>
 struct SegPlan {
   static constexpr int D = MSEG * 1024;
   static constexpr int TPR = 128;
   static constexpr int SPW = MSEG / 4;  // segments per warp
-  static constexpr int RPC = MSEG == 4 ? 2 : 1;
+  static constexpr int RPC = STAGED ? 1 : 2;
   static constexpr int NT = TPR * RPC;
-  static constexpr size_t SMEM = size_t(RPC) * D * 4 + 64 * 4;
+  // [red 256 B][fp32 rows][fp16 staging row (STAGED)][mbarrier (STAGED)]
+  static constexpr size_t OFF_BUF = 64 * 4;
+  static constexpr size_t OFF_STAGE = OFF_BUF + size_t(RPC) * D * 4;
+  static constexpr size_t OFF_MBAR = OFF_STAGE + (STAGED ? size_t(D) * 2 : 0);
+  static constexpr size_t SMEM = OFF_MBAR + 16;
 };
 
-template <int MSEG>
-__global__ void __launch_bounds__(SegPlan<MSEG>::NT)
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// STAGED = true: persistent CTAs, one row at a time; while a row runs rounds 2
+// and 3, the next row's fp16 data arrives in a staging buffer by a bulk
+// asynchronous copy, so the load latency of one row hides behind the
+// arithmetic of the previous one.
+template <int MSEG, bool STAGED>
+__global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT)
 rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
                         float clip_ratio, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
                         float* __restrict__ rot_out) {
-  using PL = SegPlan<MSEG>;
+  using PL = SegPlan<MSEG, STAGED>;
   constexpr int D = PL::D;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* red = reinterpret_cast<float*>(smem_raw);
@@ -302,8 +316,29 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   const int r_local = tid / PL::TPR;
   const int t = tid % PL::TPR;
   const int lane = t & 31, w = t >> 5;
-  float4* buf = reinterpret_cast<float4*>(smem_raw + 64 * 4) + size_t(r_local) * (D / 4);
-  const int64_t row = int64_t(blockIdx.x) * PL::RPC + r_local;
+  float4* buf = reinterpret_cast<float4*>(smem_raw + PL::OFF_BUF) + size_t(r_local) * (D / 4);
+  const __half* stage = reinterpret_cast<const __half*>(smem_raw + PL::OFF_STAGE);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_raw + PL::OFF_MBAR);
+  const int64_t row_stride = STAGED ? int64_t(gridDim.x) : int64_t(0);
+  int64_t row = STAGED ? int64_t(blockIdx.x) : int64_t(blockIdx.x) * PL::RPC + r_local;
+  if constexpr (STAGED) {
+    if (tid == 0) {
+      mbar_init(mbar, 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0 && row < M) {
+      mbar_arrive_expect_tx(mbar, uint32_t(D) * 2u);
+      bulk_copy_g2s(smem_u32(stage), x + row * ld_x, uint32_t(D) * 2u, mbar);
+    }
+  }
+  for (int it = 0;; ++it, row += row_stride) {
+  if constexpr (STAGED) {
+    if (row >= M) break;
+    if (!mbar_wait_bounded(mbar, uint32_t(it & 1), nullptr)) break;
+  } else {
+    if (it > 0) break;
+  }
   const bool valid = row < M;
   const __half* xr = x + (valid ? row : 0) * ld_x;
 
@@ -316,7 +351,8 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     for (int i = 0; i < 4; ++i) {
       const int chunk = lane + 32 * i;
       uint4 raw = make_uint4(0, 0, 0, 0);
-      if (valid) raw = __ldcs(reinterpret_cast<const uint4*>(xr + a * 1024 + 8 * chunk));
+      if constexpr (STAGED) raw = *reinterpret_cast<const uint4*>(stage + a * 1024 + 8 * chunk);
+      else if (valid) raw = __ldcs(reinterpret_cast<const uint4*>(xr + a * 1024 + 8 * chunk));
       if (signs != nullptr) {
         const uint2 sg = __ldg(reinterpret_cast<const uint2*>(signs + a * 1024 + 8 * chunk));
         // sign bit of byte k of the sign word -> bit 15 / 31 of the fp16 pair
@@ -371,6 +407,14 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     }
   }
   __syncthreads();
+  if constexpr (STAGED) {
+    // every warp is past round 1: the staging buffer may take the next row
+    const int64_t next = row + row_stride;
+    if (tid == 0 && next < M) {
+      mbar_arrive_expect_tx(mbar, uint32_t(D) * 2u);
+      bulk_copy_g2s(smem_u32(stage), x + next * ld_x, uint32_t(D) * 2u, mbar);
+    }
+  }
 
   // ---- round 3: cross-segment transform on elements 8t .. 8t+7
   float2 v[MSEG][4];
@@ -455,20 +499,32 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
       }
     }
   }
+  }  // row loop
 }
 
-template <int MSEG>
+template <int MSEG, bool STAGED>
 static int launch_seg(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, uint8_t* q,
                       void* s, float* rot, cudaStream_t st) {
-  using PL = SegPlan<MSEG>;
-  auto kern = rotate_quant_seg_kernel<MSEG>;
+  using PL = SegPlan<MSEG, STAGED>;
+  auto kern = rotate_quant_seg_kernel<MSEG, STAGED>;
   static bool attr_set = false;
+  static int per_sm = 1;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PL::SMEM)) != cudaSuccess)
       return QUAROT_ERR_LAUNCH;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PL::NT, PL::SMEM) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
     attr_set = true;
   }
-  const int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
+  int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
+  if constexpr (STAGED) {
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QUAROT_ERR_CUDA;
+    const int64_t cap = int64_t(sms) * per_sm;
+    blocks = blocks < cap ? blocks : cap;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || ((ld_x * 2) & 15)) return QUAROT_ERR_ALIGNMENT;
+  }
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(static_cast<const __half*>(x), M, ld_x, signs, clip,
                                                                 q, static_cast<__half*>(s), rot);
@@ -519,11 +575,11 @@ extern "C" int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t 
     case 512: return launch_rq<9, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 1024: return launch_rq<10, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 2048: return launch_rq<11, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 4096: return launch_seg<4>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
+    case 4096: return launch_seg<4, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 8192: return launch_rq<13, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 3072: return launch_rq<8, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     case 6144: return launch_rq<9, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 12288: return launch_seg<12>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
+    case 12288: return launch_seg<12, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
     default: return QUAROT_ERR_UNSUPPORTED;
   }
 }
