@@ -35,9 +35,11 @@
 //                 codes of their rows
 //   warps 14-17   epilogue: TMEM -> registers -> integer correction -> fp16
 // Tiles are 128 x BN (BN in {128..224} chosen per shape so the tiles split
-// evenly over the SMs).  Tensor memory holds two accumulators (columns
-// [0, BN) and [BN, 2 BN)), so the epilogue of one tile overlaps the main loop
-// of the next, and the two A stages (columns 448.. and 480..).  Every wait is bounded; an expired wait
+// evenly over the SMs).  Tensor memory holds the accumulator (columns
+// [0, BN)) and four A stages (columns 256 + 32 s).  Four unpacked stages give
+// the MMA issue chain (MMA done -> commit -> converter -> barrier -> next MMA)
+// three k-blocks of tensor work to hide behind; with two stages the tensor
+// pipe idled between k-blocks.  Every wait is bounded; an expired wait
 // records QUAROT_ERR_TIMEOUT and the CTA drains its copies and MMAs, frees
 // TMEM and returns.
 #include <cuda.h>
@@ -52,8 +54,8 @@ namespace gemm {
 
 constexpr int BM = 128, BN_MAX = 224, BK = 128;  // tile in codes
 constexpr int BKB = BK / 2;                      // packed bytes per row per k-block
-constexpr int SP = 6;                            // packed ring stages
-constexpr int SU = 2;                            // unpacked ring stages (A in TMEM, W in smem)
+constexpr int SP = 4;                            // packed ring stages
+constexpr int SU = 4;                            // unpacked ring stages (A in TMEM, W in smem)
 constexpr int NCONV = 384;                       // converter threads (12 warps)
 constexpr int NEPI = 128;                        // epilogue threads (4 warps)
 constexpr int EPI_WARP0 = 2 + NCONV / 32;        // 14
@@ -70,8 +72,8 @@ constexpr int OFF_RSA = OFF_MISC + 16;             // int [2][BM]
 constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;      // int [2][BN_MAX]
 constexpr int SMEM_USED = OFF_RSB + 2 * BN_MAX * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
-constexpr uint32_t TMEM_COLS = 512;           // two accumulators of up to 224 columns + A stages
-constexpr uint32_t TMEM_A_COL = 448;          // A stage s at column 448 + 32 s (128 bytes per row)
+constexpr uint32_t TMEM_COLS = 512;           // accumulator (up to 224 columns) + A stages
+constexpr uint32_t TMEM_A_COL = 256;          // A stage s at column 256 + 32 s (128 bytes per row)
 constexpr int NCONV_WARPS = NCONV / 32;       // arrivals per converter barrier phase
 constexpr int NEPI_WARPS = NEPI / 32;
 constexpr int MAX_K = 65536;
@@ -292,10 +294,10 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       long it = 0;
       int ti = 0;
       for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
-        const int a = ti & 1;
-        if (!mbar_wait_bounded(&acc_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+        const int a = 0;  // one accumulator: the epilogue must drain it first
+        if (!mbar_wait_bounded(&acc_empty[0], uint32_t(ti & 1) ^ 1u, abort_flag)) break;
         fence_after_sync();
-        const uint32_t tmem_d = tmem_base + uint32_t(a * BN);
+        const uint32_t tmem_d = tmem_base;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = int(it % SU);
@@ -312,7 +314,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           mma_commit(&un_empty[s]);
         }
         if (!ok) break;
-        mma_commit(&acc_full[a]);
+        mma_commit(&acc_full[a]);  // a == 0
       }
       // every issued MMA must finish before TMEM is freed
       mma_commit(drain);
@@ -368,9 +370,10 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const bool vec_ok = (N % 8) == 0;
     int ti = 0;
     for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
-      const int a = ti & 1;
+      const int a = ti & 1;  // row-sum buffer (double-buffered); the accumulator is single
       const uint32_t par = uint32_t((ti >> 1) & 1);
-      if (!mbar_wait_bounded(&acc_full[a], par, abort_flag) || !mbar_wait_bounded(&rs_full[a], par, abort_flag))
+      if (!mbar_wait_bounded(&acc_full[0], uint32_t(ti & 1), abort_flag) ||
+          !mbar_wait_bounded(&rs_full[a], par, abort_flag))
         break;
       fence_after_sync();
       const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
@@ -378,7 +381,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
       const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[a * BM + r]);
       const int* rsb = rsB + a * BN_MAX;
-      const uint32_t tmem_row = tmem_base + uint32_t(a * BN) + (uint32_t(32 * q) << 16);
+      const uint32_t tmem_row = tmem_base + (uint32_t(32 * q) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
@@ -420,7 +423,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&acc_empty[a]);
+        mbar_arrive(&acc_empty[0]);
         mbar_arrive(&rs_empty[a]);
       }
     }

@@ -477,18 +477,25 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     uint32_t* qrow = reinterpret_cast<uint32_t*>(q_out + row * (D / 2));
     const float2 fv = make_float2(f, f);
     const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    // With clip ratio 1 the scale is max|x~| / 7 rounded to fp16, so
+    // |x~ / S| <= 7 (1 + 2^-11) + rounding < 7.5: the clamp cannot bind.
+    const bool need_clamp = clip_ratio < 1.0f;
 #pragma unroll
     for (int a = 0; a < MSEG; ++a) {
-      uint32_t word = 0;
+      uint32_t byte[4];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         float2 yv = __fmul2_rn(v[a][jj], fv);
-        yv.x = fminf(fmaxf(yv.x, -8.0f), 7.0f);
-        yv.y = fminf(fmaxf(yv.y, -8.0f), 7.0f);
+        if (need_clamp) {
+          yv.x = fminf(fmaxf(yv.x, -8.0f), 7.0f);
+          yv.y = fminf(fmaxf(yv.y, -8.0f), 7.0f);
+        }
         const float2 rr = __fadd2_rn(yv, magic);
-        word |= (uint32_t(__float_as_int(rr.x)) & 0xFu) << (8 * jj);
-        word |= (uint32_t(__float_as_int(rr.y)) & 0xFu) << (8 * jj + 4);
+        // low nibble of each: the round-half-even integer in two's complement
+        byte[jj] = (uint32_t(__float_as_int(rr.x)) & 0x0Fu) | ((uint32_t(__float_as_int(rr.y)) << 4) & 0xF0u);
       }
+      const uint32_t word = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040),
+                                        0x5410);
       __stcs(qrow + a * 128 + t, word);
       if (rot_out != nullptr) {
         float4* ro = reinterpret_cast<float4*>(rot_out + row * D + a * 1024 + 8 * t);
