@@ -478,8 +478,9 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     const float2 fv = make_float2(f, f);
     const float2 magic = make_float2(12582912.0f, 12582912.0f);
     // With clip ratio 1 the scale is max|x~| / 7 rounded to fp16, so
-    // |x~ / S| <= 7 (1 + 2^-11) + rounding < 7.5: the clamp cannot bind.
-    const bool need_clamp = clip_ratio < 1.0f;
+    // |x~ / S| <= 7 (1 + 2^-11) + rounding < 7.5 and the clamp cannot bind --
+    // unless the scale saturated at the fp16 maximum.
+    const bool need_clamp = clip_ratio < 1.0f || __half2float(S) >= 65504.0f;
 #pragma unroll
     for (int a = 0; a < MSEG; ++a) {
       uint32_t byte[4];
