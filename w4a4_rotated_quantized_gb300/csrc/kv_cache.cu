@@ -166,31 +166,46 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 }
 
 // One CTA per (split, b, g): the partial softmax state of the group's G query
-// heads over `chunk` tokens (a multiple of 16), on tensor cores.  Four warps take 16-token tiles in
-// turn.  Per tile:
+// heads over `chunk` tokens (a multiple of 16), on tensor cores.  Four warps
+// take 16-token tiles in turn.  Each warp keeps a ring of NS tiles in shared
+// memory, filled by bulk asynchronous copies (keys 1 KB, values 1 KB, their
+// scales 32 B each) issued NS tiles ahead.  Per tile:
 //   scores  S^T[16 tok x 2G] = Kcodes[16 x 128] . Q~^T, m16n8k16 with the
 //           query split into fp16 hi and lo halves (the 2G columns), so the
 //           product keeps fp32-level precision; the key scale multiplies the
-//           fp32 result.  Head dims are permuted identically on both
-//           operands so that each thread's fragment bytes are one 16-byte load.
-//   softmax online per head, warp-uniform running max, exp2 (log2 e folded
-//           into q~).
+//           fp32 result.  Head dims are permuted identically on both operands
+//           so that fragment pairs come from one masked word.
+//   softmax online per head, exp2 (log2 e folded into q~); the running max is
+//           raised (and the accumulators rescaled) only when a tile exceeds it
+//           by more than 8, so p stays below 2^8.
 //   output  O^T[128 x 2G] += Vcodes^T[128 x 16 tok] . P'^T, with P' = p * v_scale
-//           split into fp16 hi and lo columns; the output dims are permuted so
-//           each thread's value bytes are one 8-byte load per token.
+//           split into fp16 hi and lo columns; output dims are permuted so each
+//           thread's value bytes are one 8-byte load per token.
+constexpr int NS = 4;                 // tiles in flight per warp
+constexpr int TILE_BYTES = 2 * 16 * (HD / 2) + 2 * 32;  // K, V codes + scales = 2112
+constexpr int TILE_STRIDE = 2176;     // rounded to 128 bytes
+constexpr int QS = HD + 16;           // padded q~ row: dim d at d + 4 (d >> 5)
+constexpr int WO = HD + 4;            // padded merge row
+
+template <int G>
+constexpr size_t decode_smem_bytes() {
+  return size_t(G) * QS * 4 + size_t(DT / 32) * NS * TILE_STRIDE + size_t(DT / 32) * NS * 8 + 64;
+}
+
 template <int G>
 __global__ void __launch_bounds__(DT, 4)
 decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, const __half* __restrict__ ks,
                   const uint8_t* __restrict__ vq, const __half* __restrict__ vs, int Hq, int Hkv, int T,
                   int T_max, float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits,
-                  int chunk) {
+                  int chunk, int bulk_ok) {
   constexpr int NT = (2 * G + 7) / 8;  // n8 tiles of (head, hi/lo) columns
   constexpr int NW = DT / 32;
-  constexpr int QS = HD + 16;          // padded q~ row: dim d at d + 4 (d >> 5)
-  constexpr int WO = HD + 4;           // padded merge row
-  __shared__ __align__(16) float qs[G * QS];
+  extern __shared__ __align__(128) unsigned char dsm[];
+  unsigned char* ring = dsm;                                        // [NW][NS][TILE_STRIDE]
+  float* qs = reinterpret_cast<float*>(dsm + NW * NS * TILE_STRIDE);  // [G][QS]
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(dsm + NW * NS * TILE_STRIDE + G * QS * 4);  // [NW][NS]
   __shared__ float wm[NW][G], wl[NW][G];
-  __shared__ __align__(16) float wo[NW * G * WO];
+  float* wo = reinterpret_cast<float*>(ring);  // merge rows, reuse the ring after the last tile
 
   const int split = blockIdx.x;
   const int bg = blockIdx.y;
@@ -204,8 +219,54 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   const uint8_t* vbase = vq + cache_row * (HD / 2);
   const __half* ksb = ks + cache_row;
   const __half* vsb = vs + cache_row;
+  unsigned char* wring = ring + wid * NS * TILE_STRIDE;
+  uint64_t* wbar = tbar + wid * NS;
 
-  // ---- q~ = q H / sqrt(d) * qscale (FWHT in shared memory)
+  if (lane == 0) {
+    for (int st = 0; st < NS; ++st) mbar_init(&wbar[st], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // tile i of this warp starts at token wid * 16 + i * NW * 16
+  auto issue = [&](int i) {
+    const int tt = wid * 16 + i * NW * 16;
+    if (tt >= tn) return;
+    unsigned char* dst = wring + (i % NS) * TILE_STRIDE;
+    if (bulk_ok && tt + 16 <= tn) {
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&wbar[i % NS], TILE_BYTES);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
+                         smem_u32(dst)), "l"(kbase + int64_t(tt) * (HD / 2)), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
+                         smem_u32(dst + 1024)), "l"(vbase + int64_t(tt) * (HD / 2)), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
+                         smem_u32(dst + 2048)), "l"(ksb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
+                         smem_u32(dst + 2080)), "l"(vsb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
+      }
+    } else {
+      // ragged last tile (or unaligned cache): plain loads, zero beyond tn
+      for (int k = lane; k < 128; k += 32) {  // 64 x 16 B of codes
+        const int tok = (k & 63) >> 2, part = k & 3;
+        const uint8_t* srcb = (k < 64 ? kbase : vbase) + int64_t(tt + tok) * (HD / 2);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (tt + tok < tn) val = __ldcs(reinterpret_cast<const uint4*>(srcb) + part);
+        *reinterpret_cast<uint4*>(dst + (k < 64 ? 0 : 1024) + tok * 64 + part * 16) = val;
+      }
+      if (lane < 16) {
+        const bool in = tt + lane < tn;
+        reinterpret_cast<__half*>(dst + 2048)[lane] = in ? ksb[tt + lane] : __float2half(0.f);
+        reinterpret_cast<__half*>(dst + 2080)[lane] = in ? vsb[tt + lane] : __float2half(0.f);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wbar[i % NS]);
+    }
+  };
+#pragma unroll 1
+  for (int i = 0; i < NS; ++i) issue(i);
+
+  // ---- q~ = q H / sqrt(d) (FWHT in shared memory)
   auto qidx = [](int hh, int d) { return hh * QS + d + 4 * (d >> 5); };
   for (int i = tid; i < G * HD; i += DT) {
     const int hh = i / HD, e = i % HD;
@@ -223,27 +284,34 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     __syncthreads();
   }
 
-  // ---- B fragments of Q~^T: column n = lane/4 of n-tile nt is head (4 nt + n/2),
-  // hi half for even n, lo half for odd n.  Step j uses head dims
-  // 32c + 4j + {0,1} (b0) and 32c + 4j + {2,3} (b1): one 16-byte load.
+  // ---- B fragments of Q~^T.  Column n = lane/4 of n-tile nt is head
+  // 4 nt + n/2 (hi half for even n, lo half for odd n).  Step j pairs head dims
+  // d0 = 32c + 8 (j >> 1) + 2 (j & 1): b0 = (d0, d0 + 4), b1 = (d0 + 1, d0 + 5),
+  // matching the key fragments built by masking one word of packed codes.
   uint32_t qb[NT][8][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 4 + (r >> 1);
     const bool lo_part = (r & 1) != 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (hh < G) x4 = *reinterpret_cast<const float4*>(&qs[qidx(hh, 32 * c + 4 * j)]);
-      const float xs[4] = {x4.x * qscale, x4.y * qscale, x4.z * qscale, x4.w * qscale};
-      __half e4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __half hi = __float2half_rn(xs[e]);
-        e4[e] = lo_part ? __float2half_rn(xs[e] - __half2float(hi)) : hi;
+    for (int m4 = 0; m4 < 4; ++m4) {
+      float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hh < G) {
+        xa = *reinterpret_cast<const float4*>(&qs[qidx(hh, 32 * c + 8 * m4)]);
+        xb = *reinterpret_cast<const float4*>(&qs[qidx(hh, 32 * c + 8 * m4 + 4)]);
       }
-      qb[nt][j][0] = pack_h2(e4[0], e4[1]);
-      qb[nt][j][1] = pack_h2(e4[2], e4[3]);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      __half hv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = xv[e] * qscale;
+        const __half hi = __float2half_rn(x);
+        hv[e] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
+      }
+      qb[nt][2 * m4][0] = pack_h2(hv[0], hv[4]);
+      qb[nt][2 * m4][1] = pack_h2(hv[1], hv[5]);
+      qb[nt][2 * m4 + 1][0] = pack_h2(hv[2], hv[6]);
+      qb[nt][2 * m4 + 1][1] = pack_h2(hv[3], hv[7]);
     }
   }
 
@@ -261,38 +329,28 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     l_run[nt] = 0.f;
   }
 
-  // ---- tiles of 16 tokens, warp-strided; the next tile's codes and scales
-  // are loaded while the current one is processed
-  auto load_tile = [&](int tt, uint4& k0, uint4& k1, float& ks0, float& ks1, uint2* vw, float* vsc) {
-    const int tr0 = tt + r, tr1 = tt + r + 8;
-    k0 = tr0 < tn ? __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr0) * (HD / 2)) + c) : make_uint4(0, 0, 0, 0);
-    k1 = tr1 < tn ? __ldcs(reinterpret_cast<const uint4*>(kbase + int64_t(tr1) * (HD / 2)) + c) : make_uint4(0, 0, 0, 0);
-    ks0 = tr0 < tn ? __half2float(ksb[tr0]) : 0.f;
-    ks1 = tr1 < tn ? __half2float(ksb[tr1]) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int tv = tt + 2 * c + (u & 1) + 8 * (u >> 1);
-      vw[u] = tv < tn ? __ldcs(reinterpret_cast<const uint2*>(vbase + int64_t(tv) * (HD / 2)) + r) : make_uint2(0, 0);
-      vsc[u] = tv < tn ? __half2float(vsb[tv]) : 0.f;
-    }
-  };
-  uint4 nk0, nk1;
-  float nks0, nks1, nvsc[4];
-  uint2 nvw[4];
-  load_tile(wid * 16, nk0, nk1, nks0, nks1, nvw, nvsc);
-  for (int tt = wid * 16; tt < tn; tt += NW * 16) {
-    const int tr0 = tt + r, tr1 = tt + r + 8;
-    const uint4 k0 = nk0, k1 = nk1;
-    const float ks0 = nks0, ks1 = nks1;
+  int i = 0;
+  for (int tt = wid * 16; tt < tn; tt += NW * 16, ++i) {
+    const unsigned char* src = wring + (i % NS) * TILE_STRIDE;
+    if (!mbar_wait_bounded(&wbar[i % NS], uint32_t((i / NS) & 1), nullptr)) break;
+    // ---- fragments: keys of tokens r, r+8 (bytes 16c..16c+15), values of
+    // tokens 2c, 2c+1, 2c+8, 2c+9 (bytes 8r..8r+7), scales
+    const uint4 k0 = *reinterpret_cast<const uint4*>(src + r * 64 + 16 * c);
+    const uint4 k1 = *reinterpret_cast<const uint4*>(src + (r + 8) * 64 + 16 * c);
     uint2 vw[4];
     float vsc[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      vw[u] = nvw[u];
-      vsc[u] = nvsc[u];
+      const int tok = 2 * c + (u & 1) + 8 * (u >> 1);
+      vw[u] = *reinterpret_cast<const uint2*>(src + 1024 + tok * 64 + 8 * r);
+      vsc[u] = __half2float(reinterpret_cast<const __half*>(src + 2080)[tok]);
     }
-    if (tt + NW * 16 < tn) load_tile(tt + NW * 16, nk0, nk1, nks0, nks1, nvw, nvsc);
+    const float ks0 = __half2float(reinterpret_cast<const __half*>(src + 2048)[r]);
+    const float ks1 = __half2float(reinterpret_cast<const __half*>(src + 2048)[r + 8]);
+    __syncwarp();
+    issue(i + NS);  // refill this stage NS tiles ahead
 
+    const int tr0 = tt + r, tr1 = tt + r + 8;
     // ---- scores
     const uint32_t kw0[4] = {k0.x, k0.y, k0.z, k0.w};
     const uint32_t kw1[4] = {k1.x, k1.y, k1.z, k1.w};
@@ -302,12 +360,21 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int wi = j >> 1, p0 = 2 * (j & 1);
-      const uint32_t a0 = byte_pair(kw0[wi], p0), a2 = byte_pair(kw0[wi], p0 + 1);
-      const uint32_t a1 = byte_pair(kw1[wi], p0), a3 = byte_pair(kw1[wi], p0 + 1);
+    for (int m4 = 0; m4 < 4; ++m4) {
+      const uint32_t w0 = kw0[m4], w1 = kw1[m4], w0s = w0 >> 8, w1s = w1 >> 8;
+      const uint32_t p0a = hfma2_u32((w0 & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
+      const uint32_t p1a = hfma2_u32((w0 & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
+      const uint32_t p2a = hfma2_u32((w0s & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
+      const uint32_t p3a = hfma2_u32((w0s & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
+      const uint32_t p0b = hfma2_u32((w1 & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
+      const uint32_t p1b = hfma2_u32((w1 & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
+      const uint32_t p2b = hfma2_u32((w1s & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
+      const uint32_t p3b = hfma2_u32((w1s & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(sacc[nt], a0, a1, a2, a3, qb[nt][j][0], qb[nt][j][1]);
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816(sacc[nt], p0a, p0b, p1a, p1b, qb[nt][2 * m4][0], qb[nt][2 * m4][1]);
+        mma16816(sacc[nt], p2a, p2b, p3a, p3b, qb[nt][2 * m4 + 1][0], qb[nt][2 * m4 + 1][1]);
+      }
     }
 
 #pragma unroll
@@ -319,16 +386,20 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-      const float m_new = fmaxf(m_run[nt], mt);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_run[nt] - m_use);
-      m_run[nt] = m_new;
+      // raise the running max only when it grows by more than 8 (p <= 2^8)
+      if (__any_sync(0xffffffffu, mt > m_run[nt] + 8.0f)) {
+        const float m_new = mt > m_run[nt] + 8.0f ? mt : m_run[nt];
+        const float alpha = exp2f(m_run[nt] - m_new);  // 0 when the old max is -inf
+        m_run[nt] = m_new;
+        l_run[nt] *= alpha;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[nt][ii][e] *= alpha;
+      }
+      const float m_use = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
       const float P0 = exp2f(s0 - m_use), P1 = exp2f(s1 - m_use);
-      l_run[nt] = l_run[nt] * alpha + P0 + P1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[nt][i][e] *= alpha;
+      l_run[nt] += P0 + P1;
 
       // B fragment of P'^T: column n = r is head 4 nt + r/2 (hi for even r, lo
       // for odd r); rows are tokens 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1).
@@ -342,21 +413,23 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
         ph[u] = (r & 1) ? __float2half_rn(pv[u] - __half2float(hi)) : hi;
       }
       const uint32_t pb0 = pack_h2(ph[0], ph[1]), pb1 = pack_h2(ph[2], ph[3]);
-      // ---- O^T += V^T P'^T over 8 m-tiles of 16 dims: m-tile i, row r is dim
-      // 16r + 2i, row r + 8 is dim 16r + 2i + 1 (byte i of the 8-byte chunk)
+      // ---- O^T += V^T P'^T over 8 m-tiles of 16 dims: m-tile ii, row r is dim
+      // 16r + 2ii, row r + 8 is dim 16r + 2ii + 1 (byte ii of the 8-byte chunk)
       const uint32_t va[2] = {vw[0].x, vw[0].y}, vb[2] = {vw[1].x, vw[1].y};
       const uint32_t vc[2] = {vw[2].x, vw[2].y}, vd[2] = {vw[3].x, vw[3].y};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int ii = 0; ii < 8; ++ii) {
         uint32_t a0, a1, a2, a3;
-        byte_cross(va[i >> 2], vb[i >> 2], i & 3, a0, a1);
-        byte_cross(vc[i >> 2], vd[i >> 2], i & 3, a2, a3);
-        mma16816(o[nt][i], a0, a1, a2, a3, pb0, pb1);
+        byte_cross(va[ii >> 2], vb[ii >> 2], ii & 3, a0, a1);
+        byte_cross(vc[ii >> 2], vd[ii >> 2], ii & 3, a2, a3);
+        mma16816(o[nt][ii], a0, a1, a2, a3, pb0, pb1);
       }
     }
   }
 
-  // ---- merge the warps of the CTA, then write the split's partial state
+  // ---- merge the warps of the CTA (the ring is free: reuse it), then write
+  // the split's partial state
+  __syncthreads();
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 4 + c;
@@ -371,8 +444,8 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
       }
       float* wrow = wo + (wid * G + hh) * WO + 16 * r;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<float2*>(wrow + 2 * i) = make_float2(o[nt][i][0] + o[nt][i][1], o[nt][i][2] + o[nt][i][3]);
+      for (int ii = 0; ii < 8; ++ii)
+        *reinterpret_cast<float2*>(wrow + 2 * ii) = make_float2(o[nt][ii][0] + o[nt][ii][1], o[nt][ii][2] + o[nt][ii][3]);
     }
   }
   __syncthreads();
@@ -507,18 +580,32 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   float* ws_ml = ws_o + size_t(B * Hq * splits) * kv::HD;
   dim3 grid(unsigned(splits), unsigned(B * Hkv));
   const int G = int(Hq / Hkv);
-  auto args = [&](auto kern) {
-    kern<<<grid, kv::DT, 0, st>>>(static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q,
-                                  static_cast<const __half*>(v_s), int(Hq), int(Hkv), int(T), int(T_max),
-                                  qscale, ws_o, ws_ml, splits, int(chunk));
+  // bulk copies need 16-byte aligned sources: every (b, g) row of the scale
+  // arrays starts at a multiple of 8 tokens
+  const int bulk_ok = (T_max % 8) == 0 && !mis(k_s, 16) && !mis(v_s, 16);
+  int lrc = QUAROT_OK;
+  auto args = [&](auto kern, size_t smem) {
+    static bool attr[4] = {false, false, false, false};
+    const int slot = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+    if (!attr[slot]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
+        lrc = QUAROT_ERR_LAUNCH;
+        return;
+      }
+      attr[slot] = true;
+    }
+    kern<<<grid, kv::DT, smem, st>>>(static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q,
+                                     static_cast<const __half*>(v_s), int(Hq), int(Hkv), int(T), int(T_max),
+                                     qscale, ws_o, ws_ml, splits, int(chunk), bulk_ok);
   };
   switch (G) {
-    case 1: args(kv::decode_mma_kernel<1>); break;
-    case 2: args(kv::decode_mma_kernel<2>); break;
-    case 4: args(kv::decode_mma_kernel<4>); break;
-    case 8: args(kv::decode_mma_kernel<8>); break;
+    case 1: args(kv::decode_mma_kernel<1>, kv::decode_smem_bytes<1>()); break;
+    case 2: args(kv::decode_mma_kernel<2>, kv::decode_smem_bytes<2>()); break;
+    case 4: args(kv::decode_mma_kernel<4>, kv::decode_smem_bytes<4>()); break;
+    case 8: args(kv::decode_mma_kernel<8>, kv::decode_smem_bytes<8>()); break;
     default: return QUAROT_ERR_UNSUPPORTED;
   }
+  if (lrc != QUAROT_OK) return lrc;
   kv::decode_combine_kernel<<<unsigned(B * Hq), kv::HD, 0, st>>>(ws_o, ws_ml, splits, unrotate_out,
                                                                  static_cast<__half*>(out));
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
