@@ -506,6 +506,24 @@ decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ 
   out[int64_t(bh) * HD + e] = __float2half_rn(r);
 }
 
+// Resident CTAs per SM of the decode kernel for group size G (queried once).
+int decode_ctas_per_sm(int G) {
+  static int cache[4] = {0, 0, 0, 0};
+  const int slot = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  if (cache[slot] == 0) {
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (G) {
+      case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<1>, DT, decode_smem_bytes<1>()); break;
+      case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<2>, DT, decode_smem_bytes<2>()); break;
+      case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<4>, DT, decode_smem_bytes<4>()); break;
+      default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<8>, DT, decode_smem_bytes<8>()); break;
+    }
+    cache[slot] = (e == cudaSuccess && n > 0) ? n : 1;
+  }
+  return cache[slot];
+}
+
 }  // namespace kv
 }  // namespace quarot
 
@@ -564,12 +582,15 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
       mis(workspace, 256))
     return QUAROT_ERR_ALIGNMENT;
   if (B * Hkv > 65535 || T > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
-  // Splits: enough CTAs to fill the GPU (about 4 per SM), never more than the
-  // workspace bound of one split per kv::CHUNK tokens; chunks are multiples of 16.
+  // Splits: as many as fit one wave of resident CTAs (no tail wave), at least
+  // one, never more than the workspace bound of one split per kv::CHUNK
+  // tokens; chunks are multiples of 16 tokens.
+  const int G = int(Hq / Hkv);
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int per_sm = kv::decode_ctas_per_sm(G);
   const int64_t max_splits = kv::num_splits(T);
-  int64_t want = (int64_t(4) * sms + B * Hkv - 1) / (B * Hkv);
+  int64_t want = (int64_t(per_sm) * sms) / (B * Hkv);
   want = want < 1 ? 1 : (want > max_splits ? max_splits : want);
   int64_t chunk = (T + want - 1) / want;
   chunk = (chunk + 15) / 16 * 16;
@@ -579,7 +600,6 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   float* ws_o = static_cast<float*>(workspace);
   float* ws_ml = ws_o + size_t(B * Hq * splits) * kv::HD;
   dim3 grid(unsigned(splits), unsigned(B * Hkv));
-  const int G = int(Hq / Hkv);
   // bulk copies need 16-byte aligned sources: every (b, g) row of the scale
   // arrays starts at a multiple of 8 tokens
   const int bulk_ok = (T_max % 8) == 0 && !mis(k_s, 16) && !mis(v_s, 16);
