@@ -179,8 +179,8 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 //           raised (and the accumulators rescaled) only when a tile exceeds it
 //           by more than 8, so p stays below 2^8.
 //   output  O^T[128 x 2G] += Vcodes^T[128 x 16 tok] . P'^T, with P' = p * v_scale
-//           split into fp16 hi and lo columns; output dims are permuted so each
-//           thread's value bytes are one 8-byte load per token.
+//           in fp16 (even columns; odd columns zero); output dims are permuted
+//           so each thread's value bytes are one 8-byte load per token.
 constexpr int NS = 4;                 // tiles in flight per warp
 constexpr int TILE_BYTES = 2 * 16 * (HD / 2) + 2 * 32;  // K, V codes + scales = 2112
 constexpr int TILE_STRIDE = 2176;     // rounded to 128 bytes
@@ -288,6 +288,11 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   // 4 nt + n/2 (hi half for even n, lo half for odd n).  Step j pairs head dims
   // d0 = 32c + 8 (j >> 1) + 2 (j & 1): b0 = (d0, d0 + 4), b1 = (d0 + 1, d0 + 5),
   // matching the key fragments built by masking one word of packed codes.
+  // The key fragments keep the fp16 magic offsets: a low-nibble code u + 8
+  // arrives as 1024 + (v + 8) and a high-nibble code as 1024 + 16 (v + 8), so
+  // the query weights of high-nibble dims (odd d) are divided by 16 and every
+  // score carries the per-head constant sum_even 1032 q~ + sum_odd 72 q~,
+  // subtracted after the product.
   uint32_t qb[NT][8][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -304,7 +309,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
       __half hv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float x = xv[e] * qscale;
+        const float x = xv[e] * qscale * ((e & 1) ? 0.0625f : 1.0f);
         const __half hi = __float2half_rn(x);
         hv[e] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
       }
@@ -313,6 +318,22 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
       qb[nt][2 * m4 + 1][0] = pack_h2(hv[2], hv[6]);
       qb[nt][2 * m4 + 1][1] = pack_h2(hv[3], hv[7]);
     }
+  }
+  // per-head offset constant of the scores, from the fp16 weights actually used
+  float qoff[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int hh = nt * 4 + c;  // the head whose scores this thread holds
+    float acc = 0.f;
+    if (hh < G) {
+      for (int d = 0; d < HD; ++d) {
+        const float x = qs[qidx(hh, d)] * qscale * ((d & 1) ? 0.0625f : 1.0f);
+        const __half hi = __float2half_rn(x);
+        const float lo = __half2float(__float2half_rn(x - __half2float(hi)));
+        acc += (__half2float(hi) + lo) * ((d & 1) ? 1152.0f : 1032.0f);
+      }
+    }
+    qoff[nt] = acc;
   }
 
   float o[NT][8][4];
@@ -354,34 +375,34 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     // ---- scores
     const uint32_t kw0[4] = {k0.x, k0.y, k0.z, k0.w};
     const uint32_t kw1[4] = {k1.x, k1.y, k1.z, k1.w};
-    float sacc[NT][4];
+    float sacc[NT][2][4];  // two accumulation chains (even / odd steps)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) sacc[nt][0][e] = sacc[nt][1][e] = 0.f;
 #pragma unroll
     for (int m4 = 0; m4 < 4; ++m4) {
       const uint32_t w0 = kw0[m4], w1 = kw1[m4], w0s = w0 >> 8, w1s = w1 >> 8;
-      const uint32_t p0a = hfma2_u32((w0 & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
-      const uint32_t p1a = hfma2_u32((w0 & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
-      const uint32_t p2a = hfma2_u32((w0s & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
-      const uint32_t p3a = hfma2_u32((w0s & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
-      const uint32_t p0b = hfma2_u32((w1 & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
-      const uint32_t p1b = hfma2_u32((w1 & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
-      const uint32_t p2b = hfma2_u32((w1s & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
-      const uint32_t p3b = hfma2_u32((w1s & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
+      const uint32_t p0a = (w0 & 0x000F000Fu) ^ 0x64086408u, p1a = (w0 & 0x00F000F0u) ^ 0x64806480u;
+      const uint32_t p2a = (w0s & 0x000F000Fu) ^ 0x64086408u, p3a = (w0s & 0x00F000F0u) ^ 0x64806480u;
+      const uint32_t p0b = (w1 & 0x000F000Fu) ^ 0x64086408u, p1b = (w1 & 0x00F000F0u) ^ 0x64806480u;
+      const uint32_t p2b = (w1s & 0x000F000Fu) ^ 0x64086408u, p3b = (w1s & 0x00F000F0u) ^ 0x64806480u;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        mma16816(sacc[nt], p0a, p0b, p1a, p1b, qb[nt][2 * m4][0], qb[nt][2 * m4][1]);
-        mma16816(sacc[nt], p2a, p2b, p3a, p3b, qb[nt][2 * m4 + 1][0], qb[nt][2 * m4 + 1][1]);
+        mma16816(sacc[nt][0], p0a, p0b, p1a, p1b, qb[nt][2 * m4][0], qb[nt][2 * m4][1]);
+        mma16816(sacc[nt][1], p2a, p2b, p3a, p3b, qb[nt][2 * m4 + 1][0], qb[nt][2 * m4 + 1][1]);
       }
     }
 
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       // thread holds head 4 nt + c for tokens tr0 (sacc 0 + 1) and tr1 (sacc 2 + 3)
-      const float s0 = tr0 < tn ? (sacc[nt][0] + sacc[nt][1]) * ks0 : -INFINITY;
-      const float s1 = tr1 < tn ? (sacc[nt][2] + sacc[nt][3]) * ks1 : -INFINITY;
+      const float s0 = tr0 < tn
+                           ? (((sacc[nt][0][0] + sacc[nt][1][0]) + (sacc[nt][0][1] + sacc[nt][1][1])) - qoff[nt]) * ks0
+                           : -INFINITY;
+      const float s1 = tr1 < tn
+                           ? (((sacc[nt][0][2] + sacc[nt][1][2]) + (sacc[nt][0][3] + sacc[nt][1][3])) - qoff[nt]) * ks1
+                           : -INFINITY;
       float mt = fmaxf(s0, s1);
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
@@ -406,13 +427,10 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
       const int src0 = 8 * c + (r >> 1), src1 = 8 * c + 4 + (r >> 1);
       const float pv[4] = {__shfl_sync(0xffffffffu, P0, src0) * vsc[0], __shfl_sync(0xffffffffu, P0, src1) * vsc[1],
                            __shfl_sync(0xffffffffu, P1, src0) * vsc[2], __shfl_sync(0xffffffffu, P1, src1) * vsc[3]};
-      __half ph[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const __half hi = __float2half_rn(pv[u]);
-        ph[u] = (r & 1) ? __float2half_rn(pv[u] - __half2float(hi)) : hi;
-      }
-      const uint32_t pb0 = pack_h2(ph[0], ph[1]), pb1 = pack_h2(ph[2], ph[3]);
+      // fp16 p' (relative rounding 2^-11, uncorrelated across tokens); the odd
+      // columns stay zero
+      const uint32_t pb0 = (r & 1) ? 0u : pack_h2(__float2half_rn(pv[0]), __float2half_rn(pv[1]));
+      const uint32_t pb1 = (r & 1) ? 0u : pack_h2(__float2half_rn(pv[2]), __float2half_rn(pv[3]));
       // ---- O^T += V^T P'^T over 8 m-tiles of 16 dims: m-tile ii, row r is dim
       // 16r + 2ii, row r + 8 is dim 16r + 2ii + 1 (byte ii of the 8-byte chunk)
       const uint32_t va[2] = {vw[0].x, vw[0].y}, vb[2] = {vw[1].x, vw[1].y};
