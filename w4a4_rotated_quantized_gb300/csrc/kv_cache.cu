@@ -152,15 +152,6 @@ __device__ __forceinline__ void byte_cross(uint32_t wa, uint32_t wb, int p, uint
   hi = hfma2_u32((x & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
 }
 
-// 16- / 8-byte asynchronous global -> shared copies; a false predicate
-// zero-fills the destination without reading global memory.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(pred ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, bool pred) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(pred ? 8 : 0) : "memory");
-}
-
 __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -177,7 +168,8 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 // One CTA per (split, b, g): the partial softmax state of the group's G query
 // heads over `chunk` tokens (a multiple of 16), on tensor cores.  Four warps
 // take 16-token tiles in turn.  Each warp keeps a ring of NS tiles in shared
-// memory, filled NS - 1 tiles ahead by per-lane asynchronous copies.  Per tile:
+// memory, filled by bulk asynchronous copies (keys 1 KB, values 1 KB, their
+// scales 32 B each) issued NS tiles ahead.  Per tile:
 //   scores  S^T[16 tok x 2G] = Kcodes[16 x 128] . Q~^T, m16n8k16 with the
 //           query split into fp16 hi and lo halves (the 2G columns), so the
 //           product keeps fp32-level precision; the key scale multiplies the
@@ -197,7 +189,7 @@ constexpr int WO = HD + 4;            // padded merge row
 
 template <int G>
 constexpr size_t decode_smem_bytes() {
-  return size_t(G) * QS * 4 + size_t(DT / 32) * NS * TILE_STRIDE + 64;
+  return size_t(G) * QS * 4 + size_t(DT / 32) * NS * TILE_STRIDE + size_t(DT / 32) * NS * 8 + 64;
 }
 
 template <int G>
@@ -205,12 +197,13 @@ __global__ void __launch_bounds__(DT, 4)
 decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, const __half* __restrict__ ks,
                   const uint8_t* __restrict__ vq, const __half* __restrict__ vs, int Hq, int Hkv, int T,
                   int T_max, float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits,
-                  int chunk, int scales_vec) {
+                  int chunk, int bulk_ok) {
   constexpr int NT = (2 * G + 7) / 8;  // n8 tiles of (head, hi/lo) columns
   constexpr int NW = DT / 32;
   extern __shared__ __align__(128) unsigned char dsm[];
   unsigned char* ring = dsm;                                        // [NW][NS][TILE_STRIDE]
   float* qs = reinterpret_cast<float*>(dsm + NW * NS * TILE_STRIDE);  // [G][QS]
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(dsm + NW * NS * TILE_STRIDE + G * QS * 4);  // [NW][NS]
   __shared__ float wm[NW][G], wl[NW][G];
   float* wo = reinterpret_cast<float*>(ring);  // merge rows, reuse the ring after the last tile
 
@@ -227,45 +220,51 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   const __half* ksb = ks + cache_row;
   const __half* vsb = vs + cache_row;
   unsigned char* wring = ring + wid * NS * TILE_STRIDE;
+  uint64_t* wbar = tbar + wid * NS;
 
-  // Tile i of this warp starts at token wid * 16 + i * NW * 16.  Every lane
-  // copies, with 16- and 8-byte cp.async, exactly the bytes of its own
-  // fragments into its private slots of ring stage i % NS:
-  //   keys   tokens r, r+8, bytes 16c..16c+15       -> lane slot [0, 32)
-  //   values tokens 2c, 2c+1, 2c+8, 2c+9, bytes 8r.. -> lane slot [32, 64)
-  // and lanes 0..3 copy the tile's 16 key / 16 value scales (32 B each) into the
-  // stage's shared scale area.  Out-of-range tokens are zero-filled.
+  if (lane == 0) {
+    for (int st = 0; st < NS; ++st) mbar_init(&wbar[st], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // tile i of this warp starts at token wid * 16 + i * NW * 16
   auto issue = [&](int i) {
     const int tt = wid * 16 + i * NW * 16;
-    if (tt < tn) {
-      unsigned char* stage = wring + (i % NS) * TILE_STRIDE;
-      const uint32_t slot = smem_u32(stage + lane * 64);
-      const int tk0 = tt + r, tk1 = tt + r + 8;
-      cp_async16(slot, kbase + int64_t(min(tk0, tn - 1)) * (HD / 2) + 16 * c, tk0 < tn);
-      cp_async16(slot + 16, kbase + int64_t(min(tk1, tn - 1)) * (HD / 2) + 16 * c, tk1 < tn);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int tv = tt + 2 * c + (u & 1) + 8 * (u >> 1);
-        cp_async8(slot + 32 + 8 * u, vbase + int64_t(min(tv, tn - 1)) * (HD / 2) + 8 * r, tv < tn);
+    if (tt >= tn) return;
+    unsigned char* dst = wring + (i % NS) * TILE_STRIDE;
+    if (bulk_ok && tt + 16 <= tn) {
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&wbar[i % NS], TILE_BYTES);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
+                         smem_u32(dst)), "l"(kbase + int64_t(tt) * (HD / 2)), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
+                         smem_u32(dst + 1024)), "l"(vbase + int64_t(tt) * (HD / 2)), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
+                         smem_u32(dst + 2048)), "l"(ksb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
+                         smem_u32(dst + 2080)), "l"(vsb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
       }
-      if (lane < 4) {
-        // lane 0/1: key scales tokens 0-7 / 8-15; lane 2/3: value scales
-        const __half* srcs = (lane < 2 ? ksb : vsb) + tt + 8 * (lane & 1);
-        const int ntok = tn - (tt + 8 * (lane & 1));
-        const uint32_t dsts = smem_u32(stage + 2048 + 32 * (lane >> 1) + 16 * (lane & 1));
-        if (scales_vec && ntok >= 8) {
-          cp_async16(dsts, srcs, true);
-        } else {
-          for (int k = 0; k < 8; ++k)
-            reinterpret_cast<__half*>(stage + 2048 + 32 * (lane >> 1) + 16 * (lane & 1))[k] =
-                k < ntok ? srcs[k] : __float2half(0.f);
-        }
+    } else {
+      // ragged last tile (or unaligned cache): plain loads, zero beyond tn
+      for (int k = lane; k < 128; k += 32) {  // 64 x 16 B of codes
+        const int tok = (k & 63) >> 2, part = k & 3;
+        const uint8_t* srcb = (k < 64 ? kbase : vbase) + int64_t(tt + tok) * (HD / 2);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (tt + tok < tn) val = __ldcs(reinterpret_cast<const uint4*>(srcb) + part);
+        *reinterpret_cast<uint4*>(dst + (k < 64 ? 0 : 1024) + tok * 64 + part * 16) = val;
       }
+      if (lane < 16) {
+        const bool in = tt + lane < tn;
+        reinterpret_cast<__half*>(dst + 2048)[lane] = in ? ksb[tt + lane] : __float2half(0.f);
+        reinterpret_cast<__half*>(dst + 2080)[lane] = in ? vsb[tt + lane] : __float2half(0.f);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wbar[i % NS]);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   };
 #pragma unroll 1
-  for (int i = 0; i < NS - 1; ++i) issue(i);
+  for (int i = 0; i < NS; ++i) issue(i);
 
   // ---- q~ = q H / sqrt(d) (FWHT in shared memory)
   auto qidx = [](int hh, int d) { return hh * QS + d + 4 * (d >> 5); };
@@ -353,24 +352,24 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 
   int i = 0;
   for (int tt = wid * 16; tt < tn; tt += NW * 16, ++i) {
-    issue(i + NS - 1);  // keep NS - 1 tiles in flight beyond this one
-    asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");
-    __syncwarp();  // the scale area is written by lanes 0..3
-    const unsigned char* stage = wring + (i % NS) * TILE_STRIDE;
-    const unsigned char* mine = stage + lane * 64;
-    const uint4 k0 = *reinterpret_cast<const uint4*>(mine);
-    const uint4 k1 = *reinterpret_cast<const uint4*>(mine + 16);
+    const unsigned char* src = wring + (i % NS) * TILE_STRIDE;
+    if (!mbar_wait_bounded(&wbar[i % NS], uint32_t((i / NS) & 1), nullptr)) break;
+    // ---- fragments: keys of tokens r, r+8 (bytes 16c..16c+15), values of
+    // tokens 2c, 2c+1, 2c+8, 2c+9 (bytes 8r..8r+7), scales
+    const uint4 k0 = *reinterpret_cast<const uint4*>(src + r * 64 + 16 * c);
+    const uint4 k1 = *reinterpret_cast<const uint4*>(src + (r + 8) * 64 + 16 * c);
     uint2 vw[4];
     float vsc[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int tok = 2 * c + (u & 1) + 8 * (u >> 1);
-      vw[u] = *reinterpret_cast<const uint2*>(mine + 32 + 8 * u);
-      vsc[u] = __half2float(reinterpret_cast<const __half*>(stage + 2080)[tok]);
+      vw[u] = *reinterpret_cast<const uint2*>(src + 1024 + tok * 64 + 8 * r);
+      vsc[u] = __half2float(reinterpret_cast<const __half*>(src + 2080)[tok]);
     }
-    const float ks0 = __half2float(reinterpret_cast<const __half*>(stage + 2048)[r]);
-    const float ks1 = __half2float(reinterpret_cast<const __half*>(stage + 2048)[r + 8]);
-    __syncwarp();  // every lane has its copy before the stage is refilled
+    const float ks0 = __half2float(reinterpret_cast<const __half*>(src + 2048)[r]);
+    const float ks1 = __half2float(reinterpret_cast<const __half*>(src + 2048)[r + 8]);
+    __syncwarp();
+    issue(i + NS);  // refill this stage NS tiles ahead
 
     const int tr0 = tt + r, tr1 = tt + r + 8;
     // ---- scores
@@ -448,7 +447,6 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 
   // ---- merge the warps of the CTA (the ring is free: reuse it), then write
   // the split's partial state
-  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -620,9 +618,9 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   float* ws_o = static_cast<float*>(workspace);
   float* ws_ml = ws_o + size_t(B * Hq * splits) * kv::HD;
   dim3 grid(unsigned(splits), unsigned(B * Hkv));
-  // 16-byte scale copies need every (b, g) row of the scale arrays to start at
-  // a multiple of 8 tokens
-  const int scales_vec = (T_max % 8) == 0 && !mis(k_s, 16) && !mis(v_s, 16);
+  // bulk copies need 16-byte aligned sources: every (b, g) row of the scale
+  // arrays starts at a multiple of 8 tokens
+  const int bulk_ok = (T_max % 8) == 0 && !mis(k_s, 16) && !mis(v_s, 16);
   int lrc = QUAROT_OK;
   auto args = [&](auto kern, size_t smem) {
     static bool attr[4] = {false, false, false, false};
@@ -636,7 +634,7 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
     }
     kern<<<grid, kv::DT, smem, st>>>(static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q,
                                      static_cast<const __half*>(v_s), int(Hq), int(Hkv), int(T), int(T_max),
-                                     qscale, ws_o, ws_ml, splits, int(chunk), scales_vec);
+                                     qscale, ws_o, ws_ml, splits, int(chunk), bulk_ok);
   };
   switch (G) {
     case 1: args(kv::decode_mma_kernel<1>, kv::decode_smem_bytes<1>()); break;
