@@ -442,27 +442,29 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
       float2 z[11];
 #pragma unroll
       for (int j = 0; j < 11; ++j) z[j] = v[1 + j][jj];
-      float2 T = z[0];
-#pragma unroll
-      for (int j = 1; j < 11; ++j) T = __fadd2_rn(T, z[j]);
+      const float2 t01 = __fadd2_rn(z[0], z[1]), t23 = __fadd2_rn(z[2], z[3]), t45 = __fadd2_rn(z[4], z[5]);
+      const float2 t67 = __fadd2_rn(z[6], z[7]), t89 = __fadd2_rn(z[8], z[9]);
+      const float2 T = __fadd2_rn(__fadd2_rn(__fadd2_rn(t01, t23), __fadd2_rn(t45, t67)), __fadd2_rn(t89, z[10]));
       const float2 y0 = __ffma2_rn(T, make_float2(-1.f, -1.f), v[0][jj]);
       v[0][jj] = y0;
 #pragma unroll
       for (int j = 0; j < 11; ++j) {
-        float2 A = __fadd2_rn(z[(j + 10) % 11], z[(j + 8) % 11]);
-        A = __fadd2_rn(A, z[(j + 7) % 11]);
-        A = __fadd2_rn(A, z[(j + 6) % 11]);
-        A = __fadd2_rn(A, z[(j + 2) % 11]);
-        A = __fadd2_rn(A, z[j]);
+        const float2 A = __fadd2_rn(__fadd2_rn(__fadd2_rn(z[(j + 10) % 11], z[(j + 8) % 11]),
+                                               __fadd2_rn(z[(j + 7) % 11], z[(j + 6) % 11])),
+                                    __fadd2_rn(z[(j + 2) % 11], z[j]));
         v[1 + j][jj] = __ffma2_rn(A, make_float2(2.f, 2.f), y0);
       }
     }
   }
-  float amax = 0.f;
+  float am[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial maxima
 #pragma unroll
   for (int a = 0; a < MSEG; ++a)
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) amax = fmaxf(amax, fmaxf(fabsf(v[a][jj].x), fabsf(v[a][jj].y)));
+    for (int jj = 0; jj < 4; ++jj) {
+      am[2 * jj] = fmaxf(am[2 * jj], fabsf(v[a][jj].x));
+      am[2 * jj + 1] = fmaxf(am[2 * jj + 1], fabsf(v[a][jj].y));
+    }
+  float amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])), fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if (lane == 0) red[r_local * 4 + w] = amax;
