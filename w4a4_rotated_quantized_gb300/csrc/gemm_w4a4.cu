@@ -323,85 +323,45 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ converters
     // warps 2-5: A rows 32 * (warp % 4) + lane (the TMEM lane quadrant the warp
-    // may access); warps 6-13: W rows 0..255.  Software-pipelined: the packed
-    // chunks of the next k-block are loaded while the current one is stored.
+    // may access); warps 6-13: W rows 0..255
     const bool is_a = warp < 6;
     const int r = is_a ? 32 * (warp & 3) + lane : int(threadIdx.x) - 64 - BM;
-    const bool active = is_a || r < BN;
     const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16);
-    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
-    const long total = long(my_tiles) * nkb;
-    const int src_off = is_a ? OFF_AP + r * 64 : OFF_BP + r * 64;
-    const int src_stride = is_a ? A_PK : B_PK;
-    auto load_packed = [&](long j, uint4* w) -> bool {
-      const int sp = int(j % SP);
-      if (!mbar_wait_bounded(&pk_full[sp], uint32_t((j / SP) & 1), abort_flag)) return false;
-      if (active) {
-        const unsigned char* src = sm + src_off + sp * src_stride;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(src + ((c ^ ((r >> 1) & 3)) << 4));
-      }
-      return true;
-    };
-    uint4 cur[4], nxt[4];
-    bool ok = total > 0 ? load_packed(0, nxt) : true;
-    uint32_t sum = 0;
-    for (long it = 0; it < total && ok; ++it) {
-      const int kb = int(it % nkb);
-      const int sp = int(it % SP), su = int(it % SU);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
-      if (kb == 0) sum = 0;
-      if (!mbar_wait_bounded(&un_empty[su], uint32_t((it / SU) & 1) ^ 1u, abort_flag)) break;
-      if (is_a) {
-        uint32_t o[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          unpack_word(cur[c].x, o[8 * c + 0], o[8 * c + 1]);
-          unpack_word(cur[c].y, o[8 * c + 2], o[8 * c + 3]);
-          unpack_word(cur[c].z, o[8 * c + 4], o[8 * c + 5]);
-          unpack_word(cur[c].w, o[8 * c + 6], o[8 * c + 7]);
-          sum = __dp4a((o[8 * c] + o[8 * c + 1]) + (o[8 * c + 2] + o[8 * c + 3]) + (o[8 * c + 4] + o[8 * c + 5]) +
-                           (o[8 * c + 6] + o[8 * c + 7]),
-                       0x01010101u, sum);
+    long it = 0;
+    int ti = 0;
+    for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++ti) {
+      uint32_t sum = 0;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int sp = int(it % SP), su = int(it % SU);
+        if (!mbar_wait_bounded(&pk_full[sp], uint32_t((it / SP) & 1), abort_flag) ||
+            !mbar_wait_bounded(&un_empty[su], uint32_t((it / SU) & 1) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
         }
-        QUAROT_TMEM_ST32(tmem_a_row + uint32_t(32 * su), o);
-      } else if (active) {
-        unsigned char* dst = sm + OFF_BU + su * B_UN + r * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
-          unpack_word(cur[c].x, l0, h0);
-          unpack_word(cur[c].y, l1, h1);
-          unpack_word(cur[c].z, l2, h2);
-          unpack_word(cur[c].w, l3, h3);
-          sum = __dp4a((l0 + h0) + (l1 + h1) + (l2 + h2) + (l3 + h3), 0x01010101u, sum);
-          *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
-          *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
+        if (is_a) {
+          uint32_t o[32];
+          sum += convert_row_regs(sm + OFF_AP + sp * A_PK + r * 64, r, o);
+          QUAROT_TMEM_ST32(tmem_a_row + uint32_t(32 * su), o);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          fence_before_sync();
+        } else {
+          if (r < BN) sum += convert_row(sm + OFF_BP + sp * B_PK + r * 64, r, sm + OFF_BU + su * B_UN + r * 128);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-      }
-      // prefetch the next k-block's packed chunks while the stores drain
-      if (it + 1 < total) ok = load_packed(it + 1, nxt);
-      if (is_a) {
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        fence_before_sync();
-      } else {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&un_full[su]);
-        mbar_arrive(&pk_empty[sp]);
-      }
-      if (kb == nkb - 1) {
-        const int ti = int(it / nkb);
-        const int a = ti & 1;
-        if (!mbar_wait_bounded(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
-        if (is_a) rsA[a * BM + r] = int(sum);
-        else if (r < BN_MAX) rsB[a * BN_MAX + r] = int(sum);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&rs_full[a]);
+        if (lane == 0) {
+          mbar_arrive(&un_full[su]);
+          mbar_arrive(&pk_empty[sp]);
+        }
       }
+      if (!ok) break;
+      const int a = ti & 1;
+      if (!mbar_wait_bounded(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+      if (is_a) rsA[a * BM + r] = int(sum);
+      else if (r < BN_MAX) rsB[a * BN_MAX + r] = int(sum);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rs_full[a]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
