@@ -438,6 +438,364 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   }
 }
 
+// ===================================================================== 2-SM kernel
+// The same contraction on CTA pairs (thread-block clusters of 2) with the
+// 2-SM MMA, tcgen05.mma.cta_group::2: a pair computes a 256 x BN tile; each
+// CTA holds its 128 rows of A (converted into its own tensor memory) and one
+// half of the BN weight rows (converted into its own shared memory), so each
+// SM converts 128 + BN/2 rows per k-block instead of 128 + BN.  The leader
+// CTA (rank 0) issues the MMAs; completion is committed to both CTAs'
+// barriers (multicast); the peer's converters and epilogue signal the
+// leader's barriers remotely.  Per CTA, tensor memory holds two accumulators
+// (columns [0, BN) and [BN, 2 BN)) and two A stages (columns 448, 480).
+namespace pair {
+
+constexpr int BM = 128;          // rows per CTA (256 per pair)
+constexpr int BNH_MAX = 112;     // weight rows per CTA (BN <= 224)
+constexpr int SP = 6;            // packed ring stages
+constexpr int SA = 2;            // A stages (tensor memory)
+constexpr int SB = 4;            // W stages (shared memory)
+constexpr int NCW = 8;           // converter warps: 4 for A, 4 for W
+constexpr int NEW = 4;           // epilogue warps
+constexpr int NTHREADS = 32 * (2 + NCW + NEW);  // 448
+constexpr int A_PK = BM * BKB, B_PK = BNH_MAX * BKB;  // 8 KB, 7 KB
+constexpr int B_UN = BNH_MAX * BK;                     // 14 KB
+constexpr int OFF_BU = 0;
+constexpr int OFF_AP = OFF_BU + SB * B_UN;
+constexpr int OFF_BP = OFF_AP + SP * A_PK;
+constexpr int OFF_BAR = ((OFF_BP + SP * B_PK) + 1023) / 1024 * 1024;
+// barriers: pk_full[SP] pk_empty[SP] a_full[SA] a_empty[SA] b_full[SB] b_empty[SB]
+//           acc_full[2] acc_empty[2] rs_full[2] rs_empty[2] drain
+constexpr int NBAR = 2 * SP + 2 * SA + 2 * SB + 8 + 1;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int OFF_RSA = OFF_MISC + 16;          // int [2][BM]
+constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;   // int [2][BNH_MAX]
+constexpr int SMEM_USED = OFF_RSB + 2 * BNH_MAX * 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_A_COL = 448;
+constexpr uint32_t IDESC_BASE = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(256 >> 4) << 24);
+static_assert(OFF_AP % 1024 == 0 && OFF_BP % 1024 == 0, "stage alignment");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void arrive_at(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa(smem_u32(bar), rank))
+               : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded cluster-scope wait (QUAROT_ERR_TIMEOUT after kWaitLimitNs).
+__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (try_wait_cluster(bar, parity)) return true;
+    if ((it & 63) == 63) {
+      if (abort != nullptr && *abort) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        record_error(QUAROT_ERR_TIMEOUT);
+        if (abort != nullptr) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void mma2_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void commit2(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(uint16_t(3))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K, int BN,
+                      __half* __restrict__ y, int32_t* __restrict__ acc_out) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* pk_full = bars;
+  uint64_t* pk_empty = pk_full + SP;
+  uint64_t* a_full = pk_empty + SP;
+  uint64_t* a_empty = a_full + SA;
+  uint64_t* b_full = a_empty + SA;
+  uint64_t* b_empty = b_full + SB;
+  uint64_t* acc_full = b_empty + SB;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* rs_full = acc_empty + 2;
+  uint64_t* rs_empty = rs_full + 2;
+  uint64_t* drain = rs_empty + 2;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
+  int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
+  int* rsB = reinterpret_cast<int*>(sm + OFF_RSB);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair_id = int(blockIdx.x) >> 1, n_pairs = int(gridDim.x) >> 1;
+  const int BNH = BN / 2;
+  const int nkb = K / BK;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + 2 * BM - 1) / (2 * BM)) * n_tiles_n;
+  const uint32_t idesc = IDESC_BASE | (uint32_t(BN >> 3) << 17);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SP; ++s) {
+      mbar_init(&pk_full[s], 1);
+      mbar_init(&pk_empty[s], NCW);
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&a_full[s], 2 * 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&b_full[s], 2 * 4);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 2 * NEW);
+      mbar_init(&rs_full[s], 2 * NCW);
+      mbar_init(&rs_empty[s], 2 * NEW);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival
+  fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      long issued = 0, it = 0;
+      const int b_bytes = BNH * BKB;
+      for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs) {
+        const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
+        const int n0 = (tile % n_tiles_n) * BN + int(rank) * BNH;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = int(it % SP);
+          if (!mbar_wait_bounded(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(&pk_full[s], A_PK + b_bytes);
+          tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
+          tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
+          issued = it + 1;
+        }
+      }
+      if (*abort_flag) {
+        for (long j = (issued > SP ? issued - SP : 0); j < issued; ++j)
+          mbar_wait_bounded(&pk_full[j % SP], uint32_t((j / SP) & 1), nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      long it = 0;
+      int ti = 0;
+      for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
+        const int a = ti & 1;
+        if (!wait_cluster(&acc_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+        fence_after_sync();
+        const uint32_t tmem_d = tmem_base + uint32_t(a * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int sa = int(it % SA), sb = int(it % SB);
+          if (!wait_cluster(&a_full[sa], uint32_t((it / SA) & 1), abort_flag) ||
+              !wait_cluster(&b_full[sb], uint32_t((it / SB) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          const uint32_t ta = tmem_base + TMEM_A_COL + uint32_t(32 * sa);
+          const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + sb * B_UN));
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            mma2_ts(tmem_d, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
+          commit2(&a_empty[sa]);
+          commit2(&b_empty[sb]);
+        }
+        if (!ok) break;
+        commit2(&acc_full[a]);
+      }
+      commit2(drain);
+      wait_cluster(drain, 0, nullptr);
+    }
+  } else if (warp < 2 + NCW) {
+    // ------------------------------------------------------------ converters
+    // warps 2-5: A rows 32 * (warp % 4) + lane (TMEM lane quadrant); warps 6-9:
+    // this CTA's half of the weight rows
+    const bool is_a = warp < 6;
+    const int r = is_a ? 32 * (warp & 3) + lane : int(threadIdx.x) - 32 * 6;
+    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16);
+    long it = 0;
+    int ti = 0;
+    for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
+      uint32_t sum = 0;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int sp = int(it % SP);
+        const int ss = is_a ? int(it % SA) : int(it % SB);
+        const uint32_t par = is_a ? uint32_t((it / SA) & 1) : uint32_t((it / SB) & 1);
+        if (!mbar_wait_bounded(&pk_full[sp], uint32_t((it / SP) & 1), abort_flag) ||
+            !wait_cluster(is_a ? &a_empty[ss] : &b_empty[ss], par ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (is_a) {
+          uint32_t o[32];
+          sum += convert_row_regs(sm + OFF_AP + sp * A_PK + r * 64, r, o);
+          QUAROT_TMEM_ST32(tmem_a_row + uint32_t(32 * ss), o);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          fence_before_sync();
+        } else {
+          if (r < BNH) sum += convert_row(sm + OFF_BP + sp * B_PK + r * 64, r, sm + OFF_BU + ss * B_UN + r * 128);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) {
+          arrive_at(is_a ? &a_full[ss] : &b_full[ss], 0);
+          mbar_arrive(&pk_empty[sp]);
+        }
+      }
+      if (!ok) break;
+      const int a = ti & 1;
+      if (!wait_cluster(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+      if (is_a) rsA[a * BM + r] = int(sum);
+      else if (r < BNH_MAX) rsB[a * BNH_MAX + r] = int(sum);
+      __syncwarp();
+      if (lane == 0) {
+        arrive_at(&rs_full[a], 0);
+        arrive_at(&rs_full[a], 1);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int r = 32 * q + lane;
+    const bool vec_ok = (N % 8) == 0;
+    int ti = 0;
+    for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
+      const int a = ti & 1;
+      const uint32_t par = uint32_t((ti >> 1) & 1);
+      if (!wait_cluster(&acc_full[a], par, abort_flag) || !wait_cluster(&rs_full[a], par, abort_flag)) break;
+      fence_after_sync();
+      const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM, n0 = (tile % n_tiles_n) * BN;
+      const int gm = m0 + r;
+      const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
+      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[a * BM + r]);
+      const uint32_t rsb0 = mapa(smem_u32(rsB + a * BNH_MAX), 0), rsb1 = mapa(smem_u32(rsB + a * BNH_MAX), 1);
+      const uint32_t tmem_row = tmem_base + uint32_t(a * BN) + (uint32_t(32 * q) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        __syncwarp();
+        QUAROT_TMEM_LD32(tmem_row + uint32_t(c0), v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int gn = n0 + c0;
+        if (gm < M && gn < N) {
+          float acc[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c0 + j;  // < BNH: rows of rank 0, else rank 1
+            const int rsbv = col < BNH ? ld_cluster_s32(rsb0 + 4u * uint32_t(col))
+                                       : ld_cluster_s32(rsb1 + 4u * uint32_t(col - BNH));
+            acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(rsbv)) + bias_r;
+          }
+          __half* yrow = y + size_t(gm) * N + gn;
+          if (vec_ok && gn + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sw + gn + j));
+              const uint32_t sws[4] = {s8.x, s8.y, s8.z, s8.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 wsc = h2_to_f2(sws[e]);
+                const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x));
+                const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
+                o[e] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+              }
+              *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          } else {
+            for (int j = 0; j < 32 && gn + j < N; ++j)
+              yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
+          }
+          if (acc_out != nullptr) {
+            int32_t* arow = acc_out + size_t(gm) * N + gn;
+            for (int j = 0; j < 32 && gn + j < N; ++j) arow[j] = __float2int_rn(acc[j]);
+          }
+        }
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        arrive_at(&acc_empty[a], 0);
+        arrive_at(&rs_empty[a], 0);
+        arrive_at(&rs_empty[a], 1);
+      }
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
+  if (warp == 1) {
+    fence_after_sync();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace pair
+
 // ------------------------------------------------------------------ host
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::once_flag g_encode_once;
@@ -482,6 +840,23 @@ static int pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
+// Pair kernel: the N-tile width minimising the per-pair makespan.
+static int pick_bn_pair(int64_t M, int64_t N, int pairs) {
+  const int cands[4] = {224, 192, 160, 128};
+  int best = 224;
+  int64_t best_cost = -1;
+  const int64_t mt = (M + 255) / 256;
+  for (int bn : cands) {
+    const int64_t tiles = mt * ((N + bn - 1) / bn);
+    const int64_t cost = ((tiles + pairs - 1) / pairs) * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -510,6 +885,39 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   if (!get_encoder()) return QUAROT_ERR_CUDA;
   const int sms = sm_count();
   if (sms <= 0) return QUAROT_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M > BM && sms >= 2) {
+    // 2-SM path: clusters of two CTAs, one 256 x BN tile per pair
+    const int pairs = sms / 2;
+    const int bn = pick_bn_pair(M, N, pairs);
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, a_q, M, K, pair::BM) || !make_map(&tb, w_q, N, K, bn / 2)) return QUAROT_ERR_CUDA;
+    static bool pattr = false;
+    if (!pattr) {
+      if (cudaFuncSetAttribute(pair::w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               pair::SMEM_BYTES) != cudaSuccess)
+        return QUAROT_ERR_LAUNCH;
+      pattr = true;
+    }
+    const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+    const int64_t npairs = tiles < pairs ? tiles : pairs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(2 * npairs));
+    cfg.blockDim = dim3(pair::NTHREADS);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::w4a4_gemm_pair_kernel, ta, tb,
+                                             static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale),
+                                             int(M), int(N), int(K), bn, static_cast<__half*>(y), acc_out);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+  }
   const int bn = pick_bn(M, N, sms);
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_q, M, K, BM) || !make_map(&tb, w_q, N, K, bn)) return QUAROT_ERR_CUDA;
@@ -522,7 +930,7 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   }
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
   const unsigned grid = unsigned(tiles < sms ? tiles : sms);
-  w4a4_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(
+  w4a4_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(
       ta, tb, static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale), int(M), int(N),
       int(K), bn, static_cast<__half*>(y), acc_out);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
