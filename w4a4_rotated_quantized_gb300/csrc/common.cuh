@@ -66,6 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or `ns` elapse, instead of returning at once and spinning
+// (a spinning waiter takes issue slots from the warps that share its
+// scheduler, which are usually the ones it is waiting for).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records QUAROT_ERR_TIMEOUT) if it does not within kWaitLimitNs, or if
 // *abort is set by another thread of the CTA.
@@ -73,15 +89,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (abort != nullptr && *abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        record_error(QUAROT_ERR_TIMEOUT);
-        if (abort != nullptr) *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      record_error(QUAROT_ERR_TIMEOUT);
+      if (abort != nullptr) *abort = 1;
+      return false;
     }
   }
 }

@@ -411,12 +411,15 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
               *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
             }
           } else {
-            for (int j = 0; j < 32 && gn + j < N; ++j)
-              yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
           }
           if (acc_out != nullptr) {
             int32_t* arow = acc_out + size_t(gm) * N + gn;
-            for (int j = 0; j < 32 && gn + j < N; ++j) arow[j] = __float2int_rn(acc[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) arow[j] = __float2int_rn(acc[j]);
           }
         }
       }
@@ -450,32 +453,120 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // (columns [0, BN) and [BN, 2 BN)) and two A stages (columns 448, 480).
 namespace pair {
 
+// 2-SM variant for M > 128: clusters of two CTAs on one TPC share a 256 x BN
+// tile through tcgen05.mma.cta_group::2 (M = 256).  Each CTA converts its own
+// 128 activation rows (into its tensor memory, as the A operand) and HALF of
+// the BN weight rows (into its shared memory); the pair's tensor cores read
+// both halves of W, so per SM a k-block needs 128 + BN/2 converted rows
+// instead of 128 + BN.  Only the leader CTA (rank 0) issues MMAs and its
+// commits are multicast back to both CTAs.  Warps signal only barriers of
+// their own CTA (cta-scope release, no cluster-wide fence on the converters'
+// critical path); in the other CTA one relay thread (warp 1, idle there)
+// forwards each completed stage to the leader with a single remote arrival.
+//
+// Converted operands go through one ring of S = 8 stages: stage s holds the A
+// k-block in tensor memory (columns 256 + 32 s) and this CTA's W half in shared
+// memory, behind one full and one empty barrier.  Tensor memory also holds one
+// accumulator in columns [0, BN).  Eight stages let the converters run ahead
+// of the MMA by 8 k-blocks, which hides the cross-SM round trip (converters
+// done -> relay -> leader MMA -> multicast commit -> stage free, about 2 us)
+// and the epilogue of the previous tile (the MMA of the next tile waits for
+// the epilogue to drain the accumulator, the converters do not).  Row sums of the converted W rows are
+// written into both CTAs' shared memory so that each epilogue reads its
+// correction terms locally.
+//
+//   warp 0         TMA producer (this CTA's 128 A rows and BN/2 W rows)
+//   warp 1         TMEM allocator; MMA issuer in the leader, relay in the peer
+//   warps 2-9      A converters (packed -> e4m3 bytes -> TMEM), two warps per
+//                  TMEM lane quadrant, each converting half of every row
+//   warps 10-17    W converters (packed -> e4m3 bytes -> shared memory), 16
+//                  rows per warp, lanes l and l + 16 converting the two halves
+//                  of one row
+//   warps 18-21    epilogue, one warp per TMEM lane quadrant
+// Converting half rows gives each thread a short dependency chain per k-block
+// and four converter warps per scheduler to hide it.
 constexpr int BM = 128;          // rows per CTA (256 per pair)
 constexpr int BNH_MAX = 112;     // weight rows per CTA (BN <= 224)
-constexpr int SP = 6;            // packed ring stages
-constexpr int SA = 2;            // A stages (tensor memory)
-constexpr int SB = 4;            // W stages (shared memory)
-constexpr int NCW = 8;           // converter warps: 4 for A, 4 for W
+constexpr int SP = 4;            // packed ring stages
+constexpr int S = 8;             // converted stages (A in tensor memory, W in shared memory)
+constexpr int NAW = 8, NBW = 8;  // A / W converter warps
+constexpr int NCW = NAW + NBW;
 constexpr int NEW = 4;           // epilogue warps
-constexpr int NTHREADS = 32 * (2 + NCW + NEW);  // 448
+constexpr int EPI_WARP0 = 2 + NCW;
+constexpr int NTHREADS = 32 * (2 + NCW + NEW);  // 704
 constexpr int A_PK = BM * BKB, B_PK = BNH_MAX * BKB;  // 8 KB, 7 KB
 constexpr int B_UN = BNH_MAX * BK;                     // 14 KB
 constexpr int OFF_BU = 0;
-constexpr int OFF_AP = OFF_BU + SB * B_UN;
+constexpr int OFF_AP = OFF_BU + S * B_UN;
 constexpr int OFF_BP = OFF_AP + SP * A_PK;
 constexpr int OFF_BAR = ((OFF_BP + SP * B_PK) + 1023) / 1024 * 1024;
-// barriers: pk_full[SP] pk_empty[SP] a_full[SA] a_empty[SA] b_full[SB] b_empty[SB]
-//           acc_full[2] acc_empty[2] rs_full[2] rs_empty[2] drain
-constexpr int NBAR = 2 * SP + 2 * SA + 2 * SB + 8 + 1;
+// barriers: pk_full[SP] pk_empty[SP] full[S] empty[S] acc_full acc_empty
+//           rs_full[2] rs_empty[2] drain
+constexpr int NBAR = 2 * SP + 2 * S + 2 + 4 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int OFF_RSA = OFF_MISC + 16;          // int [2][BM]
-constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;   // int [2][BNH_MAX]
-constexpr int SMEM_USED = OFF_RSB + 2 * BNH_MAX * 4;
+constexpr int OFF_RSA = OFF_MISC + 16;             // int [2][2][BM]: per half row
+constexpr int OFF_RSB = OFF_RSA + 4 * BM * 4;      // int [2][BN_MAX]: the whole tile's W row sums
+constexpr int OFF_SW = OFF_RSB + 2 * BN_MAX * 4;   // float [NEW][BN_MAX]: each epilogue warp's weight scales
+constexpr int SMEM_USED = OFF_SW + NEW * BN_MAX * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_A_COL = 448;
+constexpr uint32_t TMEM_A_COL = 256;
 constexpr uint32_t IDESC_BASE = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(256 >> 4) << 24);
 static_assert(OFF_AP % 1024 == 0 && OFF_BP % 1024 == 0, "stage alignment");
+static_assert(B_PK % 1024 == 0 && B_UN % 1024 == 0 && A_PK % 1024 == 0, "stage alignment");
+static_assert(TMEM_A_COL + 32 * S <= TMEM_COLS && BN_MAX <= int(TMEM_A_COL), "tensor memory plan");
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+
+#define QUAROT_TMEM_ST16(taddr, r)                                                                 \
+  asm volatile(                                                                                    \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+      "%15,%16};" ::"r"(taddr),                                                                    \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),     \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]) \
+      : "memory")
+
+// Half `part` of a packed row (its 16-byte chunks 2 part and 2 part + 1,
+// 64B-swizzled source) -> 16 words of e4m3 bytes, the row's TMEM columns
+// [16 part, 16 part + 16) in the K order of convert_row_regs; returns the byte
+// sum of the offset codes.
+__device__ __forceinline__ uint32_t convert_half_regs(const unsigned char* src_row, int r, int part, uint32_t* o) {
+  uint4 w[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) w[c] = *reinterpret_cast<const uint4*>(src_row + (((2 * part + c) ^ ((r >> 1) & 3)) << 4));
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    unpack_word(w[c].x, o[8 * c + 0], o[8 * c + 1]);
+    unpack_word(w[c].y, o[8 * c + 2], o[8 * c + 3]);
+    unpack_word(w[c].z, o[8 * c + 4], o[8 * c + 5]);
+    unpack_word(w[c].w, o[8 * c + 6], o[8 * c + 7]);
+    acc = __dp4a((o[8 * c] + o[8 * c + 1]) + (o[8 * c + 2] + o[8 * c + 3]) + (o[8 * c + 4] + o[8 * c + 5]) +
+                     (o[8 * c + 6] + o[8 * c + 7]),
+                 0x01010101u, acc);
+  }
+  return acc;
+}
+// Half `part` of a packed row -> its 64 e4m3 bytes in the 128B-swizzled
+// K-major destination row (the same layout as convert_row).
+__device__ __forceinline__ uint32_t convert_half(const unsigned char* src_row, int r, int part, unsigned char* dst_row) {
+  uint4 w[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) w[c] = *reinterpret_cast<const uint4*>(src_row + (((2 * part + c) ^ ((r >> 1) & 3)) << 4));
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int cc = 2 * part + c;
+    uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+    unpack_word(w[c].x, l0, h0);
+    unpack_word(w[c].y, l1, h1);
+    unpack_word(w[c].z, l2, h2);
+    unpack_word(w[c].w, l3, h3);
+    acc = __dp4a((l0 + h0) + (l1 + h1) + (l2 + h2) + (l3 + h3), 0x01010101u, acc);
+    *reinterpret_cast<uint4*>(dst_row + (((2 * cc) ^ (r & 7)) << 4)) = make_uint4(l0, h0, l1, h1);
+    *reinterpret_cast<uint4*>(dst_row + (((2 * cc + 1) ^ (r & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
+  }
+  return acc;
+}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -487,44 +578,70 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// Arrival on a barrier of CTA `rank` that publishes generic-proxy shared-memory
+// data written for that CTA (release at cluster scope: costs a cluster-wide
+// fence of ~0.5 us on the issuing thread, so used once per tile only).
 __device__ __forceinline__ void arrive_at(uint64_t* bar, uint32_t rank) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa(smem_u32(bar), rank))
                : "memory");
 }
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
+// Stage hand-off to the leader (release at CTA scope, no cluster-wide fence).
+// What the leader's MMA reads was published before this arrival by the
+// writers themselves: shared-memory operands by fence.proxy.async (visible to
+// the tensor cores), tensor-memory operands by tcgen05.wait::st, and drained
+// accumulator reads by tcgen05.wait::ld.
+__device__ __forceinline__ void handoff_at(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(mapa(smem_u32(bar), rank)) : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }
-// Bounded cluster-scope wait (QUAROT_ERR_TIMEOUT after kWaitLimitNs).
+// Bounded wait with cluster-scope acquire (QUAROT_ERR_TIMEOUT after
+// kWaitLimitNs), for barriers that publish generic-proxy data written by the
+// other CTA.  The acquire costs ~0.4 us per call, so it is used once per tile;
+// the per-k-block stage barriers use CTA-scope waits.
 __device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (try_wait_cluster(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (try_wait_cluster(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (abort != nullptr && *abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        record_error(QUAROT_ERR_TIMEOUT);
-        if (abort != nullptr) *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (try_wait_cluster(bar, parity, 20000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      record_error(QUAROT_ERR_TIMEOUT);
+      if (abort != nullptr) *abort = 1;
+      return false;
     }
   }
+}
+// Warp-uniform forms for the single-issuer roles: the whole warp waits and
+// loops (lane 0 issues), so no lane of these warps sits at the final CTA
+// barrier while lane 0 is still working.  (With lane 0 alone in the loop, the
+// converter warps sharing its scheduler woke ~1.3 us late from every barrier
+// phase.)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
+}
+__device__ __forceinline__ bool warp_flag(volatile int* flag) {
+  return __shfl_sync(0xffffffffu, *flag, 0) != 0;
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
+// 256-bit global store (one full 32-byte sector per thread; p 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* o) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+               "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+               : "memory");
 }
 __device__ __forceinline__ void mma2_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -552,19 +669,18 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* pk_full = bars;
   uint64_t* pk_empty = pk_full + SP;
-  uint64_t* a_full = pk_empty + SP;
-  uint64_t* a_empty = a_full + SA;
-  uint64_t* b_full = a_empty + SA;
-  uint64_t* b_empty = b_full + SB;
-  uint64_t* acc_full = b_empty + SB;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* rs_full = acc_empty + 2;
+  uint64_t* full = pk_empty + SP;
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* rs_full = acc_empty + 1;
   uint64_t* rs_empty = rs_full + 2;
   uint64_t* drain = rs_empty + 2;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
   int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
   int* rsB = reinterpret_cast<int*>(sm + OFF_RSB);
+  float* swS = reinterpret_cast<float*>(sm + OFF_SW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -581,19 +697,16 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       mbar_init(&pk_full[s], 1);
       mbar_init(&pk_empty[s], NCW);
     }
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(&a_full[s], 2 * 4);
-      mbar_init(&a_empty[s], 1);
+    // the leader's full barriers count its own converter warps plus the relay
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], leader ? NCW + 1 : NCW);
+      mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < SB; ++s) {
-      mbar_init(&b_full[s], 2 * 4);
-      mbar_init(&b_empty[s], 1);
-    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, leader ? NEW + 1 : NEW);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&acc_full[s], 1);
-      mbar_init(&acc_empty[s], 2 * NEW);
-      mbar_init(&rs_full[s], 2 * NCW);
-      mbar_init(&rs_empty[s], 2 * NEW);
+      mbar_init(&rs_full[s], 2 * NCW);   // every converter warp of the pair
+      mbar_init(&rs_empty[s], 2 * NEW);  // every epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -614,66 +727,92 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      long issued = 0, it = 0;
-      const int b_bytes = BNH * BKB;
-      for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs) {
-        const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
-        const int n0 = (tile % n_tiles_n) * BN + int(rank) * BNH;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = int(it % SP);
-          if (!mbar_wait_bounded(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
+    long issued = 0, it = 0;
+    const int b_bytes = BNH * BKB;
+    for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs) {
+      const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
+      const int n0 = (tile % n_tiles_n) * BN + int(rank) * BNH;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = int(it % SP);
+        if (!warp_wait(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
+        if (lane == 0) {
           mbar_arrive_expect_tx(&pk_full[s], A_PK + b_bytes);
           tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
           tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
-          issued = it + 1;
         }
-      }
-      if (*abort_flag) {
-        for (long j = (issued > SP ? issued - SP : 0); j < issued; ++j)
-          mbar_wait_bounded(&pk_full[j % SP], uint32_t((j / SP) & 1), nullptr);
+        __syncwarp();
+        issued = it + 1;
       }
     }
+    if (warp_flag(abort_flag) && lane == 0) {
+      for (long j = (issued > SP ? issued - SP : 0); j < issued; ++j)
+        mbar_wait_bounded(&pk_full[j % SP], uint32_t((j / SP) & 1), nullptr);
+    }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader)
-    if (leader && lane == 0) {
+    if (leader) {
+      // ---------------------------------------------------------- MMA issuer
       long it = 0;
       int ti = 0;
-      for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
-        const int a = ti & 1;
-        if (!wait_cluster(&acc_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+      for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs, ++ti) {
+        if (!warp_wait(acc_empty, uint32_t(ti & 1) ^ 1u, abort_flag)) break;
         fence_after_sync();
-        const uint32_t tmem_d = tmem_base + uint32_t(a * BN);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int sa = int(it % SA), sb = int(it % SB);
-          if (!wait_cluster(&a_full[sa], uint32_t((it / SA) & 1), abort_flag) ||
-              !wait_cluster(&b_full[sb], uint32_t((it / SB) & 1), abort_flag)) {
+          const int s = int(it % S);
+          if (!warp_wait(&full[s], uint32_t((it / S) & 1), abort_flag)) {
             ok = false;
             break;
           }
           fence_after_sync();
-          const uint32_t ta = tmem_base + TMEM_A_COL + uint32_t(32 * sa);
-          const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + sb * B_UN));
+          if (lane == 0) {
+            const uint32_t ta = tmem_base + TMEM_A_COL + uint32_t(32 * s);
+            const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + s * B_UN));
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk)
-            mma2_ts(tmem_d, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
-          commit2(&a_empty[sa]);
-          commit2(&b_empty[sb]);
+            for (int kk = 0; kk < BK / 32; ++kk)
+              mma2_ts(tmem_base, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
+            commit2(&empty[s]);
+          }
+          __syncwarp();
         }
         if (!ok) break;
-        commit2(&acc_full[a]);
+        if (lane == 0) commit2(acc_full);
+        __syncwarp();
       }
-      commit2(drain);
-      wait_cluster(drain, 0, nullptr);
+      if (lane == 0) {
+        commit2(drain);
+        mbar_wait_bounded(drain, 0, nullptr);
+      }
+    } else {
+      // ---------------------------------------------------------- relay
+      // forward this CTA's completed stages to the leader, in the order the
+      // MMA issuer consumes them
+      long it = 0;
+      int ti = 0;
+      bool ok = true;
+      for (int tile = pair_id; ok && tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs, ++ti) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = int(it % S);
+          if (!warp_wait(&full[s], uint32_t((it / S) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) handoff_at(&full[s], 0);
+          __syncwarp();
+        }
+        if (!ok || !warp_wait(acc_empty, uint32_t(ti & 1), abort_flag)) break;
+        if (lane == 0) handoff_at(acc_empty, 0);
+        __syncwarp();
+      }
     }
-  } else if (warp < 2 + NCW) {
+  } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ converters
-    // warps 2-5: A rows 32 * (warp % 4) + lane (TMEM lane quadrant); warps 6-9:
-    // this CTA's half of the weight rows
-    const bool is_a = warp < 6;
-    const int r = is_a ? 32 * (warp & 3) + lane : int(threadIdx.x) - 32 * 6;
-    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16);
+    // A: row 32 * (warp % 4) + lane (the warp's TMEM lane quadrant), half
+    // (warp - 2) / 4; W: row 16 * (warp - 10) + lane % 16 of this CTA's half of
+    // the weight rows, half lane / 16
+    const bool is_a = warp < 2 + NAW;
+    const int r = is_a ? 32 * (warp & 3) + lane : 16 * (warp - 2 - NAW) + (lane & 15);
+    const int part = is_a ? (warp - 2) >> 2 : lane >> 4;
+    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(16 * part);
     long it = 0;
     int ti = 0;
     for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
@@ -681,34 +820,40 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int sp = int(it % SP);
-        const int ss = is_a ? int(it % SA) : int(it % SB);
-        const uint32_t par = is_a ? uint32_t((it / SA) & 1) : uint32_t((it / SB) & 1);
+        const int ss = int(it % S);
         if (!mbar_wait_bounded(&pk_full[sp], uint32_t((it / SP) & 1), abort_flag) ||
-            !wait_cluster(is_a ? &a_empty[ss] : &b_empty[ss], par ^ 1u, abort_flag)) {
+            !mbar_wait_bounded(&empty[ss], uint32_t((it / S) & 1) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         if (is_a) {
-          uint32_t o[32];
-          sum += convert_row_regs(sm + OFF_AP + sp * A_PK + r * 64, r, o);
-          QUAROT_TMEM_ST32(tmem_a_row + uint32_t(32 * ss), o);
+          uint32_t o[16];
+          sum += convert_half_regs(sm + OFF_AP + sp * A_PK + r * 64, r, part, o);
+          QUAROT_TMEM_ST16(tmem_a_row + uint32_t(32 * ss), o);
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           fence_before_sync();
         } else {
-          if (r < BNH) sum += convert_row(sm + OFF_BP + sp * B_PK + r * 64, r, sm + OFF_BU + ss * B_UN + r * 128);
+          if (r < BNH)
+            sum += convert_half(sm + OFF_BP + sp * B_PK + r * 64, r, part, sm + OFF_BU + ss * B_UN + r * 128);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
         if (lane == 0) {
-          arrive_at(is_a ? &a_full[ss] : &b_full[ss], 0);
+          mbar_arrive(&full[ss]);
           mbar_arrive(&pk_empty[sp]);
         }
       }
       if (!ok) break;
       const int a = ti & 1;
+      if (!is_a) sum += __shfl_xor_sync(0xffffffffu, sum, 16);  // the row's other half
       if (!wait_cluster(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
-      if (is_a) rsA[a * BM + r] = int(sum);
-      else if (r < BNH_MAX) rsB[a * BNH_MAX + r] = int(sum);
+      if (is_a) {
+        rsA[(2 * a + part) * BM + r] = int(sum);
+      } else if (part == 0 && r < BNH) {
+        int* dst = rsB + a * BN_MAX + int(rank) * BNH + r;
+        *dst = int(sum);
+        st_cluster_s32(mapa(smem_u32(dst), rank ^ 1u), int(sum));
+      }
       __syncwarp();
       if (lane == 0) {
         arrive_at(&rs_full[a], 0);
@@ -717,67 +862,78 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int e = warp - EPI_WARP0;  // 0..3
+    const int q = warp & 3;          // TMEM lane quadrant of this warp
     const int r = 32 * q + lane;
-    const bool vec_ok = (N % 8) == 0;
+    const int nchunks = BN / 32;
+    const bool vec_ok = (N % 16) == 0 && (reinterpret_cast<uintptr_t>(y) & 31) == 0;
     int ti = 0;
     for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
       const int a = ti & 1;
-      const uint32_t par = uint32_t((ti >> 1) & 1);
-      if (!wait_cluster(&acc_full[a], par, abort_flag) || !wait_cluster(&rs_full[a], par, abort_flag)) break;
-      fence_after_sync();
       const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM, n0 = (tile % n_tiles_n) * BN;
       const int gm = m0 + r;
+      // this warp's weight scales of the tile (warp-private, loaded before the
+      // accumulator is ready; the warp's reads of the previous tile are done)
+      float* sws_w = swS + e * BN_MAX;
+      for (int c = 0; c < nchunks; ++c)
+        sws_w[32 * c + lane] = n0 + 32 * c + lane < N ? __half2float(sw[n0 + 32 * c + lane]) : 0.f;
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
-      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[a * BM + r]);
-      const uint32_t rsb0 = mapa(smem_u32(rsB + a * BNH_MAX), 0), rsb1 = mapa(smem_u32(rsB + a * BNH_MAX), 1);
-      const uint32_t tmem_row = tmem_base + uint32_t(a * BN) + (uint32_t(32 * q) << 16);
+      __syncwarp();
+      if (!mbar_wait_bounded(acc_full, uint32_t(ti & 1), abort_flag) ||
+          !wait_cluster(&rs_full[a], uint32_t((ti >> 1) & 1), abort_flag))
+        break;
+      fence_after_sync();
+      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[2 * a * BM + r] + rsA[(2 * a + 1) * BM + r]);
+      const int* rsb = rsB + a * BN_MAX;
+      const uint32_t tmem_row = tmem_base + (uint32_t(32 * q) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int c0 = 32 * c;
+        const float* sws = sws_w + c0;  // sws[j]: scale of column n0 + c0 + j
         uint32_t v[32];
         __syncwarp();
         QUAROT_TMEM_LD32(tmem_row + uint32_t(c0), v);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (c == nchunks - 1) {  // the accumulator is no longer needed by this warp
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        }
         const int gn = n0 + c0;
         if (gm < M && gn < N) {
           float acc[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = c0 + j;  // < BNH: rows of rank 0, else rank 1
-            const int rsbv = col < BNH ? ld_cluster_s32(rsb0 + 4u * uint32_t(col))
-                                       : ld_cluster_s32(rsb1 + 4u * uint32_t(col - BNH));
-            acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(rsbv)) + bias_r;
-          }
+          for (int j = 0; j < 32; ++j)
+            acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(rsb[c0 + j])) + bias_r;
           __half* yrow = y + size_t(gm) * N + gn;
           if (vec_ok && gn + 32 <= N) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sw + gn + j));
-              const uint32_t sws[4] = {s8.x, s8.y, s8.z, s8.w};
-              uint32_t o[4];
+            for (int j = 0; j < 32; j += 16) {
+              uint32_t o[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 wsc = h2_to_f2(sws[e]);
-                const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x));
-                const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
-                o[e] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+              for (int t = 0; t < 8; ++t) {
+                const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * t], sxr), sws[j + 2 * t]));
+                const __half hi =
+                    __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * t + 1], sxr), sws[j + 2 * t + 1]));
+                o[t] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
               }
-              *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
+              st_global_v8(yrow + j, o);
             }
           } else {
-            for (int j = 0; j < 32 && gn + j < N; ++j)
-              yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), __half2float(sw[gn + j])));
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), sws[j]));
           }
           if (acc_out != nullptr) {
             int32_t* arow = acc_out + size_t(gm) * N + gn;
-            for (int j = 0; j < 32 && gn + j < N; ++j) arow[j] = __float2int_rn(acc[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) arow[j] = __float2int_rn(acc[j]);
           }
         }
       }
-      fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        arrive_at(&acc_empty[a], 0);
         arrive_at(&rs_empty[a], 0);
         arrive_at(&rs_empty[a], 1);
       }
