@@ -139,8 +139,12 @@ def _gemm_case(q, M, N, K, seed, codes_a=None, codes_w=None):
     return a, w, sx, sw, y.cpu().numpy(), acc.cpu().numpy()
 
 
+# M <= 128 runs the one-SM kernel; M > 128 with K % 256 == 0 the CTA-pair kernel
+# (ragged M and N tails in either CTA of a pair); (257, 513, 384) has an odd
+# k-block count and takes the one-SM kernel at M > 128
 @pytest.mark.parametrize("M,N,K", [(16, 256, 256), (128, 256, 128), (200, 300, 256), (1, 8, 128),
-                                   (257, 513, 384), (256, 512, 4096), (130, 264, 12288)])
+                                   (257, 513, 384), (256, 512, 4096), (130, 264, 12288),
+                                   (385, 136, 768), (600, 1000, 1024)])
 def test_gemm_bit_exact(q, M, N, K):
     a, w, sx, sw, y, acc = _gemm_case(q, M, N, K, 100 + M + N + K)
     ref = O.int_gemm(a, w)

@@ -516,6 +516,7 @@ static_assert(OFF_AP % 1024 == 0 && OFF_BP % 1024 == 0, "stage alignment");
 static_assert(B_PK % 1024 == 0 && B_UN % 1024 == 0 && A_PK % 1024 == 0, "stage alignment");
 static_assert(TMEM_A_COL + 32 * S <= TMEM_COLS && BN_MAX <= int(TMEM_A_COL), "tensor memory plan");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+static_assert(SP % 2 == 0 && S % 2 == 0, "converters take stages in pairs");
 
 #define QUAROT_TMEM_ST16(taddr, r)                                                                 \
   asm volatile(                                                                                    \
@@ -566,6 +567,15 @@ __device__ __forceinline__ uint32_t convert_half(const unsigned char* src_row, i
     *reinterpret_cast<uint4*>(dst_row + (((2 * cc + 1) ^ (r & 7)) << 4)) = make_uint4(l2, h2, l3, h3);
   }
   return acc;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -811,44 +821,101 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     // the weight rows, half lane / 16
     const bool is_a = warp < 2 + NAW;
     const int r = is_a ? 32 * (warp & 3) + lane : 16 * (warp - 2 - NAW) + (lane & 15);
-    const int part = is_a ? (warp - 2) >> 2 : lane >> 4;
-    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(16 * part);
-    long it = 0;
+    const uint32_t part = is_a ? uint32_t(warp - 2) >> 2 : uint32_t(lane) >> 4;
+    const bool active = is_a || r < BNH;
+    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16) + 16u * part;
+    // 32-bit shared addresses, swizzled chunk offsets hoisted out of the loop:
+    // the packed half row is 16-byte chunks 2 part and 2 part + 1 (64B swizzle),
+    // the unpacked half row chunks 4 part .. 4 part + 3 (128B swizzle)
+    const uint32_t swz_src = uint32_t(r >> 1) & 3u, swz_dst = uint32_t(r) & 7u;
+    const uint32_t src_row = smem_u32(sm + (is_a ? OFF_AP : OFF_BP)) + uint32_t(r) * 64u;
+    const uint32_t src0 = src_row + (((2u * part) ^ swz_src) << 4), src1 = src_row + (((2u * part + 1u) ^ swz_src) << 4);
+    const uint32_t pk_stride = is_a ? uint32_t(A_PK) : uint32_t(B_PK);
+    const uint32_t dst_row = smem_u32(sm + OFF_BU) + uint32_t(r) * 128u;
+    const uint32_t d0 = ((4u * part) ^ swz_dst) << 4, d1 = ((4u * part + 1u) ^ swz_dst) << 4;
+    const uint32_t d2 = ((4u * part + 2u) ^ swz_dst) << 4, d3 = ((4u * part + 3u) ^ swz_dst) << 4;
+    // Each iteration converts two consecutive k-blocks (stages sp, sp + 1 and
+    // ss, ss + 1: both rings have even sizes and the k-block count is even, so
+    // a pair never straddles a wrap): twice the independent work per thread
+    // and one set of waits, fences and arrivals per two k-blocks.
+    uint32_t sp = 0, pk_par = 0, ss = 0, s_par = 0;  // ring positions and phase parities
     int ti = 0;
     for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
       uint32_t sum = 0;
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int sp = int(it % SP);
-        const int ss = int(it % S);
-        if (!mbar_wait_bounded(&pk_full[sp], uint32_t((it / SP) & 1), abort_flag) ||
-            !mbar_wait_bounded(&empty[ss], uint32_t((it / S) & 1) ^ 1u, abort_flag)) {
+      for (int kb = 0; kb < nkb; kb += 2) {
+        if (!mbar_wait_bounded(&pk_full[sp], pk_par, abort_flag) ||
+            !mbar_wait_bounded(&pk_full[sp + 1], pk_par, abort_flag) ||
+            !mbar_wait_bounded(&empty[ss], s_par ^ 1u, abort_flag) ||
+            !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
+        uint32_t o[32];
+        if (active) {
+          const uint4 w0 = lds128(src0 + sp * pk_stride), w1 = lds128(src1 + sp * pk_stride);
+          const uint4 w2 = lds128(src0 + (sp + 1) * pk_stride), w3 = lds128(src1 + (sp + 1) * pk_stride);
+          unpack_word(w0.x, o[0], o[1]);
+          unpack_word(w0.y, o[2], o[3]);
+          unpack_word(w0.z, o[4], o[5]);
+          unpack_word(w0.w, o[6], o[7]);
+          unpack_word(w1.x, o[8], o[9]);
+          unpack_word(w1.y, o[10], o[11]);
+          unpack_word(w1.z, o[12], o[13]);
+          unpack_word(w1.w, o[14], o[15]);
+          unpack_word(w2.x, o[16], o[17]);
+          unpack_word(w2.y, o[18], o[19]);
+          unpack_word(w2.z, o[20], o[21]);
+          unpack_word(w2.w, o[22], o[23]);
+          unpack_word(w3.x, o[24], o[25]);
+          unpack_word(w3.y, o[26], o[27]);
+          unpack_word(w3.z, o[28], o[29]);
+          unpack_word(w3.w, o[30], o[31]);
+          // byte lanes of each 16-word sum stay below 16 * 15 = 240
+          sum = __dp4a((((o[0] + o[1]) + (o[2] + o[3])) + ((o[4] + o[5]) + (o[6] + o[7]))) +
+                           (((o[8] + o[9]) + (o[10] + o[11])) + ((o[12] + o[13]) + (o[14] + o[15]))),
+                       0x01010101u, sum);
+          sum = __dp4a((((o[16] + o[17]) + (o[18] + o[19])) + ((o[20] + o[21]) + (o[22] + o[23]))) +
+                           (((o[24] + o[25]) + (o[26] + o[27])) + ((o[28] + o[29]) + (o[30] + o[31]))),
+                       0x01010101u, sum);
+          if (!is_a) {
+            const uint32_t d = dst_row + ss * uint32_t(B_UN), e = d + uint32_t(B_UN);
+            sts128(d + d0, o[0], o[1], o[2], o[3]);
+            sts128(d + d1, o[4], o[5], o[6], o[7]);
+            sts128(d + d2, o[8], o[9], o[10], o[11]);
+            sts128(d + d3, o[12], o[13], o[14], o[15]);
+            sts128(e + d0, o[16], o[17], o[18], o[19]);
+            sts128(e + d1, o[20], o[21], o[22], o[23]);
+            sts128(e + d2, o[24], o[25], o[26], o[27]);
+            sts128(e + d3, o[28], o[29], o[30], o[31]);
+          }
+        }
         if (is_a) {
-          uint32_t o[16];
-          sum += convert_half_regs(sm + OFF_AP + sp * A_PK + r * 64, r, part, o);
-          QUAROT_TMEM_ST16(tmem_a_row + uint32_t(32 * ss), o);
+          QUAROT_TMEM_ST16(tmem_a_row + 32u * ss, o);
+          QUAROT_TMEM_ST16(tmem_a_row + 32u * (ss + 1), (o + 16));
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           fence_before_sync();
         } else {
-          if (r < BNH)
-            sum += convert_half(sm + OFF_BP + sp * B_PK + r * 64, r, part, sm + OFF_BU + ss * B_UN + r * 128);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&full[ss]);
+          mbar_arrive(&full[ss + 1]);
           mbar_arrive(&pk_empty[sp]);
+          mbar_arrive(&pk_empty[sp + 1]);
         }
+        sp += 2;
+        if (sp == uint32_t(SP)) { sp = 0; pk_par ^= 1u; }
+        ss += 2;
+        if (ss == uint32_t(S)) { ss = 0; s_par ^= 1u; }
       }
       if (!ok) break;
       const int a = ti & 1;
       if (!is_a) sum += __shfl_xor_sync(0xffffffffu, sum, 16);  // the row's other half
       if (!wait_cluster(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
       if (is_a) {
-        rsA[(2 * a + part) * BM + r] = int(sum);
+        rsA[(2 * a + int(part)) * BM + r] = int(sum);
       } else if (part == 0 && r < BNH) {
         int* dst = rsB + a * BN_MAX + int(rank) * BNH + r;
         *dst = int(sum);
@@ -1042,8 +1109,9 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   const int sms = sm_count();
   if (sms <= 0) return QUAROT_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (M > BM && sms >= 2) {
-    // 2-SM path: clusters of two CTAs, one 256 x BN tile per pair
+  if (M > BM && sms >= 2 && (K / BK) % 2 == 0) {
+    // 2-SM path: clusters of two CTAs, one 256 x BN tile per pair (its
+    // converters take k-blocks in pairs, so K % 256 == 0)
     const int pairs = sms / 2;
     const int bn = pick_bn_pair(M, N, pairs);
     CUtensorMap ta, tb;
