@@ -504,7 +504,7 @@ constexpr int OFF_BAR = ((OFF_BP + SP * B_PK) + 1023) / 1024 * 1024;
 //           rs_full[2] rs_empty[2] drain
 constexpr int NBAR = 2 * SP + 2 * S + 2 + 4 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int OFF_RSA = OFF_MISC + 16;             // int [2][2][BM]: per half row
+constexpr int OFF_RSA = (OFF_MISC + 16 + 127) / 128 * 128;  // int [2][2][BM]: per half row
 constexpr int OFF_RSB = OFF_RSA + 4 * BM * 4;      // int [2][BN_MAX]: the whole tile's W row sums
 constexpr int OFF_SW = OFF_RSB + 2 * BN_MAX * 4;   // float [NEW][BN_MAX]: each epilogue warp's weight scales
 constexpr int SMEM_USED = OFF_SW + NEW * BN_MAX * 4;
@@ -517,6 +517,7 @@ static_assert(B_PK % 1024 == 0 && B_UN % 1024 == 0 && A_PK % 1024 == 0, "stage a
 static_assert(TMEM_A_COL + 32 * S <= TMEM_COLS && BN_MAX <= int(TMEM_A_COL), "tensor memory plan");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(SP % 2 == 0 && S % 2 == 0, "converters take stages in pairs");
+static_assert(OFF_RSB % 16 == 0 && OFF_SW % 16 == 0 && (BN_MAX * 4) % 16 == 0, "16-byte shared loads of row sums and scales");
 
 #define QUAROT_TMEM_ST16(taddr, r)                                                                 \
   asm volatile(                                                                                    \
@@ -968,34 +969,47 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
         const int gn = n0 + c0;
         if (gm < M && gn < N) {
-          float acc[32];
+          // exact integer accumulator, in place: acc = 2^18 * D - 8 * rowsum_w + bias_r
+          const uint32_t rs_addr = smem_u32(rsb + c0), sw_addr = smem_u32(sws);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(rsb[c0 + j])) + bias_r;
+          for (int j = 0; j < 32; j += 4) {
+            const uint4 r4 = lds128(rs_addr + 4u * uint32_t(j));
+            v[j] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(int(r4.x))) + bias_r);
+            v[j + 1] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j + 1]), 262144.0f), 8.0f * float(int(r4.y))) + bias_r);
+            v[j + 2] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j + 2]), 262144.0f), 8.0f * float(int(r4.z))) + bias_r);
+            v[j + 3] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j + 3]), 262144.0f), 8.0f * float(int(r4.w))) + bias_r);
+          }
           __half* yrow = y + size_t(gm) * N + gn;
           if (vec_ok && gn + 32 <= N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 16) {
               uint32_t o[8];
 #pragma unroll
-              for (int t = 0; t < 8; ++t) {
-                const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * t], sxr), sws[j + 2 * t]));
-                const __half hi =
-                    __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * t + 1], sxr), sws[j + 2 * t + 1]));
-                o[t] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+              for (int t = 0; t < 8; t += 2) {
+                const uint4 s4 = lds128(sw_addr + 4u * uint32_t(j + 2 * t));
+                const float sv[4] = {__uint_as_float(s4.x), __uint_as_float(s4.y), __uint_as_float(s4.z),
+                                     __uint_as_float(s4.w)};
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int jj = j + 2 * (t + u);
+                  const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), sxr), sv[2 * u]));
+                  const __half hi =
+                      __float2half_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj + 1]), sxr), sv[2 * u + 1]));
+                  o[t + u] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+                }
               }
               st_global_v8(yrow + j, o);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (gn + j < N) yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(acc[j], sxr), sws[j]));
+              if (gn + j < N) yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[j]), sxr), sws[j]));
           }
           if (acc_out != nullptr) {
             int32_t* arow = acc_out + size_t(gm) * N + gn;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (gn + j < N) arow[j] = __float2int_rn(acc[j]);
+              if (gn + j < N) arow[j] = __float2int_rn(__uint_as_float(v[j]));
           }
         }
       }
