@@ -266,23 +266,63 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll 1
   for (int i = 0; i < NS; ++i) issue(i);
 
-  // ---- q~ = q H / sqrt(d) (FWHT in shared memory)
-  auto qidx = [](int hh, int d) { return hh * QS + d + 4 * (d >> 5); };
-  for (int i = tid; i < G * HD; i += DT) {
-    const int hh = i / HD, e = i % HD;
-    qs[qidx(hh, e)] = __half2float(q[(int64_t(b) * Hq + g * G + hh) * HD + e]);
+  // This CTA's inputs are read only after the loop; the combine kernel may be
+  // scheduled now (it waits in griddepcontrol.wait for this grid to finish).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- q~ = q H / sqrt(d): one warp per query head; lane l holds dims
+  // 4l .. 4l+3.  Butterflies of spans 1 and 2 run in registers, spans 4 .. 64
+  // across lanes, in the stage order of a natural-order FWHT (lower index
+  // a + b, upper a - b).  Each scaled value x (odd dims divided by 16) splits
+  // into fp16 hi + lo halves; the head's score offset
+  // sum_d (hi + lo)(d) * (1032 for even d, 1152 for odd d) is a warp sum (a
+  // per-head constant, so its rounding does not change the softmax).
+  __half* qh = reinterpret_cast<__half*>(qs);                   // [G][2][HD]: hi row, lo row
+  float* qoff_s = reinterpret_cast<float*>(qh + 2 * G * HD);    // [G]
+  for (int hh = wid; hh < G; hh += NW) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(q + (int64_t(b) * Hq + g * G + hh) * HD + 4 * lane);
+    const float2 x01 = h2_to_f2(raw.x), x23 = h2_to_f2(raw.y);
+    float x[4] = {x01.x, x01.y, x23.x, x23.y};
+    float u0 = x[0], u1 = x[1];
+    x[0] = u0 + u1;
+    x[1] = u0 - u1;
+    u0 = x[2];
+    u1 = x[3];
+    x[2] = u0 + u1;
+    x[3] = u0 - u1;
+    u0 = x[0];
+    u1 = x[2];
+    x[0] = u0 + u1;
+    x[2] = u0 - u1;
+    u0 = x[1];
+    u1 = x[3];
+    x[1] = u0 + u1;
+    x[3] = u0 - u1;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const bool upper = (lane & s) != 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float other = __shfl_xor_sync(0xffffffffu, x[k], s);
+        x[k] = upper ? other - x[k] : x[k] + other;
+      }
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int dd = 4 * lane + k;
+      const float xs = x[k] * qscale * ((dd & 1) ? 0.0625f : 1.0f);
+      const __half hi = __float2half_rn(xs);
+      const __half lo = __float2half_rn(xs - __half2float(hi));
+      part += (__half2float(hi) + __half2float(lo)) * ((dd & 1) ? 1152.0f : 1032.0f);
+      qh[(2 * hh) * HD + dd] = hi;
+      qh[(2 * hh + 1) * HD + dd] = lo;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+    if (lane == 0) qoff_s[hh] = part;
   }
   __syncthreads();
-  for (int hspan = 1; hspan < HD; hspan <<= 1) {
-    for (int i = tid; i < G * HD / 2; i += DT) {
-      const int hh = i / (HD / 2), pr = i % (HD / 2);
-      const int lo = (pr / hspan) * 2 * hspan + (pr % hspan);
-      const float a = qs[qidx(hh, lo)], cc = qs[qidx(hh, lo + hspan)];
-      qs[qidx(hh, lo)] = a + cc;
-      qs[qidx(hh, lo + hspan)] = a - cc;
-    }
-    __syncthreads();
-  }
 
   // ---- B fragments of Q~^T.  Column n = lane/4 of n-tile nt is head
   // 4 nt + n/2 (hi half for even n, lo half for odd n).  Step j pairs head dims
@@ -297,43 +337,26 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 4 + (r >> 1);
-    const bool lo_part = (r & 1) != 0;
+    const int part = r & 1;  // 0: hi, 1: lo
 #pragma unroll
     for (int m4 = 0; m4 < 4; ++m4) {
-      float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (hh < G) {
-        xa = *reinterpret_cast<const float4*>(&qs[qidx(hh, 32 * c + 8 * m4)]);
-        xb = *reinterpret_cast<const float4*>(&qs[qidx(hh, 32 * c + 8 * m4 + 4)]);
-      }
-      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
       __half hv[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x = xv[e] * qscale * ((e & 1) ? 0.0625f : 1.0f);
-        const __half hi = __float2half_rn(x);
-        hv[e] = lo_part ? __float2half_rn(x - __half2float(hi)) : hi;
-      }
+      for (int e2 = 0; e2 < 8; ++e2)
+        hv[e2] = hh < G ? qh[(2 * hh + part) * HD + 32 * c + 8 * m4 + e2] : __float2half(0.f);
       qb[nt][2 * m4][0] = pack_h2(hv[0], hv[4]);
       qb[nt][2 * m4][1] = pack_h2(hv[1], hv[5]);
       qb[nt][2 * m4 + 1][0] = pack_h2(hv[2], hv[6]);
       qb[nt][2 * m4 + 1][1] = pack_h2(hv[3], hv[7]);
     }
   }
-  // per-head offset constant of the scores, from the fp16 weights actually used
+  // per-head offset constant of the scores (the head whose scores this
+  // thread holds)
   float qoff[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int hh = nt * 4 + c;  // the head whose scores this thread holds
-    float acc = 0.f;
-    if (hh < G) {
-      for (int d = 0; d < HD; ++d) {
-        const float x = qs[qidx(hh, d)] * qscale * ((d & 1) ? 0.0625f : 1.0f);
-        const __half hi = __float2half_rn(x);
-        const float lo = __half2float(__float2half_rn(x - __half2float(hi)));
-        acc += (__half2float(hi) + lo) * ((d & 1) ? 1152.0f : 1032.0f);
-      }
-    }
-    qoff[nt] = acc;
+    const int hh = nt * 4 + c;
+    qoff[nt] = hh < G ? qoff_s[hh] : 0.f;
   }
 
   float o[NT][8][4];
@@ -496,6 +519,9 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 __global__ void __launch_bounds__(HD)
 decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int splits,
                       int unrotate, __half* __restrict__ out) {
+  // launched as a programmatic dependent of the decode kernel: wait for it to
+  // complete (and its writes to be visible) before reading the workspace
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float ov[HD];
   const int bh = blockIdx.x, e = threadIdx.x;
   const int64_t base = int64_t(bh) * splits;
@@ -644,7 +670,22 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
     default: return QUAROT_ERR_UNSUPPORTED;
   }
   if (lrc != QUAROT_OK) return lrc;
-  kv::decode_combine_kernel<<<unsigned(B * Hq), kv::HD, 0, st>>>(ws_o, ws_ml, splits, unrotate_out,
-                                                                 static_cast<__half*>(out));
+  // the combine kernel is a programmatic dependent launch: it is scheduled
+  // while the decode kernel runs and waits for it in griddepcontrol.wait, so
+  // its launch latency overlaps the decode
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(B * Hq));
+  cfg.blockDim = dim3(kv::HD);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kv::decode_combine_kernel, static_cast<const float*>(ws_o),
+                         static_cast<const float*>(ws_ml), splits, unrotate_out, static_cast<__half*>(out)) !=
+      cudaSuccess)
+    return QUAROT_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
