@@ -34,6 +34,10 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 M_TOK, K_DIM, N_OUT = 2048, 12288, 4096
+# DRAM bytes (read + write) of one launch of the down_proj GEMM, from an ncu
+# capture of this bench (profiles/w4a4_gemm_pair_down_proj_2048x4096x12288.md);
+# None whenever the kernel has changed since that capture.
+GEMM_TRAFFIC_BYTES = 38_776_064  # 37.810176 MB read + 0.965888 MB written
 KV = W.CONFIGS["kv4"]
 METRIC = "W4A4 layer tokens/s"
 WORKLOAD = ("down_proj W4A4 layer 2048x12288->4096 (H12(x)H1024 rotate+quant, INT4 GEMM, fp16 out) "
@@ -364,13 +368,15 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "tokens_per_step": M_TOK, "l2": "flushed between steps (2x L2 write)",
                    "parallelism": f"replicas x{ws}", "launch": "CUDA graph per step" if graphs else "direct"},
         "roofline": {"bound": "tensor", "kernel": "w4a4_gemm", "achieved": gemm_tflops, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": GEMM_TRAFFIC_BYTES,
                      "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio)"},
         "stages": stages,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": dict(clocks.summary(), samples_in_timed_region=timed_samples),
     }
+    if rank == 0 and not args.no_extra:
+        line["other_configs"] = _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak)
     if rank == 0 and not args.no_cpu_baseline:
         import torch as _t  # noqa: F401
 
@@ -385,6 +391,53 @@ def run_ours(args):
     return 0
 
 
+def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
+    """The other measured workloads: rotate+quant of 2048 x 4096 (H_4096, HBM
+    roof) and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096,
+    12288} (tensor roof).  Same cold-L2 protocol as the stages; rank 0 only."""
+    import torch
+
+    def timed(f):
+        for _ in range(3):
+            f()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            f()
+            b.record(stream)
+        torch.cuda.synchronize()
+        q.quarot_check_error(stream)
+        return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+    res = {}
+    x, _, s = W.layer_inputs("rotq4096")
+    xt, st = torch.from_numpy(x).to(dev), torch.from_numpy(s).to(dev)
+    M, d = x.shape
+    qo = torch.empty((M, d // 2), dtype=torch.uint8, device=dev)
+    so = torch.empty((M,), dtype=torch.float16, device=dev)
+    ms = timed(lambda: q.quarot_rotate_quant(xt, st, q_out=qo, scale_out=so, stream=stream))
+    nbytes = M * d * 2 + M * d // 2 + M * 2
+    res["rotate_quant_2048x4096"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                     "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+    del xt, qo, so
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    K = 4096
+    for N in (4096, 12288):
+        wq = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g).to(dev)
+        ws_ = (torch.rand(N, generator=g) * 0.01 + 0.001).half().to(dev)
+        for M in (512, 2048, 8192):
+            aq = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, generator=g).to(dev)
+            as_ = (torch.rand(M, generator=g) * 0.1 + 0.01).half().to(dev)
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            ms = timed(lambda: q.quarot_w4a4_gemm(aq, as_, wq, ws_, y=y, stream=stream))
+            tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+            res[f"w4a4_gemm_{M}x{K}x{N}"] = {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak}
+            del aq, as_, y
+        del wq, ws_
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,6 +445,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the rotate 2048x4096 and GEMM sweep lines")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

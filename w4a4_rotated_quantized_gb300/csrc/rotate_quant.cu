@@ -238,13 +238,13 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
 // Segment kernel for the hot widths d = 4096 (m = 4, Sylvester: H4 (x) H1024)
 // and d = 12288 (m = 12, H12 (x) H1024).  Four warps own a row; warp w owns
 // segments a = w * m/4 .. of 1024 elements.
-//   round 1  lane l loads 16-byte chunks l + 32 i (i = 0..3) of its segment:
+//   pass 1  lane l loads 16-byte chunks l + 32 i (i = 0..3) of its segment:
 //            element bits {0,1,2} (within the chunk) and {8,9} (i) are local;
 //            sign flip on the fp16 bits, 32-point FWHT in registers, store to
 //            a swizzled fp32 segment in shared memory;
-//   round 2  lane l re-reads the 32 elements whose bits {0,1,2,8,9} equal l and
+//   pass 2  lane l re-reads the 32 elements whose bits {0,1,2,8,9} equal l and
 //            runs the 32-point FWHT over bits 3..7, stores back;
-//   round 3  thread t takes elements 8t .. 8t+7 of every segment, applies the
+//   pass 3  thread t takes elements 8t .. 8t+7 of every segment, applies the
 //            m-point transform across segments (H4, or Paley-12 in the form
 //            y_0 = x_0 - T, y_{j+1} = 2 (z_j + A_j) + y_0 with z = x_1..x_11,
 //            T = sum z and A_j = sum of z_{j-r} over the quadratic residues r
@@ -253,8 +253,8 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
 // Packed fp32x2 arithmetic (__fadd2_rn / __ffma2_rn) carries the butterflies.
 // Shared-memory layout: float4 slot V of a segment lives at
 // V ^ (((V >> 6) & 3) << 1) ^ ((V >> 3) & 1), which keeps the 16-byte
-// stores of round 1, the strided scalar loads of round 2 and the 16-byte loads
-// of round 3 free of bank conflicts.
+// stores of pass 1, the strided scalar loads of pass 2 and the 16-byte loads
+// of pass 3 free of bank conflicts.
 __device__ __forceinline__ int seg_swz(int V) { return V ^ (((V >> 6) & 3) << 1) ^ ((V >> 3) & 1); }
 
 __device__ __forceinline__ void bfly2(float2& a, float2& b) {
@@ -299,7 +299,7 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                : "memory");
 }
 
-// STAGED = true: persistent CTAs, one row at a time; while a row runs rounds 2
+// STAGED = true: persistent CTAs, one row at a time; while a row runs passes 2
 // and 3, the next row's fp16 data arrives in a staging buffer by a bulk
 // asynchronous copy, so the load latency of one row hides behind the
 // arithmetic of the previous one.
@@ -342,7 +342,7 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   const bool valid = row < M;
   const __half* xr = x + (valid ? row : 0) * ld_x;
 
-  // ---- round 1
+  // ---- pass 1
 #pragma unroll 1
   for (int sgi = 0; sgi < PL::SPW; ++sgi) {
     const int a = w * PL::SPW + sgi;
@@ -377,7 +377,7 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   }
   __syncwarp();
 
-  // ---- round 2: bits 3..7; element e = (lane & 7) + 8 k + 256 (lane >> 3)
+  // ---- pass 2: bits 3..7; element e = (lane & 7) + 8 k + 256 (lane >> 3)
   {
     const int lh = lane >> 3;
     const int base0 = ((lane & 7) >> 2) | (lh << 6);  // float4 slot bits 0 and 6,7
@@ -408,7 +408,7 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   }
   __syncthreads();
   if constexpr (STAGED) {
-    // every warp is past round 1: the staging buffer may take the next row
+    // every warp is past pass 1: the staging buffer may take the next row
     const int64_t next = row + row_stride;
     if (tid == 0 && next < M) {
       mbar_arrive_expect_tx(mbar, uint32_t(D) * 2u);
@@ -416,7 +416,7 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     }
   }
 
-  // ---- round 3: cross-segment transform on elements 8t .. 8t+7
+  // ---- pass 3: cross-segment transform on elements 8t .. 8t+7
   float2 v[MSEG][4];
 #pragma unroll
   for (int a = 0; a < MSEG; ++a) {
