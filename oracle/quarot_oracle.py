@@ -35,6 +35,8 @@ design notes):
     (saturating at 65504), codes = clamp(round_half_even(x~ / S_fp16), -8, 7);
   * two codes per byte, even index in the low nibble, two's complement;
   * dequant epilogue Y = fp16(fp32(fp32(acc) * sx_i) * sw_j);
+  * RMSNorm is scale-free, x / sqrt(mean(x^2) + eps), applied before the
+    rotation (they commute: the rotation preserves the row norm);
   * KV: head-wise H_128 without random signs, per-(token, head) symmetric INT4
     with an fp16 scale; decode softmax in full precision, GQA head h reads KV
     head h // (Hq / Hkv); output optionally rotated back by the same H_128.
@@ -209,6 +211,37 @@ def rotate_quant(x: np.ndarray, signs: np.ndarray | None, clip_ratio: float = 1.
     Transformation": W~ = W H^T, one scale per output row).
     """
     r = rotate(x, signs)
+    q, S = quantize_rows(r, clip_ratio)
+    return pack_int4(q), S, r
+
+
+# ---------------------------------------------------------------------------
+# Scale-free RMSNorm fused with the rotation and the quantizer ([G] "Deep Dive:
+# The End-to-End QuaRot Layer Lifecycle", part 2 "Online Activation Rotation
+# Fused into RMSNorm"; [S] "Computational Invariance and Between-Block
+# Rotation (Stage 1a)": the learned RMSNorm scale is absorbed into the next
+# weights, leaving a pure normalization)
+# ---------------------------------------------------------------------------
+def rmsnorm(x: np.ndarray, eps: float) -> np.ndarray:
+    """y = x / sqrt(mean_j x_j^2 + eps) for each row, in float64.
+
+    Scale-free: the per-feature scale is folded into the following weights,
+    so only the normalization remains.  ([S] writes it as division by the row
+    norm; the guide's form with the 1/d mean and eps differs only by the
+    constant sqrt(d), which the per-token quantizer scale absorbs.)
+    """
+    xs = np.asarray(x, dtype=np.float64)
+    return xs / np.sqrt(np.mean(xs * xs, axis=-1, keepdims=True) + eps)
+
+
+def rmsnorm_rotate_quant(x: np.ndarray, signs: np.ndarray | None, eps: float, clip_ratio: float = 1.0):
+    """RMSNorm, then the rotation, then the per-row INT4 quantizer, in that order.
+
+    Returns (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d]); the
+    rotated values are (rmsnorm(x) * s) @ H / sqrt(d), exact in float64 and
+    rounded once to fp32.
+    """
+    r = rotate(rmsnorm(x, eps), signs)
     q, S = quantize_rows(r, clip_ratio)
     return pack_int4(q), S, r
 

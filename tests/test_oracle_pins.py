@@ -223,6 +223,56 @@ def test_rmsnorm_commutation(d):
     assert np.allclose(lhs, _rmsnorm(x), rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------- fused RMSNorm + rotation + quant
+def test_rmsnorm_rotate_quant_worked_example(golden):
+    g = golden("rmsnorm_rotate_quant_worked.txt")
+    x = np.array([[float(v) for v in g["x"]]], dtype=np.float16)
+    eps = float(g["eps"][0])
+    assert np.array_equal(O.rmsnorm(x, eps)[0], np.array([float(v) for v in g["y"]]))
+    packed, S, r = O.rmsnorm_rotate_quant(x, None, eps)
+    assert np.allclose(r[0], np.array([float(v) for v in g["rotated"]]), rtol=1e-7, atol=1e-7)
+    assert float(S[0]) == float(g["scale"][0])
+    assert np.array_equal(O.unpack_int4(packed)[0], np.array([int(v) for v in g["codes"]]))
+    assert np.array_equal(packed[0], np.array([int(v) for v in g["packed"]], dtype=np.uint8))
+
+
+def test_rmsnorm_eps_inside_the_root():
+    # mean(x^2) = 1, eps = 3: 1 / sqrt(1 + 3) = 1/2 exactly
+    assert np.array_equal(O.rmsnorm(np.ones((1, 4)), 3.0), np.full((1, 4), 0.5))
+
+
+@pytest.mark.parametrize("d", [16, 4096])
+def test_rmsnorm_unit_mean_square_and_scale_invariance(d):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, d)) * rng.uniform(0.1, 100.0, (5, 1))
+    y = O.rmsnorm(x, 0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-12)
+    assert np.allclose(O.rmsnorm(7.5 * x, 0.0), y, rtol=1e-12)
+
+
+def test_rmsnorm_commutes_with_the_rotation():
+    # the pages' identity RMSNorm(X) = RMSNorm(X Q^T) Q, on the oracle's RMSNorm
+    d = 4096
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, d))
+    s = W.random_signs(d, 11)
+    H = O.hadamard(d).astype(np.float64)
+    xqt = (x @ H.T) / math.sqrt(d) * s.astype(np.float64)[None, :]
+    assert np.allclose(O.rotate_f64(O.rmsnorm(xqt, 0.0), s), O.rmsnorm(x, 0.0), rtol=1e-10, atol=1e-12)
+
+
+def test_rmsnorm_rotate_quant_zero_row_and_row_scale_freedom():
+    packed, S, r = O.rmsnorm_rotate_quant(np.zeros((1, 256), np.float16), None, 1e-6)
+    assert np.all(packed == 0) and np.all(r == 0)
+    assert float(S[0]) == float(np.float16(1e-5 / 7))
+    # a power-of-two factor on the row leaves the normalized row, hence every
+    # output, unchanged (eps = 0)
+    x, _, s = W.layer_inputs("tiny")
+    a = O.rmsnorm_rotate_quant(x, s, 0.0)
+    b = O.rmsnorm_rotate_quant((x.astype(np.float32) * 0.25).astype(np.float16), s, 0.0)
+    assert all(np.array_equal(u, v) for u, v in zip(a, b))
+
+
 # ---------------------------------------------------------------- quantizer
 def _golden_quant(g):
     x = np.array([float(v) for v in g["x"]], dtype=np.float32)
