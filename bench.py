@@ -393,8 +393,9 @@ def run_ours(args):
 
 def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     """The other measured workloads: rotate+quant of 2048 x 4096 (H_4096, HBM
-    roof) and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096,
-    12288} (tensor roof).  Same cold-L2 protocol as the stages; rank 0 only."""
+    roof), the fused RMSNorm + rotate + quant at 2048 x 4096 and 2048 x 12288,
+    and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096, 12288}
+    (tensor roof).  Same cold-L2 protocol as the stages; rank 0 only."""
     import torch
 
     def timed(f):
@@ -420,6 +421,19 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     nbytes = M * d * 2 + M * d // 2 + M * 2
     res["rotate_quant_2048x4096"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
                                      "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+    ms = timed(lambda: q.quarot_rmsnorm_rotate_quant(xt, st, eps=1e-6, q_out=qo, scale_out=so, stream=stream))
+    res["rmsnorm_rotate_quant_2048x4096"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                             "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+    del xt, qo, so
+    x, _, s = W.layer_inputs("down_proj", N=0)
+    xt, st = torch.from_numpy(x).to(dev), torch.from_numpy(s).to(dev)
+    M, d = x.shape
+    qo = torch.empty((M, d // 2), dtype=torch.uint8, device=dev)
+    so = torch.empty((M,), dtype=torch.float16, device=dev)
+    ms = timed(lambda: q.quarot_rmsnorm_rotate_quant(xt, st, eps=1e-6, q_out=qo, scale_out=so, stream=stream))
+    nbytes = M * d * 2 + M * d // 2 + M * 2
+    res["rmsnorm_rotate_quant_2048x12288"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                              "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
     del xt, qo, so
     g = torch.Generator(device="cpu").manual_seed(1234)
     K = 4096

@@ -91,6 +91,27 @@ int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, const
                         void* stream);
 
 /*
+ * quarot_rmsnorm_rotate_quant -- quarot_rotate_quant preceded by a scale-free
+ * RMSNorm of each row, fused in the same kernel.  [G] "Deep Dive: The
+ * End-to-End QuaRot Layer Lifecycle", 2 "Online Activation Rotation Fused into
+ * RMSNorm" (RMSNorm(x) = x / sqrt(mean x^2 + eps), normalize, FWHT and quantize
+ * in one kernel); [S] "Computational Invariance and Between-Block Rotation
+ * (Stage 1a)": the learned RMSNorm scale is absorbed into the next weights, so
+ * only the normalization stays online.
+ *
+ * For each row i of x:
+ *   y = x_i / sqrt(mean_j x_ij^2 + eps)            (fp32)
+ *   r = (y * s) @ H_d / sqrt(d), then S and q exactly as quarot_rotate_quant
+ * (the rotation preserves the row norm, so the sum of squares is taken from
+ * the input row).  Arguments as quarot_rotate_quant, plus:
+ *   eps       > 0 (finite); otherwise QUAROT_ERR_INVALID_ARG
+ *   rot_out   receives the normalized rotated values r, or NULL
+ */
+int quarot_rmsnorm_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, float eps,
+                                const int8_t* signs, float clip_ratio, uint8_t* q_out, void* scale_out,
+                                float* rot_out, void* stream);
+
+/*
  * quarot_w4a4_gemm -- W4A4 GEMM with INT32-exact accumulation and the
  * per-token x per-output-channel dequantization epilogue.
  * [S] Stage 2b "dequantization step", "Kernel Implementation" (INT4 GEMM,

@@ -61,6 +61,18 @@ def test_rotate_quant_validation(lib):
     assert f(FAKE, 4, 4104, 4104, None, 1.0, FAKE, FAKE, None, None) == 2  # no construction
 
 
+def test_rmsnorm_rotate_quant_validation(lib):
+    f = lib.quarot_rmsnorm_rotate_quant
+    assert f(FAKE, 0, 4096, 4096, 1e-6, None, 1.0, FAKE, FAKE, None, None) == 0  # M = 0 no-op
+    assert f(FAKE, 4, 4096, 4096, 0.0, None, 1.0, FAKE, FAKE, None, None) == 1  # eps must be > 0
+    assert f(FAKE, 4, 4096, 4096, -1.0, None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 4, 4096, 4096, float("nan"), None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 4, 4096, 4096, float("inf"), None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 4, 24, 24, 1e-6, None, 1.0, FAKE, FAKE, None, None) == 2  # no construction for 24
+    assert f(FAKE, 4, 4096, 4096, 1e-6, None, 1.5, FAKE, FAKE, None, None) == 1  # clip
+    assert f(P(0x10002), 4, 4096, 4096, 1e-6, None, 1.0, FAKE, FAKE, None, None) == 3  # misaligned x
+
+
 def test_gemm_validation(lib):
     f = lib.quarot_w4a4_gemm
     assert f(FAKE, FAKE, FAKE, FAKE, 0, 16, 256, FAKE, None, None) == 0

@@ -127,6 +127,42 @@ def test_rotate_quant_config_down_proj_sampled(q):
     check_quant(gq.cpu().numpy()[rows], gs.cpu().numpy()[rows], grot.cpu().numpy()[rows], O.rotate(x[rows], s))
 
 
+# ---------------------------------------------------------------- fused RMSNorm + rotate + quant
+@pytest.mark.parametrize("d", [16, 256, 1024, 3072, 4096, 8192, 12288])
+def test_rmsnorm_rotate_quant_widths(q, d):
+    M = 37
+    x = W.activations(M, d, W.outlier_channels(d, max(1, d // 512), 7 + d), 100.0, 13 + d)
+    s = W.random_signs(d, 23 + d)
+    gq, gs, grot = q.quarot_rmsnorm_rotate_quant(_t(x), _t(s), eps=1e-6, want_rot=True)
+    _, _, r_ref = O.rmsnorm_rotate_quant(x, s, 1e-6)
+    check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), r_ref)
+
+
+@pytest.mark.parametrize("d", [256, 4096, 12288])
+def test_rmsnorm_rotate_quant_clip_eps_edge_rows(q, d):
+    x = W.activations(9, d, [1, 5], 30.0, 41)
+    x[0] = 0.0            # zero row: eps keeps it finite, codes 0 and the floor scale
+    x[1] = 0.25           # constant row: mean square 1/16
+    x[2] *= np.float16(1e-3)  # small row: eps visible in the normalization
+    s = W.random_signs(d, 43)
+    eps = 1e-4
+    gq, gs, grot = q.quarot_rmsnorm_rotate_quant(_t(x), _t(s), eps=eps, clip_ratio=0.9, want_rot=True)
+    _, _, r_ref = O.rmsnorm_rotate_quant(x, s, eps, 0.9)
+    gq, gs, grot = gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy()
+    assert np.all(O.unpack_int4(gq)[0] == 0) and float(gs[0]) == float(np.float16(1e-5 / 7))
+    check_quant(gq, gs, grot, r_ref, clip=0.9)
+
+
+def test_rmsnorm_rotate_quant_down_proj_sampled(q):
+    """2048 x 12288: the persistent kernel takes several rows per CTA."""
+    x, _, s = W.layer_inputs("down_proj", N=0)
+    gq, gs, grot = q.quarot_rmsnorm_rotate_quant(_t(x), _t(s), eps=1e-6, want_rot=True)
+    rows = np.random.default_rng(5).choice(x.shape[0], 40, replace=False)
+    rows[:2] = [0, x.shape[0] - 1]
+    _, _, r_ref = O.rmsnorm_rotate_quant(x[rows], s, 1e-6)
+    check_quant(gq.cpu().numpy()[rows], gs.cpu().numpy()[rows], grot.cpu().numpy()[rows], r_ref)
+
+
 # ---------------------------------------------------------------- GEMM
 def _gemm_case(q, M, N, K, seed, codes_a=None, codes_w=None):
     a = W.int4_codes(M, K, seed) if codes_a is None else codes_a

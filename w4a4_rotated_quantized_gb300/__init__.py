@@ -33,6 +33,8 @@ _SIGS = {
     "quarot_version": (ctypes.c_int, []),
     "quarot_check_error": (ctypes.c_int, [_P]),
     "quarot_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "quarot_rmsnorm_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, ctypes.c_float, _P, ctypes.c_float, _P, _P,
+                                                   _P, _P]),
     "quarot_w4a4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "quarot_kv_write": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "quarot_decode_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
@@ -103,6 +105,37 @@ def quarot_check_error(stream=None, device=None) -> None:
     """Synchronizes the stream and raises if a kernel recorded a device-side error."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _check(load().quarot_check_error(_stream(stream, dev)), "quarot_check_error")
+
+
+def _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot):
+    _need(x, torch.float16, "x")
+    dev = x.device
+    M, d = x.shape
+    if signs is not None:
+        _need(signs, torch.int8, "signs", dev)
+    if q_out is None:
+        q_out = torch.empty((M, d // 2), dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float16, device=dev)
+    if rot_out is None and want_rot:
+        rot_out = torch.empty((M, d), dtype=torch.float32, device=dev)
+    _need(q_out, torch.uint8, "q_out", dev)
+    _need(scale_out, torch.float16, "scale_out", dev)
+    if rot_out is not None:
+        _need(rot_out, torch.float32, "rot_out", dev)
+    return q_out, scale_out, rot_out
+
+
+def quarot_rmsnorm_rotate_quant(x, signs=None, eps: float = 1e-6, clip_ratio: float = 1.0, q_out=None,
+                                scale_out=None, rot_out=None, stream=None, want_rot: bool = False):
+    """x: fp16 [M, d] -> RMSNorm (scale-free), rotation and INT4 quantization in
+    one kernel: (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d] or None)."""
+    q_out, scale_out, rot_out = _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot)
+    M, d = x.shape
+    st = load().quarot_rmsnorm_rotate_quant(_ptr(x), M, d, d, float(eps), _ptr(signs), float(clip_ratio),
+                                            _ptr(q_out), _ptr(scale_out), _ptr(rot_out), _stream(stream, x.device))
+    _check(st, "quarot_rmsnorm_rotate_quant")
+    return q_out, scale_out, rot_out
 
 
 def quarot_rotate_quant(x, signs=None, clip_ratio: float = 1.0, q_out=None, scale_out=None, rot_out=None,

@@ -78,15 +78,15 @@ struct RQPlan {
   static_assert(GPT * GROUP <= 64, "final pass register budget");
 };
 
-template <int LOGP, bool M12>
+template <int LOGP, bool M12, bool RMS>
 __global__ void __launch_bounds__(RQPlan<LOGP, M12>::NT)
 rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
-                    const int8_t* __restrict__ signs, float clip_ratio, uint8_t* __restrict__ q_out,
+                    const int8_t* __restrict__ signs, float clip_ratio, float rms_eps, uint8_t* __restrict__ q_out,
                     __half* __restrict__ scale_out, float* __restrict__ rot_out) {
   using PL = RQPlan<LOGP, M12>;
   constexpr int D = PL::D, P = PL::P, TPR = PL::TPR;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  float* red = reinterpret_cast<float*>(smem_raw);  // [64] cross-warp max
+  float* red = reinterpret_cast<float*>(smem_raw);  // [64]: cross-warp max [0, 32), sum of squares [32, 64)
   float* rows = reinterpret_cast<float*>(smem_raw + 64 * 4);
 
   const int tid = threadIdx.x;
@@ -97,8 +97,9 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
   float* buf = rows + r_local * PL::ROW_STRIDE;
   uint8_t* codes = reinterpret_cast<uint8_t*>(rows + PL::RPC * PL::ROW_STRIDE) + r_local * D;
 
-  // ---- 1. load pass: bits 0..2
+  // ---- 1. load pass: bits 0..2 (and the row's sum of squares for RMSNorm)
   const __half* xr = x + (valid ? row : 0) * ld_x;
+  float sq = 0.f;
   for (int c = t; c < D / 8; c += TPR) {
     float v[8];
     if (valid) {
@@ -107,6 +108,10 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
                    f3 = h2_to_f2(raw.w);
       v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
       v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
+      if constexpr (RMS) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sq = fmaf(v[i], v[i], sq);
+      }
       if (signs != nullptr) {
         const uint2 sraw = __ldg(reinterpret_cast<const uint2*>(signs + 8 * c));
         const uint32_t sw[2] = {sraw.x, sraw.y};
@@ -124,6 +129,14 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
     float4* dst = reinterpret_cast<float4*>(buf + pad_idx(8 * c));
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
     dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  constexpr int LANES = TPR < 32 ? TPR : 32;  // lanes of one row within a warp
+  if constexpr (RMS) {
+#pragma unroll
+    for (int o = LANES / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if constexpr (TPR > 32) {
+      if ((tid & 31) == 0) red[32 + (tid >> 5)] = sq;
+    }
   }
   __syncthreads();
 
@@ -173,22 +186,34 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
     }
   }
   // 1/sqrt(d): an exact power of two for even powers of two, otherwise the
-  // correctly rounded fp32 quotient.
+  // correctly rounded fp32 quotient.  With RMSNorm the row is also divided by
+  // sqrt(mean(x^2) + eps) (the rotation preserves the row norm, so the sum of
+  // squares of the input row serves).
   float inv_sqrt_d;
   if constexpr (!M12 && (LOGP % 2 == 0)) inv_sqrt_d = 1.0f / float(1 << (LOGP / 2));
   else inv_sqrt_d = 1.0f / sqrtf(float(D));
+  float post = inv_sqrt_d;
+  if constexpr (RMS) {
+    float tot = sq;
+    if constexpr (TPR > 32) {
+      constexpr int WPR = TPR / 32;
+      tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < WPR; ++w) tot += red[32 + r_local * WPR + w];
+    }
+    post = inv_sqrt_d * (1.0f / sqrtf(tot / float(D) + rms_eps));
+  }
 #pragma unroll
   for (int g = 0; g < GPT; ++g)
 #pragma unroll
     for (int a = 0; a < NA; ++a)
 #pragma unroll
       for (int j = 0; j < FJ; ++j) {
-        v[g][a][j] *= inv_sqrt_d;
+        v[g][a][j] *= post;
         amax = fmaxf(amax, fabsf(v[g][a][j]));
       }
 
   // row abs-max: lanes of the row, then warps of the row
-  constexpr int LANES = TPR < 32 ? TPR : 32;
 #pragma unroll
   for (int o = LANES / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if constexpr (TPR > 32) {
@@ -303,10 +328,10 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 // and 3, the next row's fp16 data arrives in a staging buffer by a bulk
 // asynchronous copy, so the load latency of one row hides behind the
 // arithmetic of the previous one.
-template <int MSEG, bool STAGED>
+template <int MSEG, bool STAGED, bool RMS>
 __global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT)
 rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
-                        float clip_ratio, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
+                        float clip_ratio, float rms_eps, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
                         float* __restrict__ rot_out) {
   using PL = SegPlan<MSEG, STAGED>;
   constexpr int D = PL::D;
@@ -342,7 +367,8 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   const bool valid = row < M;
   const __half* xr = x + (valid ? row : 0) * ld_x;
 
-  // ---- pass 1
+  // ---- pass 1 (and the row's sum of squares for RMSNorm)
+  float sq = 0.f;
 #pragma unroll 1
   for (int sgi = 0; sgi < PL::SPW; ++sgi) {
     const int a = w * PL::SPW + sgi;
@@ -365,6 +391,11 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
       p[4 * i + 1] = h2_to_f2(raw.y);
       p[4 * i + 2] = h2_to_f2(raw.z);
       p[4 * i + 3] = h2_to_f2(raw.w);
+      if constexpr (RMS) {
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2)
+          sq = fmaf(p[4 * i + k2].x, p[4 * i + k2].x, fmaf(p[4 * i + k2].y, p[4 * i + k2].y, sq));
+      }
     }
     fwht32_pairs(p);  // pair index n = 4 i + jj: bits 1,2 = jj, bits 3,4 = i
     float4* seg = buf + a * 256;
@@ -376,6 +407,13 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     }
   }
   __syncwarp();
+  // per-warp partial sums of squares, double-buffered by row parity (a warp
+  // can start the next row's pass 1 while another still reads this row's)
+  if constexpr (RMS) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) red[16 + (it & 1) * 8 + r_local * 4 + w] = sq;
+  }
 
   // ---- pass 2: bits 3..7; element e = (lane & 7) + 8 k + 256 (lane >> 3)
   {
@@ -470,10 +508,18 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   if (lane == 0) red[r_local * 4 + w] = amax;
   __syncthreads();
   amax = fmaxf(fmaxf(red[r_local * 4], red[r_local * 4 + 1]), fmaxf(red[r_local * 4 + 2], red[r_local * 4 + 3]));
-  // 1/sqrt(d): 1/64 for 4096; the correctly rounded quotient for 12288
+  // 1/sqrt(d): 1/64 for 4096; the correctly rounded quotient for 12288.  With
+  // RMSNorm the row is also divided by sqrt(mean(x^2) + eps) (the rotation
+  // preserves the row norm, so the input row's sum of squares serves).
   const float inv_sqrt_d = MSEG == 4 ? (1.0f / 64.0f) : 1.0f / sqrtf(float(D));
-  const __half S = quant_scale_fp16(amax * inv_sqrt_d, clip_ratio);
-  const float f = inv_sqrt_d * (1.0f / __half2float(S));
+  float post = inv_sqrt_d;
+  if constexpr (RMS) {
+    const float* rs = red + 16 + (it & 1) * 8 + r_local * 4;
+    const float tot = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+    post = inv_sqrt_d * (1.0f / sqrtf(tot / float(D) + rms_eps));
+  }
+  const __half S = quant_scale_fp16(amax * post, clip_ratio);
+  const float f = post * (1.0f / __half2float(S));
   if (valid && t == 0) scale_out[row] = S;
   if (valid) {
     uint32_t* qrow = reinterpret_cast<uint32_t*>(q_out + row * (D / 2));
@@ -502,21 +548,19 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
       __stcs(qrow + a * 128 + t, word);
       if (rot_out != nullptr) {
         float4* ro = reinterpret_cast<float4*>(rot_out + row * D + a * 1024 + 8 * t);
-        ro[0] = make_float4(v[a][0].x * inv_sqrt_d, v[a][0].y * inv_sqrt_d, v[a][1].x * inv_sqrt_d,
-                            v[a][1].y * inv_sqrt_d);
-        ro[1] = make_float4(v[a][2].x * inv_sqrt_d, v[a][2].y * inv_sqrt_d, v[a][3].x * inv_sqrt_d,
-                            v[a][3].y * inv_sqrt_d);
+        ro[0] = make_float4(v[a][0].x * post, v[a][0].y * post, v[a][1].x * post, v[a][1].y * post);
+        ro[1] = make_float4(v[a][2].x * post, v[a][2].y * post, v[a][3].x * post, v[a][3].y * post);
       }
     }
   }
   }  // row loop
 }
 
-template <int MSEG, bool STAGED>
-static int launch_seg(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, uint8_t* q,
+template <int MSEG, bool STAGED, bool RMS>
+static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps, uint8_t* q,
                       void* s, float* rot, cudaStream_t st) {
   using PL = SegPlan<MSEG, STAGED>;
-  auto kern = rotate_quant_seg_kernel<MSEG, STAGED>;
+  auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS>;
   static bool attr_set = false;
   static int per_sm = 1;
   if (!attr_set) {
@@ -537,15 +581,15 @@ static int launch_seg(const void* x, int64_t M, int64_t ld_x, const int8_t* sign
   }
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(static_cast<const __half*>(x), M, ld_x, signs, clip,
-                                                                q, static_cast<__half*>(s), rot);
+                                                                eps, q, static_cast<__half*>(s), rot);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
 
-template <int LOGP, bool M12>
-static int launch_rq(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip,
+template <int LOGP, bool M12, bool RMS>
+static int launch_rq_t(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps,
                      uint8_t* q, void* s, float* rot, cudaStream_t st) {
   using PL = RQPlan<LOGP, M12>;
-  auto kern = rotate_quant_kernel<LOGP, M12>;
+  auto kern = rotate_quant_kernel<LOGP, M12, RMS>;
   static bool attr_set = false;  // per-process; sizes are below the opt-in limit
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PL::SMEM)) !=
@@ -556,17 +600,33 @@ static int launch_rq(const void* x, int64_t M, int64_t ld_x, const int8_t* signs
   const int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(
-      static_cast<const __half*>(x), M, ld_x, signs, clip, q, static_cast<__half*>(s), rot);
+      static_cast<const __half*>(x), M, ld_x, signs, clip, eps, q, static_cast<__half*>(s), rot);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+// RMSNorm on (rms_eps >= 0) or off: separate instantiations, so the plain
+// rotation carries no sum-of-squares work.
+template <int MSEG, bool STAGED>
+static int launch_seg(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps,
+                      uint8_t* q, void* s, float* rot, cudaStream_t st) {
+  return eps >= 0.f ? launch_seg_t<MSEG, STAGED, true>(x, M, ld_x, signs, clip, eps, q, s, rot, st)
+                    : launch_seg_t<MSEG, STAGED, false>(x, M, ld_x, signs, clip, eps, q, s, rot, st);
+}
+template <int LOGP, bool M12>
+static int launch_rq(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps,
+                     uint8_t* q, void* s, float* rot, cudaStream_t st) {
+  return eps >= 0.f ? launch_rq_t<LOGP, M12, true>(x, M, ld_x, signs, clip, eps, q, s, rot, st)
+                    : launch_rq_t<LOGP, M12, false>(x, M, ld_x, signs, clip, eps, q, s, rot, st);
 }
 
 }  // namespace quarot
 
 using namespace quarot;
 
-extern "C" int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x,
-                                   const int8_t* signs, float clip_ratio, uint8_t* q_out,
-                                   void* scale_out, float* rot_out, void* stream) {
+// Shared by both entry points: rms_eps < 0 disables the RMSNorm.
+static int rotate_quant_dispatch(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                                 float clip_ratio, float rms_eps, uint8_t* q_out, void* scale_out, float* rot_out,
+                                 void* stream) {
   if (M < 0 || d <= 0 || ld_x < d) return QUAROT_ERR_INVALID_ARG;
   if (!(clip_ratio > 0.f && clip_ratio <= 1.f)) return QUAROT_ERR_INVALID_ARG;
   if (M == 0) return QUAROT_OK;
@@ -576,20 +636,34 @@ extern "C" int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t 
       (rot_out && (reinterpret_cast<uintptr_t>(rot_out) & 15)))
     return QUAROT_ERR_ALIGNMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float e = rms_eps;
   switch (d) {
-    case 16: return launch_rq<4, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 32: return launch_rq<5, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 64: return launch_rq<6, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 128: return launch_rq<7, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 256: return launch_rq<8, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 512: return launch_rq<9, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 1024: return launch_rq<10, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 2048: return launch_rq<11, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 4096: return launch_seg<4, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 8192: return launch_rq<13, false>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 3072: return launch_rq<8, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 6144: return launch_rq<9, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
-    case 12288: return launch_seg<12, true>(x, M, ld_x, signs, clip_ratio, q_out, scale_out, rot_out, st);
+    case 16: return launch_rq<4, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 32: return launch_rq<5, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 64: return launch_rq<6, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 128: return launch_rq<7, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 256: return launch_rq<8, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 512: return launch_rq<9, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 1024: return launch_rq<10, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 2048: return launch_rq<11, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 4096: return launch_seg<4, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 8192: return launch_rq<13, false>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 3072: return launch_rq<8, true>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 6144: return launch_rq<9, true>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
+    case 12288: return launch_seg<12, true>(x, M, ld_x, signs, clip_ratio, e, q_out, scale_out, rot_out, st);
     default: return QUAROT_ERR_UNSUPPORTED;
   }
+}
+
+extern "C" int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x,
+                                   const int8_t* signs, float clip_ratio, uint8_t* q_out,
+                                   void* scale_out, float* rot_out, void* stream) {
+  return rotate_quant_dispatch(x, M, d, ld_x, signs, clip_ratio, -1.0f, q_out, scale_out, rot_out, stream);
+}
+
+extern "C" int quarot_rmsnorm_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, float eps,
+                                           const int8_t* signs, float clip_ratio, uint8_t* q_out, void* scale_out,
+                                           float* rot_out, void* stream) {
+  if (!(eps > 0.f && eps < 1e30f)) return QUAROT_ERR_INVALID_ARG;
+  return rotate_quant_dispatch(x, M, d, ld_x, signs, clip_ratio, eps, q_out, scale_out, rot_out, stream);
 }
