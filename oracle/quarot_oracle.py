@@ -37,6 +37,9 @@ design notes):
   * dequant epilogue Y = fp16(fp32(fp32(acc) * sx_i) * sw_j);
   * RMSNorm is scale-free, x / sqrt(mean(x^2) + eps), applied before the
     rotation (they commute: the rotation preserves the row norm);
+  * asymmetric KV mode: a = 0.95 * (min, max) of the group, s = fp16(range / 15),
+    integer zero point z = rne(a_min / s) stored as int16, q = clamp(rne(x/s) - z,
+    0, 15), x^ = s (q + z);
   * KV: head-wise H_128 without random signs, per-(token, head) symmetric INT4
     with an fp16 scale; decode softmax in full precision, GQA head h reads KV
     head h // (Hq / Hkv); output optionally rotated back by the same H_128.
@@ -329,6 +332,103 @@ def decode_attn(q, k_cache, k_scale, v_cache, v_scale, T: int, sm_scale: float |
             vd = unpack_int4(v_cache[b, g, :T]).astype(np.float64) * v_scale[b, g, :T].astype(np.float64)[:, None]
             qs = qr[b, g * grp:(g + 1) * grp]  # [grp, d]
             s = scale * (qs @ kd.T)  # [grp, T]
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p /= p.sum(axis=1, keepdims=True)
+            out[b, g * grp:(g + 1) * grp] = p @ vd
+    if unrotate:
+        out = rotate_f64(out, None)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Asymmetric per-group KV quantizer ([S] Stage 2c "KV Cache Quantization --
+# online, per-group asymmetric": group size 128, i.e. one group per (token,
+# head) at head_dim 128; scale s = (a_max - a_min) / (2^b - 1); zero point
+# z = round(a_min / s); a_min, a_max from a clipping ratio of 0.95; dequantize
+# on the fly).  The page mixes units (z subtracted from v, "s v^ + z"); the
+# reading here keeps z on the code grid: q = clamp(rne(x / s) - z, 0, 15),
+# x^ = s (q + z).
+# ---------------------------------------------------------------------------
+ZP_MIN, ZP_MAX = -32768, 32767  # zero points are stored as int16
+
+
+def quantize_asym_rows(xr: np.ndarray, clip_ratio: float = 0.95):
+    """Per-row asymmetric 4-bit quantizer.
+
+    a_max = clip * max_j x_j, a_min = clip * min_j x_j;
+    s = fp16(min(max(a_max - a_min, 1e-5) / 15, 65504)) (quantization uses the
+    stored fp16 value); z = clamp(rne(a_min / s), int16 range);
+    q_j = clamp(rne(x_j / s) - z, 0, 15).
+    Returns (codes uint8 [..., d], scale fp16 [...], zero int16 [...]).
+    """
+    x = np.asarray(xr, dtype=np.float32).astype(np.float64)
+    a_max = clip_ratio * x.max(axis=-1)
+    a_min = clip_ratio * x.min(axis=-1)
+    s = np.minimum(np.maximum(a_max - a_min, SCALE_FLOOR) / 15.0, FP16_MAX).astype(np.float16)
+    sf = s.astype(np.float64)
+    z = np.clip(round_half_even(a_min / sf), ZP_MIN, ZP_MAX)
+    q = np.clip(round_half_even(x / sf[..., None]) - z[..., None], 0, 15)
+    return q.astype(np.uint8), s, z.astype(np.int16)
+
+
+def unpack_uint4(packed: np.ndarray) -> np.ndarray:
+    """Unsigned nibbles (0..15), even index in the low nibble: uint8 [..., 2 * nbytes]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0x0F
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def dequant_asym(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """x^ = s (q + z), float64."""
+    return scale.astype(np.float64)[..., None] * (codes.astype(np.float64) + zero.astype(np.float64)[..., None])
+
+
+def kv_quant_asym(kv: np.ndarray, clip_ratio: float = 0.95):
+    """Head-wise rotation x~ = x @ H_d / sqrt(d) (no signs), then the asymmetric
+    quantizer per (token, head).  kv: fp16 [B, T, Hkv, d] ->
+    (packed [B, Hkv, T, d/2], scale fp16 [B, Hkv, T], zero int16 [B, Hkv, T])."""
+    r = rotate(np.asarray(kv), None)
+    q, s, z = quantize_asym_rows(r, clip_ratio)
+    packed = pack_int4(q.astype(np.int16))  # unsigned nibbles pack like two's complement ones
+    tr = (0, 2, 1, 3)
+    return (np.ascontiguousarray(packed.transpose(tr)), np.ascontiguousarray(s.transpose(0, 2, 1)),
+            np.ascontiguousarray(z.transpose(0, 2, 1)))
+
+
+def kv_write_asym(k, v, t_start, k_cache, k_scale, k_zero, v_cache, v_scale, v_zero, clip_ratio: float = 0.95):
+    """Append with the asymmetric quantizer: positions t_start .. t_start + T_new - 1."""
+    T_new = np.asarray(k).shape[1]
+    sl = slice(t_start, t_start + T_new)
+    kq, ks, kz = kv_quant_asym(k, clip_ratio)
+    vq, vs, vz = kv_quant_asym(v, clip_ratio)
+    k_cache[:, :, sl, :], k_scale[:, :, sl], k_zero[:, :, sl] = kq, ks, kz
+    v_cache[:, :, sl, :], v_scale[:, :, sl], v_zero[:, :, sl] = vq, vs, vz
+
+
+def decode_attn_asym(q, k_cache, k_scale, k_zero, v_cache, v_scale, v_zero, T: int,
+                     sm_scale: float | None = None, unrotate: bool = False) -> np.ndarray:
+    """decode_attn over the asymmetric cache: k^_t = Ks[t] (kcodes_t + Kz[t]),
+    v^_t = Vs[t] (vcodes_t + Vz[t]); everything else as decode_attn.  float64 [B, Hq, d]."""
+    q = np.asarray(q)
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    grp = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if sm_scale is None or sm_scale <= 0 else float(sm_scale)
+    qr = rotate_f64(q, None)
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    if T == 0:
+        return out
+    for b in range(B):
+        for g in range(Hkv):
+            kd = dequant_asym(unpack_uint4(k_cache[b, g, :T]), k_scale[b, g, :T], k_zero[b, g, :T])
+            vd = dequant_asym(unpack_uint4(v_cache[b, g, :T]), v_scale[b, g, :T], v_zero[b, g, :T])
+            qs = qr[b, g * grp:(g + 1) * grp]
+            s = scale * (qs @ kd.T)
             s = s - s.max(axis=1, keepdims=True)
             p = np.exp(s)
             p /= p.sum(axis=1, keepdims=True)

@@ -453,6 +453,83 @@ def test_decode_brute_force_tiny():
         assert np.allclose(out[0, h], o_un, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- asymmetric KV quantizer (next row f1)
+@pytest.mark.parametrize("ex", ["A", "B"])
+def test_kv_asym_quantizer_worked_examples(golden, ex):
+    g = golden("kv_asym_quant_worked.txt")
+    x = np.array([[float(v) for v in g[f"{ex}_x"]]], dtype=np.float32)
+    q, s, z = O.quantize_asym_rows(x, float(g[f"{ex}_clip"][0]))
+    assert float(s[0]) == float(g[f"{ex}_scale"][0])
+    assert int(z[0]) == int(g[f"{ex}_zero"][0])
+    assert np.array_equal(q[0], np.array([int(v) for v in g[f"{ex}_codes"]]))
+
+
+def test_kv_asym_quantizer_invariants():
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal((200, 128)) * rng.uniform(0.01, 50.0, (200, 1))
+         + rng.uniform(-20.0, 20.0, (200, 1))).astype(np.float32)
+    q, s, z = O.quantize_asym_rows(x, 1.0)
+    assert q.min() >= 0 and q.max() <= 15
+    # the grid s (z + 0 .. 15) starts within s/2 of the row min and ends within
+    # s/2 of the row max (plus the fp16 rounding of s): error at most one step
+    err = np.abs(O.dequant_asym(q, s, z) - x.astype(np.float64))
+    assert np.all(err <= 1.01 * s.astype(np.float64)[:, None])
+    # codes are monotone in the input, and the row min / max sit at the grid ends
+    order = np.argsort(x, axis=1)
+    assert np.all(np.diff(np.take_along_axis(q.astype(int), order, axis=1), axis=1) >= 0)
+    assert np.all(q.min(axis=1) == 0) and np.all(q.max(axis=1) >= 14)
+
+
+def test_kv_asym_zero_row_and_unsigned_nibbles():
+    q, s, z = O.quantize_asym_rows(np.zeros((1, 128), np.float32))
+    assert np.all(q == 0) and int(z[0]) == 0
+    assert float(s[0]) == float(np.float16(1e-5 / 15))
+    allc = np.array(np.meshgrid(np.arange(16), np.arange(16))).reshape(2, -1).T
+    assert np.array_equal(O.unpack_uint4(O.pack_int4(allc)), allc.astype(np.uint8))
+    assert O.pack_int4(np.array([[15, 0]]))[0, 0] == 0x0F and O.pack_int4(np.array([[0, 15]]))[0, 0] == 0xF0
+
+
+def _asym_cache(B, Hkv, T, d, seed):
+    rng = np.random.default_rng(seed)
+    c = [rng.integers(0, 256, (B, Hkv, T, d // 2), dtype=np.uint8) for _ in range(2)]
+    s = [rng.uniform(0.05, 0.4, (B, Hkv, T)).astype(np.float16) for _ in range(2)]
+    z = [rng.integers(-12, 4, (B, Hkv, T)).astype(np.int16) for _ in range(2)]
+    return c[0], s[0], z[0], c[1], s[1], z[1]
+
+
+def test_decode_asym_single_token_and_identical_keys():
+    B, Hkv, Hq, d = 2, 2, 4, 128
+    kc, ks, kz, vc, vs, vz = _asym_cache(B, Hkv, 5, d, 8)
+    q = np.random.default_rng(9).standard_normal((B, Hq, d)).astype(np.float16)
+    out = O.decode_attn_asym(q, kc, ks, kz, vc, vs, vz, T=1)
+    v0 = O.dequant_asym(O.unpack_uint4(vc[:, :, 0]), vs[:, :, 0], vz[:, :, 0])  # [B, Hkv, d]
+    assert np.allclose(out, np.repeat(v0, Hq // Hkv, axis=1), rtol=1e-12, atol=1e-12)
+    kc[:, :, 1:5], ks[:, :, 1:5], kz[:, :, 1:5] = kc[:, :, :1], ks[:, :, :1], kz[:, :, :1]
+    out = O.decode_attn_asym(q, kc, ks, kz, vc, vs, vz, T=5)
+    vm = O.dequant_asym(O.unpack_uint4(vc[:, :, :5]), vs[:, :, :5], vz[:, :, :5]).mean(axis=2)
+    assert np.allclose(out, np.repeat(vm, Hq // Hkv, axis=1), rtol=1e-10, atol=1e-12)
+
+
+def test_decode_asym_brute_force_tiny():
+    # B=1, Hq=2, Hkv=1, d=4, T=3, written with explicit loops and math.exp
+    d, T = 4, 3
+    kc, ks, kz, vc, vs, vz = _asym_cache(1, 1, T, d, 10)
+    q = np.random.default_rng(11).standard_normal((1, 2, d)).astype(np.float16)
+    out = O.decode_attn_asym(q, kc, ks, kz, vc, vs, vz, T=T)
+    H4 = [[_sylvester_entry(i, j) for j in range(d)] for i in range(d)]
+    kcode = [[(int(kc[0, 0, t, j // 2]) >> (4 * (j % 2))) & 15 for j in range(d)] for t in range(T)]
+    vcode = [[(int(vc[0, 0, t, j // 2]) >> (4 * (j % 2))) & 15 for j in range(d)] for t in range(T)]
+    for h in range(2):
+        qr = [sum(float(q[0, h, i]) * H4[i][j] for i in range(d)) / 2.0 for j in range(d)]
+        s = [sum(qr[j] * float(ks[0, 0, t]) * (kcode[t][j] + int(kz[0, 0, t])) for j in range(d)) / 2.0
+             for t in range(T)]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        p = [x / sum(e) for x in e]
+        o = [sum(p[t] * float(vs[0, 0, t]) * (vcode[t][j] + int(vz[0, 0, t])) for t in range(T)) for j in range(d)]
+        assert np.allclose(out[0, h], o, rtol=1e-12, atol=1e-12)
+
+
 def test_decode_unrotated_close_to_float_attention():
     # informational sanity bound: INT4 KV attention stays near fp64 attention
     k, v, q = W.kv_inputs(B=1, T=64)
