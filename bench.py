@@ -394,7 +394,7 @@ def run_ours(args):
 def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     """The other measured workloads: rotate+quant of 2048 x 4096 (H_4096, HBM
     roof), the fused RMSNorm + rotate + quant at 2048 x 4096 and 2048 x 12288,
-    and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096, 12288}
+    decode over the asymmetric KV cache at the kv4 size, and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096, 12288}
     (tensor roof).  Same cold-L2 protocol as the stages; rank 0 only."""
     import torch
 
@@ -435,6 +435,20 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     res["rmsnorm_rotate_quant_2048x12288"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
                                               "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
     del xt, qo, so
+    # asymmetric KV cache (group 128, zero point, clip 0.95): decode at the kv4 size
+    k, v, qq = W.kv_inputs("kv4")
+    B, T, Hkv, d = k.shape
+    Hq = qq.shape[1]
+    ac = q.new_kv_cache_asym(B, Hkv, T, d, dev)
+    q.quarot_kv_write_asym(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), 0, *ac, stream=stream)
+    qd = torch.from_numpy(qq).to(dev)
+    od = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    wsd = torch.empty((q.quarot_decode_workspace_bytes(B, Hq, d, T),), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: q.quarot_decode_attn_asym(qd, *ac, T=T, out=od, workspace=wsd, stream=stream))
+    nbytes = B * Hkv * T * (d // 2) * 2 + B * Hkv * T * (2 + 2) * 2 + B * Hq * d * 2 * 2
+    res["decode_attn_asym_kv4"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                   "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+    del ac, qd, od, wsd
     g = torch.Generator(device="cpu").manual_seed(1234)
     K = 4096
     for N in (4096, 12288):

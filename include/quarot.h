@@ -186,6 +186,43 @@ int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const
                        size_t ws_bytes, void* stream);
 
 /*
+ * quarot_kv_write_asym -- quarot_kv_write with the pages' own KV quantizer:
+ * asymmetric per group of 128 with a zero point and a clipping ratio.
+ * [S] Stage 2c "KV Cache Quantization (online, per-group asymmetric)": group
+ * size 128 = one group per (token, head) vector at d = 128; s = (a_max -
+ * a_min) / (2^4 - 1); z = round(a_min / s); a_min, a_max from a clipping ratio
+ * (0.95 in the pages).  The page's formula mixes units; this library keeps
+ * the zero point on the code grid:
+ *   a = clip * (min, max) of the rotated vector,
+ *   s = fp16(min(max(a_max - a_min, 1e-5) / 15, 65504)),
+ *   z = clamp(rne(a_min / s), -32768, 32767),
+ *   q = clamp(rne(x / s) - z, 0, 15), and x^ = s (q + z) on read.
+ * The rotation is the head-wise H_d / sqrt(d) of quarot_kv_write.
+ *
+ *   k, v, B, T_new, Hkv, d, t_start, T_max   as quarot_kv_write
+ *   clip_ratio  in (0, 1]
+ *   k_q, v_q  uint8 [B, Hkv, T_max, d/2] unsigned codes (even dim in the low nibble)
+ *   k_s, v_s  fp16 [B, Hkv, T_max] scales
+ *   k_z, v_z  int16 [B, Hkv, T_max] zero points (2-byte aligned; 16-byte
+ *             aligned with T_max % 8 == 0 for the decode's bulk-copy path)
+ */
+int quarot_kv_write_asym(const void* k, const void* v, int64_t B, int64_t T_new, int64_t Hkv, int64_t d,
+                         int64_t t_start, int64_t T_max, float clip_ratio, uint8_t* k_q, void* k_s, int16_t* k_z,
+                         uint8_t* v_q, void* v_s, int16_t* v_z, void* stream);
+
+/*
+ * quarot_decode_attn_asym -- quarot_decode_attn over caches written by
+ * quarot_kv_write_asym: k^_t = k_s[t] (kcode_t + k_z[t]), v^_t likewise,
+ * dequantized on read ([S] Stage 2c "Dequantizes each group on-the-fly").
+ * Arguments as quarot_decode_attn plus the zero-point arrays; the same
+ * workspace size (quarot_decode_workspace_bytes).
+ */
+int quarot_decode_attn_asym(const void* q, const uint8_t* k_q, const void* k_s, const int16_t* k_z,
+                            const uint8_t* v_q, const void* v_s, const int16_t* v_z, int64_t B, int64_t Hq,
+                            int64_t Hkv, int64_t d, int64_t T, int64_t T_max, float sm_scale, int unrotate_out,
+                            void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * quarot_decode_attn_static -- quarot_decode_attn for callers that cannot
  * allocate device memory when they run decode (a plain C host without an
  * allocator, a serving loop that forbids cudaMalloc/cudaFree after start-up

@@ -95,6 +95,25 @@ def test_kv_validation(lib):
     assert d(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 4, 8, 0.0, 0, FAKE, FAKE, 16, None) == 1  # small ws
 
 
+def test_kv_asym_validation(lib):
+    w = lib.quarot_kv_write_asym
+    assert w(FAKE, FAKE, 0, 1, 8, 128, 0, 16, 0.95, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 0  # B = 0
+    assert w(FAKE, FAKE, 1, 1, 8, 128, 0, 16, 0.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1  # clip
+    assert w(FAKE, FAKE, 1, 1, 8, 128, 0, 16, 1.5, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert w(FAKE, FAKE, 1, 1, 8, 96, 0, 16, 0.95, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 2  # d
+    assert w(FAKE, FAKE, 1, 1, 8, 128, 0, 16, 0.95, FAKE, FAKE, None, FAKE, FAKE, FAKE, None) == 1  # no k_z
+    assert w(FAKE, FAKE, 1, 1, 8, 128, 0, 16, 0.95, FAKE, FAKE, P(0x10001), FAKE, FAKE, FAKE, None) == 3
+    assert w(FAKE, FAKE, 1, 4, 8, 128, 14, 16, 0.95, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1  # overflow
+    a = lib.quarot_decode_attn_asym
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 32, 8, 128, 16, 16, 0.0, 0, FAKE, FAKE, 0, None) == 0
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 64, 16, 16, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 2
+    assert a(FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 0, FAKE, FAKE, 1 << 20,
+             None) == 1  # no k_z
+    assert a(FAKE, FAKE, FAKE, P(0x10001), FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 0, FAKE, P(0x10000),
+             1 << 20, None) == 3  # misaligned k_z
+    assert a(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 30, 8, 128, 16, 16, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 1
+
+
 def test_workspace_size(lib):
     assert q.quarot_decode_workspace_bytes(16, 32, 128, 4096) == 16 * 32 * 16 * 130 * 4
     assert q.quarot_decode_workspace_bytes(1, 1, 128, 1) == 768  # 130 floats rounded up to 256 B

@@ -295,3 +295,80 @@ def test_kv4_config_full(q):
             assert np.all(np.abs(g.astype(np.float64) - o.astype(np.float64)) <= _fp16_ulp(o)), name
         ref = O.decode_attn(qq[b:b + 1], *oc, T=T)
         assert O.rel_fro(out[b:b + 1], ref) <= OUT_TOL
+
+
+# ---------------------------------------------------------------- asymmetric KV (next row f1)
+def _caches_asym(shape_like, T_max):
+    B, _, H, d = shape_like
+    c = [np.zeros((B, H, T_max, d // 2), np.uint8), np.zeros((B, H, T_max), np.float16),
+         np.zeros((B, H, T_max), np.int16)]
+    return c + [x.copy() for x in c]
+
+
+def _check_asym_vectors(r, clip, codes, scales, zeros):
+    """GPU (codes, scale, zero) of rotated vectors r against the oracle quantizer."""
+    q_ref, s_ref, z_ref = O.quantize_asym_rows(r, clip)
+    assert np.all(np.abs(scales.astype(np.float64) - s_ref.astype(np.float64)) <= _fp16_ulp(s_ref))
+    same = (scales == s_ref)
+    sf = s_ref.astype(np.float64)
+    a_min = clip * r.astype(np.float64).min(axis=-1)
+    zb = np.abs(np.abs(a_min / sf - np.floor(a_min / sf)) - 0.5) < 1e-4  # z on a rounding boundary
+    dz = np.abs(zeros.astype(np.int64) - z_ref.astype(np.int64))
+    assert np.all(dz[same] <= zb[same].astype(np.int64)), "zero points differ away from a boundary"
+    ok = same & (zeros == z_ref)
+    y = r.astype(np.float64) / sf[..., None]
+    near = np.abs(np.abs(y - np.floor(y)) - 0.5) < 1e-4
+    bad = (codes != q_ref) & ~near & ok[..., None]
+    assert not bad.any(), f"{int(bad.sum())} codes differ away from a rounding boundary"
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_kv_write_asym_parity(q, d):
+    B, T, H, T_max, t0, clip = 3, 37, 2, 64, 5, 0.95
+    k = W.kv_tensors(B, T, H, d, 2, 20.0, 51)
+    v = W.kv_tensors(B, T, H, d, 2, 20.0, 52)
+    gc = q.new_kv_cache_asym(B, H, T_max, d, DEV)
+    q.quarot_kv_write_asym(_t(k), _t(v), t0, *gc, clip_ratio=clip)
+    gk, gks, gkz, gv, gvs, gvz = [t.cpu().numpy() for t in gc]
+    for src, codes, scales, zeros in ((k, gk, gks, gkz), (v, gv, gvs, gvz)):
+        r = O.rotate(src, None)  # [B, T, H, d]
+        _check_asym_vectors(r, clip, O.unpack_uint4(codes[:, :, t0:t0 + T].transpose(0, 2, 1, 3)),
+                            scales[:, :, t0:t0 + T].transpose(0, 2, 1), zeros[:, :, t0:t0 + T].transpose(0, 2, 1))
+        assert np.all(codes[:, :, :t0] == 0) and np.all(codes[:, :, t0 + T:] == 0)
+        assert np.all(zeros[:, :, :t0] == 0) and np.all(zeros[:, :, t0 + T:] == 0)
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("T", [1, 17, 300, 1000])
+def test_decode_asym_parity(q, G, T):
+    B, Hkv, d, T_max = 2, 2, 128, 1024
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 61 + T)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 62 + T)
+    qq = W.query(B, Hkv * G, d, 63 + T)
+    oc = _caches_asym(k.shape, T_max)
+    O.kv_write_asym(k, v, 0, *oc)
+    for unrot in (False, True):
+        out = q.quarot_decode_attn_asym(_t(qq), *[_t(c) for c in oc], T=T, unrotate_out=unrot)
+        ref = O.decode_attn_asym(qq, *oc, T=T, unrotate=unrot)
+        assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+
+
+def test_kv4_config_full_asym(q):
+    """B16 x T4096 x Hkv8 x Hq32 with the asymmetric cache: append and decode at
+    full size; oracle on two sequences."""
+    k, v, qq = W.kv_inputs("kv4")
+    B, T, Hkv, d = k.shape
+    gc = q.new_kv_cache_asym(B, Hkv, T, d, DEV)
+    q.quarot_kv_write_asym(_t(k), _t(v), 0, *gc)
+    out = q.quarot_decode_attn_asym(_t(qq), *gc, T=T)
+    q.quarot_check_error()
+    out = out.cpu().numpy()
+    gnp = [t.cpu().numpy() for t in gc]
+    for b in (0, B - 1):
+        oc = _caches_asym(k[b:b + 1].shape, T)
+        O.kv_write_asym(k[b:b + 1], v[b:b + 1], 0, *oc)
+        for i, name in ((1, "k_s"), (4, "v_s")):
+            g_, o_ = gnp[i][b], oc[i][0]
+            assert np.all(np.abs(g_.astype(np.float64) - o_.astype(np.float64)) <= _fp16_ulp(o_)), name
+        ref = O.decode_attn_asym(qq[b:b + 1], *oc, T=T)
+        assert O.rel_fro(out[b:b + 1], ref) <= OUT_TOL

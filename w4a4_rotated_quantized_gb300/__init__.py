@@ -42,6 +42,10 @@ _SIGS = {
                                           ctypes.c_float, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
     "quarot_decode_attn_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                                  ctypes.c_float, ctypes.c_int, _P, _P]),
+    "quarot_kv_write_asym": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P,
+                                            _P, _P, _P, _P]),
+    "quarot_decode_attn_asym": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                               ctypes.c_float, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
 }
 DECODE_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024  # QUAROT_DECODE_STATIC_SCRATCH_BYTES
 EXPORTED = tuple(_SIGS)
@@ -263,3 +267,60 @@ def new_kv_cache(B: int, Hkv: int, T_max: int, d: int, device):
     ks = torch.zeros((B, Hkv, T_max), dtype=torch.float16, device=device)
     vs = torch.zeros_like(ks)
     return kq, ks, vq, vs
+
+
+def new_kv_cache_asym(B: int, Hkv: int, T_max: int, d: int, device):
+    """Zeroed asymmetric caches (k_q, k_s, k_z, v_q, v_s, v_z): unsigned codes,
+    fp16 scales, int16 zero points, in the layout quarot_kv_write_asym expects."""
+    kq = torch.zeros((B, Hkv, T_max, d // 2), dtype=torch.uint8, device=device)
+    ks = torch.zeros((B, Hkv, T_max), dtype=torch.float16, device=device)
+    kz = torch.zeros((B, Hkv, T_max), dtype=torch.int16, device=device)
+    return kq, ks, kz, torch.zeros_like(kq), torch.zeros_like(ks), torch.zeros_like(kz)
+
+
+def quarot_kv_write_asym(k, v, t_start, k_q, k_s, k_z, v_q, v_s, v_z, clip_ratio: float = 0.95, stream=None):
+    """Append with the asymmetric per-group quantizer (group = head vector)."""
+    _need(k, torch.float16, "k")
+    dev = k.device
+    _need(v, torch.float16, "v", dev)
+    for t_, n in ((k_q, "k_q"), (v_q, "v_q")):
+        _need(t_, torch.uint8, n, dev)
+    for t_, n in ((k_s, "k_s"), (v_s, "v_s")):
+        _need(t_, torch.float16, n, dev)
+    for t_, n in ((k_z, "k_z"), (v_z, "v_z")):
+        _need(t_, torch.int16, n, dev)
+    B, T_new, Hkv, d = k.shape
+    if tuple(v.shape) != tuple(k.shape):
+        raise QuarotError(1, "k and v shapes differ")
+    T_max = k_q.shape[2]
+    st = load().quarot_kv_write_asym(_ptr(k), _ptr(v), B, T_new, Hkv, d, int(t_start), T_max, float(clip_ratio),
+                                     _ptr(k_q), _ptr(k_s), _ptr(k_z), _ptr(v_q), _ptr(v_s), _ptr(v_z),
+                                     _stream(stream, dev))
+    _check(st, "quarot_kv_write_asym")
+
+
+def quarot_decode_attn_asym(q, k_q, k_s, k_z, v_q, v_s, v_z, T: int, sm_scale: float = 0.0,
+                            unrotate_out: bool = False, out=None, workspace=None, stream=None):
+    """quarot_decode_attn over the asymmetric cache -> out fp16 [B, Hq, d]."""
+    _need(q, torch.float16, "q")
+    dev = q.device
+    for t_, n in ((k_q, "k_q"), (v_q, "v_q")):
+        _need(t_, torch.uint8, n, dev)
+    for t_, n in ((k_s, "k_s"), (v_s, "v_s")):
+        _need(t_, torch.float16, n, dev)
+    for t_, n in ((k_z, "k_z"), (v_z, "v_z")):
+        _need(t_, torch.int16, n, dev)
+    B, Hq, d = q.shape
+    Hkv, T_max = k_q.shape[1], k_q.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float16, device=dev)
+    _need(out, torch.float16, "out", dev)
+    need = quarot_decode_workspace_bytes(B, Hq, d, T)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    st = load().quarot_decode_attn_asym(_ptr(q), _ptr(k_q), _ptr(k_s), _ptr(k_z), _ptr(v_q), _ptr(v_s), _ptr(v_z),
+                                        B, Hq, Hkv, d, int(T), T_max, float(sm_scale), int(bool(unrotate_out)),
+                                        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream, dev))
+    _check(st, "quarot_decode_attn_asym")
+    return out

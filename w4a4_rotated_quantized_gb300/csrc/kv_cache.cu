@@ -38,16 +38,22 @@ __device__ __forceinline__ void fwht32(float* v) {
       }
 }
 
-template <int D>
+// ASYM selects the asymmetric quantizer ([S] Stage 2c, per-group asymmetric
+// with group = the head vector): a = clip * (min, max), s = fp16(range / 15),
+// integer zero point z = rne(a_min / s) (int16), codes q = clamp(rne(x / s) - z,
+// 0, 15) stored as unsigned nibbles; x^ = s (q + z).
+template <int D, bool ASYM>
 __global__ void __launch_bounds__(256)
 kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_src, int64_t B, int64_t T_new,
                 int64_t Hkv, int64_t t_start, int64_t T_max, uint8_t* __restrict__ k_q, __half* __restrict__ k_s,
-                uint8_t* __restrict__ v_q, __half* __restrict__ v_s) {
+                uint8_t* __restrict__ v_q, __half* __restrict__ v_s, int16_t* __restrict__ k_z,
+                int16_t* __restrict__ v_z, float clip_ratio) {
   constexpr int TPV = D / 32;
   // blockIdx.y selects the tensor: 0 = keys, 1 = values
   const __half* __restrict__ src = blockIdx.y == 0 ? k_src : v_src;
   uint8_t* __restrict__ cq = blockIdx.y == 0 ? k_q : v_q;
   __half* __restrict__ cs = blockIdx.y == 0 ? k_s : v_s;
+  int16_t* __restrict__ cz = blockIdx.y == 0 ? k_z : v_z;
   const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nvec = B * Hkv * T_new;
   const int64_t vi = gt / TPV;
@@ -82,26 +88,58 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
     }
   }
   const float inv_sqrt_d = 1.0f / sqrtf(float(D));
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v[i] *= inv_sqrt_d;
-    amax = fmaxf(amax, fabsf(v[i]));
-  }
-#pragma unroll
-  for (int o = 1; o < TPV; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const __half S = quant_scale_fp16(amax, 1.0f);
-  const float inv = 1.0f / __half2float(S);
+  __half S;
+  int zp = 0;
   uint32_t w[4] = {0, 0, 0, 0};
+  if constexpr (!ASYM) {
+    float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float y = fminf(fmaxf(v[i] * inv, -8.0f), 7.0f);
-    w[i >> 3] |= nibble_rne(y) << (4 * (i & 7));
+    for (int i = 0; i < 32; ++i) {
+      v[i] *= inv_sqrt_d;
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 1; o < TPV; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    S = quant_scale_fp16(amax, 1.0f);
+    const float inv = 1.0f / __half2float(S);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float y = fminf(fmaxf(v[i] * inv, -8.0f), 7.0f);
+      w[i >> 3] |= nibble_rne(y) << (4 * (i & 7));
+    }
+  } else {
+    float vmin = INFINITY, vmax = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] *= inv_sqrt_d;
+      vmin = fminf(vmin, v[i]);
+      vmax = fmaxf(vmax, v[i]);
+    }
+#pragma unroll
+    for (int o = 1; o < TPV; o <<= 1) {
+      vmin = fminf(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    }
+    const float a_min = clip_ratio * vmin, a_max = clip_ratio * vmax;
+    S = __float2half_rn(fminf(fmaxf(a_max - a_min, 1e-5f) / 15.0f, 65504.0f));
+    const float sf = __half2float(S);
+    zp = __float2int_rn(fminf(fmaxf(__fdiv_rn(a_min, sf), -32768.0f), 32767.0f));
+    const float inv = 1.0f / sf;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      // |x / s| is below 2^24 (fp16 inputs, s >= fp16(1e-5 / 15)), so the
+      // fp32 product and the int conversion are exact enough to round
+      const int qi = min(max(__float2int_rn(fminf(fmaxf(v[i] * inv, -1.6e7f), 1.6e7f)) - zp, 0), 15);
+      w[i >> 3] |= uint32_t(qi) << (4 * (i & 7));
+    }
   }
   if (valid) {
     const int64_t pos = (b * Hkv + h) * T_max + t_start + t;
     __stcs(reinterpret_cast<uint4*>(cq + pos * (D / 2) + part * 16), make_uint4(w[0], w[1], w[2], w[3]));
-    if (part == 0) cs[pos] = S;
+    if (part == 0) {
+      cs[pos] = S;
+      if constexpr (ASYM) cz[pos] = int16_t(zp);
+    }
   }
 }
 
@@ -146,10 +184,17 @@ __device__ __forceinline__ uint32_t byte_pair(uint32_t w, int p) {
 }
 // Byte `p` of `wa` and byte `p` of `wb` -> low nibbles (lo_a, lo_b) and high
 // nibbles (hi_a, hi_b) as fp16x2.
+// ASYM: unsigned codes q (no offset): 1024 + q and 1024 + 16 q, minus 1024 / 64.
+template <bool ASYM = false>
 __device__ __forceinline__ void byte_cross(uint32_t wa, uint32_t wb, int p, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = prmt(wa, wb, uint32_t(p) | (uint32_t(p + 4) << 8));
-  lo = hfma2_u32((x & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
-  hi = hfma2_u32((x & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
+  if constexpr (ASYM) {
+    lo = hfma2_u32((x & 0x000F000Fu) | 0x64006400u, H2_ONE, 0xE400E400u);        // - 1024
+    hi = hfma2_u32((x & 0x00F000F0u) | 0x64006400u, H2_SIXTEENTH, 0xD400D400u);  // /16 - 64
+  } else {
+    lo = hfma2_u32((x & 0x000F000Fu) ^ 0x64086408u, H2_ONE, H2_M1032);
+    hi = hfma2_u32((x & 0x00F000F0u) ^ 0x64806480u, H2_SIXTEENTH, H2_M72);
+  }
 }
 
 __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -189,22 +234,29 @@ constexpr int WO = HD + 4;            // padded merge row
 
 template <int G>
 constexpr size_t decode_smem_bytes() {
+  static_assert(2 * G * HD * 2 + 2 * G * 4 <= G * QS * 4, "query halves and per-head constants fit the q region");
   return size_t(G) * QS * 4 + size_t(DT / 32) * NS * TILE_STRIDE + size_t(DT / 32) * NS * 8 + 64;
 }
 
-template <int G>
+// ASYM: the asymmetric cache (unsigned codes q, fp16 scale s, int16 zero point
+// z per token; k^ = s (q + z)).  The keys' magic form is 1024 + q (1024 + 16 q
+// for odd dims), so the per-head offset is 1024 * sum(weights); the zero point
+// adds z_t * sum_d q~_d to each score; the values' zero points add
+// sum_t p'_t z_t to every output dim of the head.  Tiles also carry the 16 K
+// and 16 V zero points (bytes 2112 .. 2175).
+template <int G, bool ASYM>
 __global__ void __launch_bounds__(DT, 4)
 decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, const __half* __restrict__ ks,
                   const uint8_t* __restrict__ vq, const __half* __restrict__ vs, int Hq, int Hkv, int T,
                   int T_max, float qscale, float* __restrict__ ws_o, float* __restrict__ ws_ml, int splits,
-                  int chunk, int bulk_ok) {
+                  int chunk, int bulk_ok, const int16_t* __restrict__ kz, const int16_t* __restrict__ vz) {
   constexpr int NT = (2 * G + 7) / 8;  // n8 tiles of (head, hi/lo) columns
   constexpr int NW = DT / 32;
   extern __shared__ __align__(128) unsigned char dsm[];
   unsigned char* ring = dsm;                                        // [NW][NS][TILE_STRIDE]
   float* qs = reinterpret_cast<float*>(dsm + NW * NS * TILE_STRIDE);  // [G][QS]
   uint64_t* tbar = reinterpret_cast<uint64_t*>(dsm + NW * NS * TILE_STRIDE + G * QS * 4);  // [NW][NS]
-  __shared__ float wm[NW][G], wl[NW][G];
+  __shared__ float wm[NW][G], wl[NW][G], wz[NW][G];
   float* wo = reinterpret_cast<float*>(ring);  // merge rows, reuse the ring after the last tile
 
   const int split = blockIdx.x;
@@ -219,6 +271,8 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   const uint8_t* vbase = vq + cache_row * (HD / 2);
   const __half* ksb = ks + cache_row;
   const __half* vsb = vs + cache_row;
+  const int16_t* kzb = ASYM ? kz + cache_row : nullptr;
+  const int16_t* vzb = ASYM ? vz + cache_row : nullptr;
   unsigned char* wring = ring + wid * NS * TILE_STRIDE;
   uint64_t* wbar = tbar + wid * NS;
 
@@ -235,7 +289,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     if (bulk_ok && tt + 16 <= tn) {
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&wbar[i % NS], TILE_BYTES);
+        mbar_arrive_expect_tx(&wbar[i % NS], TILE_BYTES + (ASYM ? 64 : 0));
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
                          smem_u32(dst)), "l"(kbase + int64_t(tt) * (HD / 2)), "r"(smem_u32(&wbar[i % NS])) : "memory");
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
@@ -244,6 +298,12 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
                          smem_u32(dst + 2048)), "l"(ksb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
                          smem_u32(dst + 2080)), "l"(vsb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        if constexpr (ASYM) {
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
+                           smem_u32(dst + 2112)), "l"(kzb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 32, [%2];" ::"r"(
+                           smem_u32(dst + 2144)), "l"(vzb + tt), "r"(smem_u32(&wbar[i % NS])) : "memory");
+        }
       }
     } else {
       // ragged last tile (or unaligned cache): plain loads, zero beyond tn
@@ -258,6 +318,10 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
         const bool in = tt + lane < tn;
         reinterpret_cast<__half*>(dst + 2048)[lane] = in ? ksb[tt + lane] : __float2half(0.f);
         reinterpret_cast<__half*>(dst + 2080)[lane] = in ? vsb[tt + lane] : __float2half(0.f);
+        if constexpr (ASYM) {
+          reinterpret_cast<int16_t*>(dst + 2112)[lane] = in ? kzb[tt + lane] : int16_t(0);
+          reinterpret_cast<int16_t*>(dst + 2144)[lane] = in ? vzb[tt + lane] : int16_t(0);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&wbar[i % NS]);
@@ -279,6 +343,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   // per-head constant, so its rounding does not change the softmax).
   __half* qh = reinterpret_cast<__half*>(qs);                   // [G][2][HD]: hi row, lo row
   float* qoff_s = reinterpret_cast<float*>(qh + 2 * G * HD);    // [G]
+  float* qsum_s = qoff_s + G;                                   // [G] (ASYM): sum_d q~_d qscale
   for (int hh = wid; hh < G; hh += NW) {
     const uint2 raw = *reinterpret_cast<const uint2*>(q + (int64_t(b) * Hq + g * G + hh) * HD + 4 * lane);
     const float2 x01 = h2_to_f2(raw.x), x23 = h2_to_f2(raw.y);
@@ -307,20 +372,28 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
         x[k] = upper ? other - x[k] : x[k] + other;
       }
     }
-    float part = 0.f;
+    float part = 0.f, qsum = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int dd = 4 * lane + k;
       const float xs = x[k] * qscale * ((dd & 1) ? 0.0625f : 1.0f);
       const __half hi = __float2half_rn(xs);
       const __half lo = __float2half_rn(xs - __half2float(hi));
-      part += (__half2float(hi) + __half2float(lo)) * ((dd & 1) ? 1152.0f : 1032.0f);
+      const float wsum = __half2float(hi) + __half2float(lo);
+      part += wsum * (ASYM ? 1024.0f : ((dd & 1) ? 1152.0f : 1032.0f));
+      qsum += wsum * ((dd & 1) ? 16.0f : 1.0f);
       qh[(2 * hh) * HD + dd] = hi;
       qh[(2 * hh + 1) * HD + dd] = lo;
     }
 #pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-    if (lane == 0) qoff_s[hh] = part;
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      part += __shfl_xor_sync(0xffffffffu, part, o2);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, o2);
+    }
+    if (lane == 0) {
+      qoff_s[hh] = part;
+      qsum_s[hh] = qsum;
+    }
   }
   __syncthreads();
 
@@ -352,11 +425,13 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
   }
   // per-head offset constant of the scores (the head whose scores this
   // thread holds)
-  float qoff[NT];
+  float qoff[NT], qsum[NT], zacc[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 4 + c;
     qoff[nt] = hh < G ? qoff_s[hh] : 0.f;
+    qsum[nt] = hh < G ? qsum_s[hh] : 0.f;
+    zacc[nt] = 0.f;  // ASYM: sum_t p'_t z_t of the head over this thread's tokens
   }
 
   float o[NT][8][4];
@@ -391,6 +466,16 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     }
     const float ks0 = __half2float(reinterpret_cast<const __half*>(src + 2048)[r]);
     const float ks1 = __half2float(reinterpret_cast<const __half*>(src + 2048)[r + 8]);
+    // ASYM: zero points of this thread's score tokens r, r + 8 (keys and values)
+    float kz0 = 0.f, kz1 = 0.f, vzp0 = 0.f, vzp1 = 0.f;
+    if constexpr (ASYM) {
+      kz0 = float(reinterpret_cast<const int16_t*>(src + 2112)[r]);
+      kz1 = float(reinterpret_cast<const int16_t*>(src + 2112)[r + 8]);
+      vzp0 = float(reinterpret_cast<const int16_t*>(src + 2144)[r]) *
+             __half2float(reinterpret_cast<const __half*>(src + 2080)[r]);
+      vzp1 = float(reinterpret_cast<const int16_t*>(src + 2144)[r + 8]) *
+             __half2float(reinterpret_cast<const __half*>(src + 2080)[r + 8]);
+    }
     __syncwarp();
     issue(i + NS);  // refill this stage NS tiles ahead
 
@@ -406,10 +491,12 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
     for (int m4 = 0; m4 < 4; ++m4) {
       const uint32_t w0 = kw0[m4], w1 = kw1[m4], w0s = w0 >> 8, w1s = w1 >> 8;
-      const uint32_t p0a = (w0 & 0x000F000Fu) ^ 0x64086408u, p1a = (w0 & 0x00F000F0u) ^ 0x64806480u;
-      const uint32_t p2a = (w0s & 0x000F000Fu) ^ 0x64086408u, p3a = (w0s & 0x00F000F0u) ^ 0x64806480u;
-      const uint32_t p0b = (w1 & 0x000F000Fu) ^ 0x64086408u, p1b = (w1 & 0x00F000F0u) ^ 0x64806480u;
-      const uint32_t p2b = (w1s & 0x000F000Fu) ^ 0x64086408u, p3b = (w1s & 0x00F000F0u) ^ 0x64806480u;
+      // magic fp16: 0x6400 | nibble bits (XOR 8 on the nibble for signed codes)
+      constexpr uint32_t ML = ASYM ? 0x64006400u : 0x64086408u, MH = ASYM ? 0x64006400u : 0x64806480u;
+      const uint32_t p0a = (w0 & 0x000F000Fu) ^ ML, p1a = (w0 & 0x00F000F0u) ^ MH;
+      const uint32_t p2a = (w0s & 0x000F000Fu) ^ ML, p3a = (w0s & 0x00F000F0u) ^ MH;
+      const uint32_t p0b = (w1 & 0x000F000Fu) ^ ML, p1b = (w1 & 0x00F000F0u) ^ MH;
+      const uint32_t p2b = (w1s & 0x000F000Fu) ^ ML, p3b = (w1s & 0x00F000F0u) ^ MH;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         mma16816(sacc[nt][0], p0a, p0b, p1a, p1b, qb[nt][2 * m4][0], qb[nt][2 * m4][1]);
@@ -421,10 +508,12 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     for (int nt = 0; nt < NT; ++nt) {
       // thread holds head 4 nt + c for tokens tr0 (sacc 0 + 1) and tr1 (sacc 2 + 3)
       const float s0 = tr0 < tn
-                           ? (((sacc[nt][0][0] + sacc[nt][1][0]) + (sacc[nt][0][1] + sacc[nt][1][1])) - qoff[nt]) * ks0
+                           ? ((((sacc[nt][0][0] + sacc[nt][1][0]) + (sacc[nt][0][1] + sacc[nt][1][1])) - qoff[nt]) +
+                              kz0 * qsum[nt]) * ks0
                            : -INFINITY;
       const float s1 = tr1 < tn
-                           ? (((sacc[nt][0][2] + sacc[nt][1][2]) + (sacc[nt][0][3] + sacc[nt][1][3])) - qoff[nt]) * ks1
+                           ? ((((sacc[nt][0][2] + sacc[nt][1][2]) + (sacc[nt][0][3] + sacc[nt][1][3])) - qoff[nt]) +
+                              kz1 * qsum[nt]) * ks1
                            : -INFINITY;
       float mt = fmaxf(s0, s1);
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
@@ -436,6 +525,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
         const float alpha = exp2f(m_run[nt] - m_new);  // 0 when the old max is -inf
         m_run[nt] = m_new;
         l_run[nt] *= alpha;
+        zacc[nt] *= alpha;
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii)
 #pragma unroll
@@ -443,6 +533,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
       }
       const float m_use = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
       const float P0 = exp2f(s0 - m_use), P1 = exp2f(s1 - m_use);
+      if constexpr (ASYM) zacc[nt] = fmaf(P0, vzp0, fmaf(P1, vzp1, zacc[nt]));
       l_run[nt] += P0 + P1;
 
       // B fragment of P'^T: column n = r is head 4 nt + r/2 (hi for even r, lo
@@ -461,8 +552,8 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
       for (int ii = 0; ii < 8; ++ii) {
         uint32_t a0, a1, a2, a3;
-        byte_cross(va[ii >> 2], vb[ii >> 2], ii & 3, a0, a1);
-        byte_cross(vc[ii >> 2], vd[ii >> 2], ii & 3, a2, a3);
+        byte_cross<ASYM>(va[ii >> 2], vb[ii >> 2], ii & 3, a0, a1);
+        byte_cross<ASYM>(vc[ii >> 2], vd[ii >> 2], ii & 3, a2, a3);
         mma16816(o[nt][ii], a0, a1, a2, a3, pb0, pb1);
       }
     }
@@ -474,13 +565,17 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int hh = nt * 4 + c;
-    float l = l_run[nt];
+    float l = l_run[nt], zs = zacc[nt];
     l += __shfl_xor_sync(0xffffffffu, l, 4);
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
+    zs += __shfl_xor_sync(0xffffffffu, zs, 4);
+    zs += __shfl_xor_sync(0xffffffffu, zs, 8);
+    zs += __shfl_xor_sync(0xffffffffu, zs, 16);
     if (hh < G) {
       if (r == 0) {
         wm[wid][hh] = m_run[nt];
+        wz[wid][hh] = zs;  // ASYM: the values' zero-point term, common to all dims
         wl[wid][hh] = l;
       }
       float* wrow = wo + (wid * G + hh) * WO + 16 * r;
@@ -503,7 +598,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
     for (int w = 0; w < NW; ++w) {
       const float f = exp2f(wm[w][hh] - m_use);
       l += f * wl[w][hh];
-      acc += f * wo[(w * G + hh) * WO + e];
+      acc += f * (wo[(w * G + hh) * WO + e] + wz[w][hh]);
     }
     const int64_t slot = base + int64_t(hh) * splits;
     ws_o[slot * HD + e] = acc;
@@ -551,6 +646,7 @@ decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ 
 }
 
 // Resident CTAs per SM of the decode kernel for group size G (queried once).
+template <bool ASYM>
 int decode_ctas_per_sm(int G) {
   static int cache[4] = {0, 0, 0, 0};
   const int slot = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
@@ -558,10 +654,10 @@ int decode_ctas_per_sm(int G) {
     int n = 0;
     cudaError_t e = cudaErrorInvalidValue;
     switch (G) {
-      case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<1>, DT, decode_smem_bytes<1>()); break;
-      case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<2>, DT, decode_smem_bytes<2>()); break;
-      case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<4>, DT, decode_smem_bytes<4>()); break;
-      default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<8>, DT, decode_smem_bytes<8>()); break;
+      case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<1, ASYM>, DT, decode_smem_bytes<1>()); break;
+      case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<2, ASYM>, DT, decode_smem_bytes<2>()); break;
+      case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<4, ASYM>, DT, decode_smem_bytes<4>()); break;
+      default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<8, ASYM>, DT, decode_smem_bytes<8>()); break;
     }
     cache[slot] = (e == cudaSuccess && n > 0) ? n : 1;
   }
@@ -573,16 +669,18 @@ int decode_ctas_per_sm(int G) {
 
 using namespace quarot;
 
-extern "C" int quarot_kv_write(const void* k, const void* v, int64_t B, int64_t T_new, int64_t Hkv,
-                               int64_t d, int64_t t_start, int64_t T_max, uint8_t* k_q, void* k_s,
-                               uint8_t* v_q, void* v_s, void* stream) {
+static int kv_write_impl(bool asym, const void* k, const void* v, int64_t B, int64_t T_new, int64_t Hkv, int64_t d,
+                         int64_t t_start, int64_t T_max, float clip_ratio, uint8_t* k_q, void* k_s, int16_t* k_z,
+                         uint8_t* v_q, void* v_s, int16_t* v_z, void* stream) {
   if (B < 0 || T_new < 0 || Hkv <= 0 || t_start < 0 || T_max <= 0) return QUAROT_ERR_INVALID_ARG;
   if (t_start + T_new > T_max) return QUAROT_ERR_INVALID_ARG;
+  if (asym && !(clip_ratio > 0.f && clip_ratio <= 1.f)) return QUAROT_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return QUAROT_ERR_UNSUPPORTED;
   if (B == 0 || T_new == 0) return QUAROT_OK;
-  if (!k || !v || !k_q || !k_s || !v_q || !v_s) return QUAROT_ERR_INVALID_ARG;
+  if (!k || !v || !k_q || !k_s || !v_q || !v_s || (asym && (!k_z || !v_z))) return QUAROT_ERR_INVALID_ARG;
   auto mis = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
-  if (mis(k, 16) || mis(v, 16) || mis(k_q, 16) || mis(v_q, 16) || mis(k_s, 2) || mis(v_s, 2))
+  if (mis(k, 16) || mis(v, 16) || mis(k_q, 16) || mis(v_q, 16) || mis(k_s, 2) || mis(v_s, 2) ||
+      (asym && (mis(k_z, 2) || mis(v_z, 2))))
     return QUAROT_ERR_ALIGNMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t threads = B * Hkv * T_new * (d / 32);
@@ -591,12 +689,32 @@ extern "C" int quarot_kv_write(const void* k, const void* v, int64_t B, int64_t 
   auto go = [&](auto kern) {
     kern<<<dim3(unsigned(blocks), 2), 256, 0, st>>>(static_cast<const __half*>(k), static_cast<const __half*>(v),
                                                     B, T_new, Hkv, t_start, T_max, k_q, static_cast<__half*>(k_s),
-                                                    v_q, static_cast<__half*>(v_s));
+                                                    v_q, static_cast<__half*>(v_s), k_z, v_z, clip_ratio);
   };
-  if (d == 64) go(kv::kv_write_kernel<64>);
-  else if (d == 128) go(kv::kv_write_kernel<128>);
-  else go(kv::kv_write_kernel<256>);
+  if (asym) {
+    if (d == 64) go(kv::kv_write_kernel<64, true>);
+    else if (d == 128) go(kv::kv_write_kernel<128, true>);
+    else go(kv::kv_write_kernel<256, true>);
+  } else {
+    if (d == 64) go(kv::kv_write_kernel<64, false>);
+    else if (d == 128) go(kv::kv_write_kernel<128, false>);
+    else go(kv::kv_write_kernel<256, false>);
+  }
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+extern "C" int quarot_kv_write(const void* k, const void* v, int64_t B, int64_t T_new, int64_t Hkv,
+                               int64_t d, int64_t t_start, int64_t T_max, uint8_t* k_q, void* k_s,
+                               uint8_t* v_q, void* v_s, void* stream) {
+  return kv_write_impl(false, k, v, B, T_new, Hkv, d, t_start, T_max, 1.0f, k_q, k_s, nullptr, v_q, v_s, nullptr,
+                       stream);
+}
+
+extern "C" int quarot_kv_write_asym(const void* k, const void* v, int64_t B, int64_t T_new, int64_t Hkv, int64_t d,
+                                    int64_t t_start, int64_t T_max, float clip_ratio, uint8_t* k_q, void* k_s,
+                                    int16_t* k_z, uint8_t* v_q, void* v_s, int16_t* v_z, void* stream) {
+  return kv_write_impl(true, k, v, B, T_new, Hkv, d, t_start, T_max, clip_ratio, k_q, k_s, k_z, v_q, v_s, v_z,
+                       stream);
 }
 
 extern "C" size_t quarot_decode_workspace_bytes(int64_t B, int64_t Hq, int64_t d, int64_t T) {
@@ -606,10 +724,11 @@ extern "C" size_t quarot_decode_workspace_bytes(int64_t B, int64_t Hq, int64_t d
   return (bytes + 255) & ~size_t(255);
 }
 
-extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const uint8_t* v_q,
-                                  const void* v_s, int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t T,
-                                  int64_t T_max, float sm_scale, int unrotate_out, void* out,
-                                  void* workspace, size_t ws_bytes, void* stream) {
+template <bool ASYM>
+static int decode_impl(const void* q, const uint8_t* k_q, const void* k_s, const int16_t* k_z, const uint8_t* v_q,
+                       const void* v_s, const int16_t* v_z, int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t T,
+                       int64_t T_max, float sm_scale, int unrotate_out, void* out, void* workspace, size_t ws_bytes,
+                       void* stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || T < 0 || T_max < 0 || T > T_max) return QUAROT_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return QUAROT_ERR_INVALID_ARG;
   if (d != kv::HD || Hq / Hkv > kv::MAXG) return QUAROT_ERR_UNSUPPORTED;
@@ -619,11 +738,11 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   if (T == 0) {
     return cudaMemsetAsync(out, 0, size_t(B * Hq * d) * 2, st) == cudaSuccess ? QUAROT_OK : QUAROT_ERR_CUDA;
   }
-  if (!k_q || !k_s || !v_q || !v_s || !workspace) return QUAROT_ERR_INVALID_ARG;
+  if (!k_q || !k_s || !v_q || !v_s || !workspace || (ASYM && (!k_z || !v_z))) return QUAROT_ERR_INVALID_ARG;
   if (ws_bytes < quarot_decode_workspace_bytes(B, Hq, d, T)) return QUAROT_ERR_INVALID_ARG;
   auto mis = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
   if (mis(q, 16) || mis(k_q, 16) || mis(v_q, 16) || mis(k_s, 2) || mis(v_s, 2) || mis(out, 16) ||
-      mis(workspace, 256))
+      mis(workspace, 256) || (ASYM && (mis(k_z, 2) || mis(v_z, 2))))
     return QUAROT_ERR_ALIGNMENT;
   if (B * Hkv > 65535 || T > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   // Splits: as many as fit one wave of resident CTAs (no tail wave), at least
@@ -632,7 +751,7 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   const int G = int(Hq / Hkv);
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int per_sm = kv::decode_ctas_per_sm(G);
+  const int per_sm = kv::decode_ctas_per_sm<ASYM>(G);
   const int64_t max_splits = kv::num_splits(T);
   int64_t want = (int64_t(per_sm) * sms) / (B * Hkv);
   want = want < 1 ? 1 : (want > max_splits ? max_splits : want);
@@ -646,7 +765,8 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
   dim3 grid(unsigned(splits), unsigned(B * Hkv));
   // bulk copies need 16-byte aligned sources: every (b, g) row of the scale
   // arrays starts at a multiple of 8 tokens
-  const int bulk_ok = (T_max % 8) == 0 && !mis(k_s, 16) && !mis(v_s, 16);
+  const int bulk_ok = (T_max % 8) == 0 && !mis(k_s, 16) && !mis(v_s, 16) &&
+                      (!ASYM || (!mis(k_z, 16) && !mis(v_z, 16)));
   int lrc = QUAROT_OK;
   auto args = [&](auto kern, size_t smem) {
     static bool attr[4] = {false, false, false, false};
@@ -660,13 +780,13 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
     }
     kern<<<grid, kv::DT, smem, st>>>(static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q,
                                      static_cast<const __half*>(v_s), int(Hq), int(Hkv), int(T), int(T_max),
-                                     qscale, ws_o, ws_ml, splits, int(chunk), bulk_ok);
+                                     qscale, ws_o, ws_ml, splits, int(chunk), bulk_ok, k_z, v_z);
   };
   switch (G) {
-    case 1: args(kv::decode_mma_kernel<1>, kv::decode_smem_bytes<1>()); break;
-    case 2: args(kv::decode_mma_kernel<2>, kv::decode_smem_bytes<2>()); break;
-    case 4: args(kv::decode_mma_kernel<4>, kv::decode_smem_bytes<4>()); break;
-    case 8: args(kv::decode_mma_kernel<8>, kv::decode_smem_bytes<8>()); break;
+    case 1: args(kv::decode_mma_kernel<1, ASYM>, kv::decode_smem_bytes<1>()); break;
+    case 2: args(kv::decode_mma_kernel<2, ASYM>, kv::decode_smem_bytes<2>()); break;
+    case 4: args(kv::decode_mma_kernel<4, ASYM>, kv::decode_smem_bytes<4>()); break;
+    case 8: args(kv::decode_mma_kernel<8, ASYM>, kv::decode_smem_bytes<8>()); break;
     default: return QUAROT_ERR_UNSUPPORTED;
   }
   if (lrc != QUAROT_OK) return lrc;
@@ -688,4 +808,20 @@ extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void*
       cudaSuccess)
     return QUAROT_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+extern "C" int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const uint8_t* v_q,
+                                  const void* v_s, int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t T,
+                                  int64_t T_max, float sm_scale, int unrotate_out, void* out,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  return decode_impl<false>(q, k_q, k_s, nullptr, v_q, v_s, nullptr, B, Hq, Hkv, d, T, T_max, sm_scale, unrotate_out,
+                            out, workspace, ws_bytes, stream);
+}
+
+extern "C" int quarot_decode_attn_asym(const void* q, const uint8_t* k_q, const void* k_s, const int16_t* k_z,
+                                       const uint8_t* v_q, const void* v_s, const int16_t* v_z, int64_t B,
+                                       int64_t Hq, int64_t Hkv, int64_t d, int64_t T, int64_t T_max, float sm_scale,
+                                       int unrotate_out, void* out, void* workspace, size_t ws_bytes, void* stream) {
+  return decode_impl<true>(q, k_q, k_s, k_z, v_q, v_s, v_z, B, Hq, Hkv, d, T, T_max, sm_scale, unrotate_out, out,
+                           workspace, ws_bytes, stream);
 }
