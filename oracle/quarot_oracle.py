@@ -35,6 +35,8 @@ design notes):
     (saturating at 65504), codes = clamp(round_half_even(x~ / S_fp16), -8, 7);
   * two codes per byte, even index in the low nibble, two's complement;
   * dequant epilogue Y = fp16(fp32(fp32(acc) * sx_i) * sw_j);
+  * cross-head transform: x~ = z (H_nh (x) I_dh) / sqrt(nh), index h * dh + j,
+    no random signs (head counts a power of two);
   * RMSNorm is scale-free, x / sqrt(mean(x^2) + eps), applied before the
     rotation (they commute: the rotation preserves the row norm);
   * asymmetric KV mode: a = 0.95 * (min, max) of the group, s = fp16(range / 15),
@@ -245,6 +247,35 @@ def rmsnorm_rotate_quant(x: np.ndarray, signs: np.ndarray | None, eps: float, cl
     rounded once to fp32.
     """
     r = rotate(rmsnorm(x, eps), signs)
+    q, S = quantize_rows(r, clip_ratio)
+    return pack_int4(q), S, r
+
+
+# ---------------------------------------------------------------------------
+# Cross-head Hadamard before the output projection ([S] Stage 1c "The online
+# Hadamard heads transform": H_{nh dh} = (I_nh (x) H_dh)(H_nh (x) I_dh); the
+# head-wise factor is in the rotated values, the cross-head factor
+# Z <- Z (H_nh (x) I_dh) runs online, then the per-token quantizer feeds the
+# W4A4 output projection)
+# ---------------------------------------------------------------------------
+def crosshead_rotate(z: np.ndarray, nh: int) -> np.ndarray:
+    """x~ = z (H_nh (x) I_dh) / sqrt(nh) for each row of d = nh * dh, element
+    index k = h * dh + j: x~[k, j] = sum_h z[h, j] H_nh[h, k] / sqrt(nh).
+    Exact in float64, returned as fp32."""
+    z = np.asarray(z)
+    d = z.shape[-1]
+    if d % nh:
+        raise ValueError("d must be a multiple of nh")
+    zs = z.reshape(-1, nh, d // nh).astype(np.float64)
+    H = hadamard(nh).astype(np.float64)
+    r = np.einsum("mhj,hk->mkj", zs, H) / math.sqrt(nh)
+    return r.reshape(z.shape).astype(np.float32)
+
+
+def crosshead_rotate_quant(z: np.ndarray, nh: int, clip_ratio: float = 1.0):
+    """Cross-head rotation, then the per-row INT4 quantize-and-pack:
+    (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d])."""
+    r = crosshead_rotate(z, nh)
     q, S = quantize_rows(r, clip_ratio)
     return pack_int4(q), S, r
 

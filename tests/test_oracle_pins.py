@@ -273,6 +273,43 @@ def test_rmsnorm_rotate_quant_zero_row_and_row_scale_freedom():
     assert all(np.array_equal(u, v) for u, v in zip(a, b))
 
 
+# ---------------------------------------------------------------- cross-head Hadamard (next row f3)
+def test_crosshead_worked_example(golden):
+    g = golden("crosshead_rotate_quant_worked.txt")
+    z = np.array([[float(v) for v in g["z"]]], dtype=np.float16)
+    packed, S, r = O.crosshead_rotate_quant(z, int(g["nh"][0]))
+    assert np.allclose(r[0], np.array([float(v) for v in g["rotated"]]), rtol=1e-6)
+    assert float(S[0]) == float(g["scale"][0])
+    assert np.array_equal(O.unpack_int4(packed)[0], np.array([int(v) for v in g["codes"]]))
+    assert np.array_equal(packed[0], np.array([int(v) for v in g["packed"]], dtype=np.uint8))
+
+
+def test_crosshead_after_headwise_is_the_full_hadamard():
+    # the pages' identity H_{nh dh} = (I_nh (x) H_dh)(H_nh (x) I_dh): the head-wise
+    # rotation (already in the rotated values) followed by the cross-head one is
+    # the full Sylvester rotation of the concatenated heads
+    nh, dh = 32, 128
+    rng = np.random.default_rng(12)
+    z = rng.standard_normal((3, nh * dh))
+    headwise = O.rotate_f64(z.reshape(3, nh, dh), None).reshape(3, nh * dh)
+    assert np.allclose(O.crosshead_rotate(headwise, nh), O.rotate_f64(z, None), rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("nh", [1, 4, 32])
+def test_crosshead_norm_and_identity(nh):
+    rng = np.random.default_rng(13)
+    z = rng.standard_normal((4, nh * 64)).astype(np.float32)
+    r = O.crosshead_rotate(z, nh).astype(np.float64)
+    assert np.allclose(np.linalg.norm(r, axis=1), np.linalg.norm(z.astype(np.float64), axis=1), rtol=1e-6)
+    if nh == 1:
+        assert np.array_equal(r, z.astype(np.float64))
+    # within-head position j only mixes with the same j of other heads
+    one = np.zeros((1, nh * 64), np.float32)
+    one[0, 5] = 1.0
+    nz = np.nonzero(O.crosshead_rotate(one, nh)[0])[0]
+    assert np.array_equal(nz % 64, np.full(nh, 5)) and len(nz) == nh
+
+
 # ---------------------------------------------------------------- quantizer
 def _golden_quant(g):
     x = np.array([float(v) for v in g["x"]], dtype=np.float32)
