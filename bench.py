@@ -435,6 +435,15 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     res["rmsnorm_rotate_quant_2048x12288"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
                                               "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
     del xt, qo, so
+    # cross-head Hadamard + INT4 of a prefill-sized attention output (2048 tokens x 32 heads x 128)
+    zt = torch.from_numpy(W.query(2048, 32, 128, 77).reshape(2048, 4096)).to(dev)
+    zq = torch.empty((2048, 2048), dtype=torch.uint8, device=dev)
+    zs = torch.empty((2048,), dtype=torch.float16, device=dev)
+    ms = timed(lambda: q.quarot_crosshead_rotate_quant(zt, 32, q_out=zq, scale_out=zs, stream=stream))
+    nbytes = 2048 * 4096 * 2 + 2048 * 2048 + 2048 * 2
+    res["crosshead_rotate_quant_2048x32x128"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                                 "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+    del zt, zq, zs
     # asymmetric KV cache (group 128, zero point, clip 0.95): decode at the kv4 size
     k, v, qq = W.kv_inputs("kv4")
     B, T, Hkv, d = k.shape

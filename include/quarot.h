@@ -112,6 +112,30 @@ int quarot_rmsnorm_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_
                                 float* rot_out, void* stream);
 
 /*
+ * quarot_crosshead_rotate_quant -- the online cross-head Hadamard applied to
+ * the concatenated attention output before the output projection, fused with
+ * per-token INT4 quantization.  [S] Stage 1c, "The online Hadamard heads
+ * transform": H_{nh dh} = (I_nh (x) H_dh)(H_nh (x) I_dh); the head-wise factor
+ * is carried by the rotated values (quarot_decode_attn with unrotate_out = 0),
+ * the cross-head factor runs here; Stage 2b per-token quantizer.
+ *
+ * For each row i of z (d = nh * dh, element h * dh + j):
+ *   r[k * dh + j] = sum_h z[h * dh + j] * H_nh[h][k] / sqrt(nh)   (fp32)
+ *   S, q exactly as quarot_rotate_quant (clip_ratio).
+ * A W_out prepared with quarot_rotate_quant(signs = NULL) at width d then
+ * sees the fully rotated input (Sylvester H_d = H_nh (x) H_dh).
+ *
+ *   z         fp16 [M, ld_z], first nh * dh columns used, 2-byte aligned
+ *   nh        power of two, 1 .. 64 (else QUAROT_ERR_UNSUPPORTED)
+ *   dh        64 or 128
+ *   q_out     uint8 [M, d/2], 4-byte aligned
+ *   scale_out fp16 [M]
+ *   rot_out   fp32 [M, d] (the rotated values), or NULL
+ */
+int quarot_crosshead_rotate_quant(const void* z, int64_t M, int64_t nh, int64_t dh, int64_t ld_z, float clip_ratio,
+                                  uint8_t* q_out, void* scale_out, float* rot_out, void* stream);
+
+/*
  * quarot_w4a4_gemm -- W4A4 GEMM with INT32-exact accumulation and the
  * per-token x per-output-channel dequantization epilogue.
  * [S] Stage 2b "dequantization step", "Kernel Implementation" (INT4 GEMM,

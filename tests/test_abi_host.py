@@ -114,6 +114,19 @@ def test_kv_asym_validation(lib):
     assert a(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 30, 8, 128, 16, 16, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 1
 
 
+def test_crosshead_validation(lib):
+    f = lib.quarot_crosshead_rotate_quant
+    assert f(FAKE, 0, 32, 128, 4096, 1.0, FAKE, FAKE, None, None) == 0  # M = 0 no-op
+    assert f(FAKE, 4, 24, 128, 3072, 1.0, FAKE, FAKE, None, None) == 2  # nh not a power of two
+    assert f(FAKE, 4, 128, 128, 16384, 1.0, FAKE, FAKE, None, None) == 2  # nh > 64
+    assert f(FAKE, 4, 32, 96, 3072, 1.0, FAKE, FAKE, None, None) == 2  # dh
+    assert f(FAKE, 4, 32, 128, 4000, 1.0, FAKE, FAKE, None, None) == 1  # ld < d
+    assert f(FAKE, 4, 32, 128, 4096, 0.0, FAKE, FAKE, None, None) == 1  # clip
+    assert f(None, 4, 32, 128, 4096, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(P(0x10001), 4, 32, 128, 4096, 1.0, FAKE, FAKE, None, None) == 3  # misaligned z
+    assert f(FAKE, 4, 32, 128, 4096, 1.0, P(0x10002), FAKE, None, None) == 3  # misaligned q_out
+
+
 def test_workspace_size(lib):
     assert q.quarot_decode_workspace_bytes(16, 32, 128, 4096) == 16 * 32 * 16 * 130 * 4
     assert q.quarot_decode_workspace_bytes(1, 1, 128, 1) == 768  # 130 floats rounded up to 256 B

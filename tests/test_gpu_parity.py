@@ -163,6 +163,46 @@ def test_rmsnorm_rotate_quant_down_proj_sampled(q):
     check_quant(gq.cpu().numpy()[rows], gs.cpu().numpy()[rows], grot.cpu().numpy()[rows], r_ref)
 
 
+# ---------------------------------------------------------------- cross-head Hadamard + quant (next row f3)
+@pytest.mark.parametrize("nh,dh", [(1, 128), (2, 64), (8, 128), (32, 128), (64, 64)])
+def test_crosshead_rotate_quant_parity(q, nh, dh):
+    M = 37
+    z = W.query(M, nh, dh, 70 + nh).reshape(M, nh * dh)
+    z[3, min(dh + 5, nh * dh - 1)] = np.float16(60.0)  # an outlier in one head
+    gq, gs, grot = q.quarot_crosshead_rotate_quant(_t(z), nh, want_rot=True)
+    check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), O.crosshead_rotate(z, nh))
+    gq, gs, grot = q.quarot_crosshead_rotate_quant(_t(z), nh, clip_ratio=0.9, want_rot=True)
+    check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), O.crosshead_rotate(z, nh), clip=0.9)
+
+
+def test_attention_output_path_end_to_end(q):
+    """Decode in the rotated basis -> cross-head Hadamard + INT4 -> W4A4 GEMM
+    against W_out rows rotated by the full H_4096 (= H_32 (x) H_128)."""
+    B, Hkv, G, d, T, N = 4, 8, 4, 128, 256, 512
+    Hq = Hkv * G
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 81)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 82)
+    qq = W.query(B, Hq, d, 83)
+    gc = q.new_kv_cache(B, Hkv, T, d, DEV)
+    q.quarot_kv_write(_t(k), _t(v), 0, *gc)
+    o_rot = q.quarot_decode_attn(_t(qq), *gc, T=T, unrotate_out=False)  # [B, Hq, d], rotated basis
+    zq, zs, _ = q.quarot_crosshead_rotate_quant(o_rot, Hq)
+    w_out = W.weights(N, Hq * d, 84)
+    wq, ws, _ = q.quarot_rotate_quant(_t(w_out), None)
+    y, _ = q.quarot_w4a4_gemm(zq, zs, wq, ws)
+    y = y.cpu().numpy().astype(np.float64)
+    # parity: the oracle's chain on the GPU's decode output
+    oz, ozs, _ = O.crosshead_rotate_quant(o_rot.cpu().numpy().reshape(B, Hq * d), Hq)
+    ow, ows, _ = O.rotate_quant(w_out, None)
+    _, oy = O.w4a4_gemm(oz, ozs, ow, ows)
+    assert O.rel_fro(y, oy) <= OUT_TOL
+    # the rotations cancel: y approximates the un-rotated attention output times
+    # W_out^T up to the W4A4 error (a wrong factor would be an O(1) error)
+    gnp = [t.cpu().numpy() for t in gc]
+    attn = O.decode_attn(qq, *gnp, T=T, unrotate=True).reshape(B, Hq * d)
+    assert O.rel_fro(y, attn @ w_out.astype(np.float64).T) < 0.25
+
+
 # ---------------------------------------------------------------- GEMM
 def _gemm_case(q, M, N, K, seed, codes_a=None, codes_w=None):
     a = W.int4_codes(M, K, seed) if codes_a is None else codes_a

@@ -35,6 +35,7 @@ _SIGS = {
     "quarot_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_rmsnorm_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, ctypes.c_float, _P, ctypes.c_float, _P, _P,
                                                    _P, _P]),
+    "quarot_crosshead_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_w4a4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "quarot_kv_write": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "quarot_decode_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
@@ -139,6 +140,22 @@ def quarot_rmsnorm_rotate_quant(x, signs=None, eps: float = 1e-6, clip_ratio: fl
     st = load().quarot_rmsnorm_rotate_quant(_ptr(x), M, d, d, float(eps), _ptr(signs), float(clip_ratio),
                                             _ptr(q_out), _ptr(scale_out), _ptr(rot_out), _stream(stream, x.device))
     _check(st, "quarot_rmsnorm_rotate_quant")
+    return q_out, scale_out, rot_out
+
+
+def quarot_crosshead_rotate_quant(z, nh: int, clip_ratio: float = 1.0, q_out=None, scale_out=None, rot_out=None,
+                                  stream=None, want_rot: bool = False):
+    """z fp16 [M, nh * dh] (or [M, nh, dh]) -> cross-head Hadamard + INT4:
+    (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d] or None)."""
+    if z.dim() == 3:
+        z = z.reshape(z.shape[0], -1)
+    q_out, scale_out, rot_out = _rotate_quant_outputs(z, None, q_out, scale_out, rot_out, want_rot)
+    M, d = z.shape
+    if d % nh:
+        raise QuarotError(1, "row width is not a multiple of nh")
+    st = load().quarot_crosshead_rotate_quant(_ptr(z), M, int(nh), d // int(nh), d, float(clip_ratio), _ptr(q_out),
+                                              _ptr(scale_out), _ptr(rot_out), _stream(stream, z.device))
+    _check(st, "quarot_crosshead_rotate_quant")
     return q_out, scale_out, rot_out
 
 
