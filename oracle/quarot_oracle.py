@@ -372,6 +372,48 @@ def decode_attn(q, k_cache, k_scale, v_cache, v_scale, T: int, sm_scale: float |
     return out
 
 
+def prefill_attn(q, k_cache, k_scale, v_cache, v_scale, T: int, sm_scale: float | None = None,
+                 causal: bool = True, unrotate: bool = False) -> np.ndarray:
+    """Prefill ("Init") attention of T query tokens over the first T cached
+    tokens ([S] "Quantized attention with KV cache", Init routine: attention
+    over the whole prompt with dequantized keys and values), float64.
+
+    q: fp16 [B, T, Hq, d]; query i sits at position i.  q~ = q @ H / sqrt(d)
+    per head; head h reads KV head h // (Hq / Hkv); s[i, t] = sm_scale *
+    (q~_i . k^_t) with k^_t = Ks[t] * codes_t, restricted to t <= i when
+    causal; p = softmax over t; o_i = sum_t p[i, t] * Vs[t] * vcodes_t;
+    optionally o <- o @ H / sqrt(d).  Returns float64 [B, T, Hq, d].
+    """
+    q = np.asarray(q)
+    B, Tq, Hq, d = q.shape
+    if Tq != T:
+        raise ValueError("prefill takes T queries for T cached tokens")
+    Hkv = k_cache.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    grp = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if sm_scale is None or sm_scale <= 0 else float(sm_scale)
+    qr = rotate_f64(q, None)  # [B, T, Hq, d]
+    out = np.zeros((B, T, Hq, d), dtype=np.float64)
+    if T == 0:
+        return out
+    mask = np.tril(np.ones((T, T), dtype=bool)) if causal else np.ones((T, T), dtype=bool)
+    for b in range(B):
+        for g in range(Hkv):
+            kd = unpack_int4(k_cache[b, g, :T]).astype(np.float64) * k_scale[b, g, :T].astype(np.float64)[:, None]
+            vd = unpack_int4(v_cache[b, g, :T]).astype(np.float64) * v_scale[b, g, :T].astype(np.float64)[:, None]
+            for h in range(g * grp, (g + 1) * grp):
+                s = scale * (qr[b, :, h] @ kd.T)  # [T, T]
+                s = np.where(mask, s, -np.inf)
+                s = s - s.max(axis=1, keepdims=True)
+                p = np.exp(s)
+                p /= p.sum(axis=1, keepdims=True)
+                out[b, :, h] = p @ vd
+    if unrotate:
+        out = rotate_f64(out, None)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Asymmetric per-group KV quantizer ([S] Stage 2c "KV Cache Quantization --
 # online, per-group asymmetric": group size 128, i.e. one group per (token,

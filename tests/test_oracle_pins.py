@@ -490,6 +490,53 @@ def test_decode_brute_force_tiny():
         assert np.allclose(out[0, h], o_un, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- prefill attention (next row f4)
+def _prefill_case(B, T, Hkv, G, d, seed):
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, seed)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, seed + 1)
+    qq = np.random.default_rng(seed + 2).standard_normal((B, T, Hkv * G, d)).astype(np.float16)
+    kc, ks, vc, vs = _fill_cache(k, v, T)
+    return qq, kc, ks, vc, vs
+
+
+def test_prefill_rows_agree_with_decode():
+    # the pinned decode is prefill's row: causal row i = decode of query i over
+    # tokens 0..i; without the mask every row = decode over all T tokens
+    B, T, Hkv, G, d = 1, 9, 2, 2, 128
+    qq, kc, ks, vc, vs = _prefill_case(B, T, Hkv, G, d, 21)
+    causal = O.prefill_attn(qq, kc, ks, vc, vs, T)
+    full = O.prefill_attn(qq, kc, ks, vc, vs, T, causal=False, unrotate=True)
+    for i in (0, 4, T - 1):
+        assert np.allclose(causal[:, i], O.decode_attn(qq[:, i], kc, ks, vc, vs, T=i + 1), rtol=1e-12, atol=1e-12)
+        assert np.allclose(full[:, i], O.decode_attn(qq[:, i], kc, ks, vc, vs, T=T, unrotate=True), rtol=1e-12,
+                           atol=1e-12)
+    # causal row 0 sees only token 0: its dequantized value
+    v0 = O.unpack_int4(vc[:, :, 0]).astype(np.float64) * vs[:, :, 0].astype(np.float64)[..., None]
+    assert np.allclose(causal[:, 0], np.repeat(v0, G, axis=1), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_brute_force_tiny():
+    # B=1, T=3, Hq=2, Hkv=1, d=4, causal: explicit loops and math.exp
+    d, T = 4, 3
+    rng = np.random.default_rng(22)
+    k = rng.standard_normal((1, T, 1, d)).astype(np.float16)
+    v = rng.standard_normal((1, T, 1, d)).astype(np.float16)
+    q = rng.standard_normal((1, T, 2, d)).astype(np.float16)
+    kc, ks, vc, vs = _fill_cache(k, v, T)
+    out = O.prefill_attn(q, kc, ks, vc, vs, T)
+    H4 = [[_sylvester_entry(i, j) for j in range(d)] for i in range(d)]
+    kcodes, vcodes = O.unpack_int4(kc[0, 0]), O.unpack_int4(vc[0, 0])
+    for h in range(2):
+        for i in range(T):
+            qr = [sum(float(q[0, i, h, a]) * H4[a][j] for a in range(d)) / 2.0 for j in range(d)]
+            s = [sum(qr[j] * float(ks[0, 0, t]) * int(kcodes[t, j]) for j in range(d)) / 2.0 for t in range(i + 1)]
+            m = max(s)
+            e = [math.exp(x - m) for x in s]
+            p = [x / sum(e) for x in e]
+            o = [sum(p[t] * float(vs[0, 0, t]) * int(vcodes[t, j]) for t in range(i + 1)) for j in range(d)]
+            assert np.allclose(out[0, i, h], o, rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- asymmetric KV quantizer (next row f1)
 @pytest.mark.parametrize("ex", ["A", "B"])
 def test_kv_asym_quantizer_worked_examples(golden, ex):
