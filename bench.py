@@ -394,7 +394,8 @@ def run_ours(args):
 def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     """The other measured workloads: rotate+quant of 2048 x 4096 (H_4096, HBM
     roof), the fused RMSNorm + rotate + quant at 2048 x 4096 and 2048 x 12288,
-    decode over the asymmetric KV cache at the kv4 size, and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096, 12288}
+    decode over the asymmetric KV cache at the kv4 size, causal prefill attention
+    (4 x 2048 tokens, fp16 tensor roof), and the GEMM sweep M in {512, 2048, 8192} x K 4096 x N in {4096, 12288}
     (tensor roof).  Same cold-L2 protocol as the stages; rank 0 only."""
     import torch
 
@@ -458,6 +459,19 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     res["decode_attn_asym_kv4"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
                                    "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
     del ac, qd, od, wsd
+    # Init (prefill) attention over the INT4 cache: 4 prompts x 2048 tokens,
+    # Hq 32 / Hkv 8, causal; flops are the useful ones (t <= i), 4 d per pair
+    k, v, qq = W.prefill_inputs("prefill")
+    B, T, Hkv, d = k.shape
+    Hq = qq.shape[2]
+    pc = q.new_kv_cache(B, Hkv, T, d, dev)
+    q.quarot_kv_write(torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev), 0, *pc, stream=stream)
+    qp = torch.from_numpy(qq).to(dev)
+    op = torch.empty_like(qp)
+    ms = timed(lambda: q.quarot_prefill_attn(qp, *pc, out=op, stream=stream))
+    tf = 4.0 * B * Hq * d * (T * (T + 1) / 2) / (ms / 1e3) / 1e12
+    res["prefill_attn_4x2048_h32kv8"] = {"ms": ms, "TFLOP/s": tf, "frac_f16_peak": tf / (fp8_peak / 2)}
+    del pc, qp, op
     g = torch.Generator(device="cpu").manual_seed(1234)
     K = 4096
     for N in (4096, 12288):

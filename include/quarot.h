@@ -210,6 +210,35 @@ int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const
                        size_t ws_bytes, void* stream);
 
 /*
+ * quarot_prefill_attn -- "Init": attention of a whole prompt over the INT4
+ * cache, flash-attention style, dequantizing keys and values on load.
+ * [S] "Kernel Implementation and Hardware Efficiency", quantized attention
+ * with KV cache, Init (flash attention with dequantized keys and values, all
+ * of them available at once during prefill); Stage 1d (the query is rotated
+ * head-wise after RoPE, as the cached keys are).
+ *
+ * Query i of head h attends to cached tokens t < T (t <= i when causal):
+ *   q~ = q[b, i, h] @ H_d / sqrt(d);  g = h / (Hq / Hkv)
+ *   s_t = sm_scale * (q~ . (k_s[t] * kcode_t)),  p = softmax(s)
+ *   out[b, i, h] = sum_t p_t * v_s[t] * vcode_t    (rotated basis, Stage 1c)
+ * Arithmetic: q~ * sm_scale * log2(e), the dequantized keys and values and
+ * the probabilities are fp16 (the pages' fp16 flash attention); products
+ * accumulate in fp32 on the tensor cores; softmax is fp32.
+ *
+ *   q         fp16 [B, T, Hq, d] (prompt tokens 0 .. T-1), 8-byte aligned
+ *   k_q, k_s, v_q, v_s  caches as written by quarot_kv_write (capacity
+ *             T_max >= T, tokens 0 .. T-1 written); k_q, v_q 16-byte aligned
+ *   d         128; Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}
+ *   sm_scale  softmax scale; <= 0 selects 1/sqrt(d)
+ *   causal    1: token i sees t <= i (prefill); 0: every token sees all T
+ *   out       fp16 [B, T, Hq, d], 16-byte aligned
+ * T == 0 or B == 0 is a no-op.
+ */
+int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void* k_s, const uint8_t* v_q,
+                        const void* v_s, int64_t B, int64_t Hq, int64_t Hkv, int64_t d, int64_t T,
+                        int64_t T_max, float sm_scale, int causal, void* out, void* stream);
+
+/*
  * quarot_kv_write_asym -- quarot_kv_write with the pages' own KV quantizer:
  * asymmetric per group of 128 with a zero point and a clipping ratio.
  * [S] Stage 2c "KV Cache Quantization (online, per-group asymmetric)": group

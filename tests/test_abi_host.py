@@ -114,6 +114,23 @@ def test_kv_asym_validation(lib):
     assert a(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 30, 8, 128, 16, 16, 0.0, 0, FAKE, FAKE, 1 << 20, None) == 1
 
 
+def test_prefill_validation(lib):
+    f = lib.quarot_prefill_attn
+    args = [FAKE] * 5
+    assert f(*args, 0, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 0  # B = 0 no-op
+    assert f(*args, 1, 32, 8, 128, 0, 16, 0.0, 1, FAKE, None) == 0  # T = 0 no-op
+    assert f(*args, 1, 32, 8, 64, 16, 16, 0.0, 1, FAKE, None) == 2  # d
+    assert f(*args, 1, 48, 4, 128, 16, 16, 0.0, 1, FAKE, None) == 2  # group of 12
+    assert f(*args, 1, 30, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 1  # Hq % Hkv
+    assert f(*args, 1, 32, 8, 128, 17, 16, 0.0, 1, FAKE, None) == 1  # T > T_max
+    assert f(*args, 1, 32, 8, 128, 16, 16, 0.0, 2, FAKE, None) == 1  # causal flag
+    assert f(*args, -1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 1
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 1  # no v_q
+    assert f(FAKE, P(0x10008), FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 3  # k_q % 16
+    assert f(P(0x10004), FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 3  # q % 8
+    assert f(*args, 1, 32, 8, 128, 16, 16, 0.0, 1, P(0x10008), None) == 3  # out % 16
+
+
 def test_crosshead_validation(lib):
     f = lib.quarot_crosshead_rotate_quant
     assert f(FAKE, 0, 32, 128, 4096, 1.0, FAKE, FAKE, None, None) == 0  # M = 0 no-op

@@ -337,6 +337,85 @@ def test_kv4_config_full(q):
         assert O.rel_fro(out[b:b + 1], ref) <= OUT_TOL
 
 
+# ---------------------------------------------------------------- prefill "Init" attention (next row f4)
+def _prefill_case(B, T, Hkv, G, seed, T_max=None):
+    k = W.kv_tensors(B, T, Hkv, 128, 2, 20.0, seed)
+    v = W.kv_tensors(B, T, Hkv, 128, 2, 20.0, seed + 1)
+    qq = W.prefill_query(B, T, Hkv * G, 128, seed + 2)
+    oc = _caches(k.shape, T_max or T)
+    O.kv_write(k, v, 0, *oc)
+    return qq, oc
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", [1, 100, 128, 300, 520])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_parity(q, G, T, causal):
+    qq, oc = _prefill_case(2, T, 2, G, 51 + T + G)
+    out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc], causal=causal)
+    q.quarot_check_error()
+    ref = O.prefill_attn(qq, *oc, T=T, causal=causal)
+    assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+    # every query row on its own, against the typical output norm of its head
+    # (fp16 rounding of v^ and p is relative to the values, not to a row whose
+    # terms cancel)
+    o = out.cpu().numpy().astype(np.float64)
+    num = np.sqrt(((o - ref) ** 2).sum(axis=-1))  # [B, T, Hq]
+    den = np.sqrt((ref ** 2).sum(axis=-1))
+    typ = np.sqrt((den ** 2).mean(axis=1, keepdims=True))
+    assert np.all(num <= 4 * OUT_TOL * np.maximum(den, typ))
+
+
+def test_prefill_ignores_cache_past_T(q):
+    """Tokens T .. T_max-1 of the cache hold garbage codes and inf/nan scales;
+    the prompt attends to tokens < T only."""
+    B, T, T_max, Hkv, G = 1, 200, 384, 2, 4
+    qq, oc = _prefill_case(B, T, Hkv, G, 61, T_max=T_max)
+    rng = np.random.default_rng(62)
+    for c in (oc[0], oc[2]):
+        c[:, :, T:] = rng.integers(0, 256, c[:, :, T:].shape, dtype=np.uint8)
+    for s in (oc[1], oc[3]):
+        s[:, :, T:] = np.array([np.inf, np.nan, 60000.0], np.float16)[rng.integers(0, 3, s[:, :, T:].shape)]
+    for causal in (True, False):
+        out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc], causal=causal)
+        ref = O.prefill_attn(qq, *oc, T=T, causal=causal)
+        assert np.isfinite(out.cpu().numpy()).all()
+        assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+
+
+def test_prefill_custom_scale_and_empty(q):
+    qq, oc = _prefill_case(1, 150, 2, 4, 71)
+    out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc], sm_scale=0.05)
+    assert O.rel_fro(out.cpu().numpy(), O.prefill_attn(qq, *oc, T=150, sm_scale=0.05)) <= OUT_TOL
+    e = q.quarot_prefill_attn(_t(qq[:, :0]), *[_t(c) for c in oc])
+    assert e.shape == (1, 0, 8, 128)
+
+
+def test_prefill_last_row_is_decode(q):
+    """The causal prefill's last row and the decode kernel answer the same question."""
+    qq, oc = _prefill_case(2, 333, 2, 4, 81)
+    g = [_t(c) for c in oc]
+    out = q.quarot_prefill_attn(_t(qq), *g)
+    dec = q.quarot_decode_attn(_t(np.ascontiguousarray(qq[:, -1])), *g, T=333)
+    assert O.rel_fro(out[:, -1].cpu().numpy(), dec.cpu().numpy().astype(np.float64)) <= 2 * OUT_TOL
+
+
+def test_prefill_config_full(q):
+    """B4 x T2048 x Hq32/Hkv8 at full size, over a cache the oracle wrote (the
+    append kernel is pinned on its own); oracle on the first and last prompt
+    (all heads, all rows)."""
+    k, v, qq = W.prefill_inputs("prefill")
+    B, T, Hkv, d = k.shape
+    oc = _caches(k.shape, T)
+    O.kv_write(k, v, 0, *oc)
+    out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc])
+    q.quarot_check_error()
+    out = out.cpu().numpy()
+    for b in (0, B - 1):
+        ref = O.prefill_attn(qq[b:b + 1], *[c[b:b + 1] for c in oc], T=T)
+        assert O.rel_fro(out[b:b + 1], ref) <= OUT_TOL
+
+
 # ---------------------------------------------------------------- asymmetric KV (next row f1)
 def _caches_asym(shape_like, T_max):
     B, _, H, d = shape_like

@@ -43,6 +43,8 @@ _SIGS = {
                                           ctypes.c_float, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
     "quarot_decode_attn_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                                  ctypes.c_float, ctypes.c_int, _P, _P]),
+    "quarot_prefill_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                           ctypes.c_float, ctypes.c_int, _P, _P]),
     "quarot_kv_write_asym": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P,
                                             _P, _P, _P, _P]),
     "quarot_decode_attn_asym": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
@@ -274,6 +276,27 @@ def quarot_decode_attn_static(q, k_q, k_s, v_q, v_s, T: int, sm_scale: float = 0
                                           int(T), T_max, float(sm_scale), int(bool(unrotate_out)), _ptr(out),
                                           _stream(stream, dev))
     _check(st, "quarot_decode_attn_static")
+    return out
+
+
+def quarot_prefill_attn(q, k_q, k_s, v_q, v_s, sm_scale: float = 0.0, causal: bool = True, out=None,
+                        stream=None):
+    """Prompt queries q fp16 [B, T, Hq, d] against cached tokens 0 .. T-1
+    ("Init") -> out fp16 [B, T, Hq, d] in the rotated basis."""
+    _need(q, torch.float16, "q")
+    dev = q.device
+    for t, n in ((k_q, "k_q"), (v_q, "v_q")):
+        _need(t, torch.uint8, n, dev)
+    for t, n in ((k_s, "k_s"), (v_s, "v_s")):
+        _need(t, torch.float16, n, dev)
+    B, T, Hq, d = q.shape
+    Hkv, T_max = k_q.shape[1], k_q.shape[2]
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.float16, device=dev)
+    _need(out, torch.float16, "out", dev)
+    st = load().quarot_prefill_attn(_ptr(q), _ptr(k_q), _ptr(k_s), _ptr(v_q), _ptr(v_s), B, Hq, Hkv, d, T, T_max,
+                                    float(sm_scale), int(bool(causal)), _ptr(out), _stream(stream, dev))
+    _check(st, "quarot_prefill_attn")
     return out
 
 

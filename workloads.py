@@ -83,6 +83,11 @@ def query(B: int, Hq: int, d: int, seed: int) -> np.ndarray:
     return _rng(seed).standard_normal((B, Hq, d), dtype=np.float32).astype(np.float16)
 
 
+def prefill_query(B: int, T: int, Hq: int, d: int, seed: int) -> np.ndarray:
+    """fp16 [B, T, Hq, d] prompt queries with N(0,1) entries."""
+    return _rng(seed).standard_normal((B, T, Hq, d), dtype=np.float32).astype(np.float16)
+
+
 # ---------------------------------------------------------------------------
 # The five workloads.  Index i uses seeds SEED_BASE + i + offset.
 # ---------------------------------------------------------------------------
@@ -93,6 +98,9 @@ CONFIGS = {
     "sweep": dict(index=3, kind="sweep", Ms=(512, 2048, 8192), K=4096, Ns=(4096, 12288),
                   n_outlier=8, factor=100.0),
     "kv4": dict(index=4, kind="kv", B=16, T=4096, Hkv=8, Hq=32, d=128, n_outlier=2, factor=20.0),
+    # Init (prefill) attention over the same cache shape: 4 prompts of 2048
+    # tokens (the pages' prefill length), 32 query / 8 KV heads, head_dim 128
+    "prefill": dict(index=5, kind="prefill", B=4, T=2048, Hkv=8, Hq=32, d=128, n_outlier=2, factor=20.0),
 }
 
 
@@ -128,4 +136,15 @@ def kv_inputs(config: str = "kv4", B: int | None = None, T: int | None = None):
     k = kv_tensors(B, T, c["Hkv"], c["d"], c["n_outlier"], c["factor"], seed_of(config, OFF_K))
     v = kv_tensors(B, T, c["Hkv"], c["d"], c["n_outlier"], c["factor"], seed_of(config, OFF_V))
     q = query(B, c["Hq"], c["d"], seed_of(config, OFF_Q))
+    return k, v, q
+
+
+def prefill_inputs(config: str = "prefill", B: int | None = None, T: int | None = None):
+    """(k, v fp16 [B,T,Hkv,d], q fp16 [B,T,Hq,d]) for the prefill attention config."""
+    c = CONFIGS[config]
+    B = B if B is not None else c["B"]
+    T = T if T is not None else c["T"]
+    k = kv_tensors(B, T, c["Hkv"], c["d"], c["n_outlier"], c["factor"], seed_of(config, OFF_K))
+    v = kv_tensors(B, T, c["Hkv"], c["d"], c["n_outlier"], c["factor"], seed_of(config, OFF_V))
+    q = prefill_query(B, T, c["Hq"], c["d"], seed_of(config, OFF_Q))
     return k, v, q
