@@ -225,7 +225,7 @@ int quarot_decode_attn(const void* q, const uint8_t* k_q, const void* k_s, const
  * the probabilities are fp16 (the pages' fp16 flash attention); products
  * accumulate in fp32 on the tensor cores; softmax is fp32.
  *
- *   q         fp16 [B, T, Hq, d] (prompt tokens 0 .. T-1), 8-byte aligned
+ *   q         fp16 [B, T, Hq, d] (prompt tokens 0 .. T-1), 16-byte aligned
  *   k_q, k_s, v_q, v_s  caches as written by quarot_kv_write (capacity
  *             T_max >= T, tokens 0 .. T-1 written); k_q, v_q 16-byte aligned
  *   d         128; Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}

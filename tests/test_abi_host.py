@@ -127,7 +127,7 @@ def test_prefill_validation(lib):
     assert f(*args, -1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 1
     assert f(FAKE, FAKE, FAKE, None, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 1  # no v_q
     assert f(FAKE, P(0x10008), FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 3  # k_q % 16
-    assert f(P(0x10004), FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 3  # q % 8
+    assert f(P(0x10004), FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 128, 16, 16, 0.0, 1, FAKE, None) == 3  # q % 16
     assert f(*args, 1, 32, 8, 128, 16, 16, 0.0, 1, P(0x10008), None) == 3  # out % 16
 
 

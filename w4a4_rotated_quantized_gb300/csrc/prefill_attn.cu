@@ -28,7 +28,7 @@
 // P(i) overwrite the first 64 columns of their score buffer and are the A
 // operand of O += P V (kind::f16, A from tensor memory).
 //   warp 0      producer: the packed K/V codes of 128 keys by bulk copies,
-//               their scales by plain loads, into a 2-stage ring
+//               their scales by plain loads, into a 4-stage ring
 //   warp 1      tensor memory allocator and single-thread MMA issuer
 //   warps 2-5   converters: key codes -> exact fp16 codes, value codes ->
 //               fp16 code * scale, in the 128-byte swizzled K-major layout
@@ -51,7 +51,7 @@ namespace prefill {
 constexpr int HD = 128;    // head dim
 constexpr int BQ = 128;    // query tokens per CTA (tensor memory lanes)
 constexpr int BKV = 128;   // keys per tile
-constexpr int SP = 2;      // packed stages
+constexpr int SP = 4;      // packed stages
 constexpr int SK = 2;      // converted key stages
 constexpr int SV = 2;      // converted value stages
 constexpr int NCW = 4;     // converter warps
@@ -145,6 +145,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -329,10 +334,10 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       }
       for (int i = 0; ok && i < nkt; ++i) {
         if (i + 1 < nkt) {
-          // buffer (i+1) % 2 held P(i-1): O += P(i-1) V must have finished
-          if (!mbar_wait_bounded(&k_full[(i + 1) % SK], uint32_t(((i + 1) / SK) & 1), abort_flag) ||
-              (i >= 1 && !mbar_wait_bounded(o_done, uint32_t((i - 1) & 1), abort_flag)))
-            break;
+          // buffer (i+1) % 2 held P(i-1), the A operand of O += P(i-1) V,
+          // issued before: the tensor pipe runs one thread's MMAs in issue
+          // order, so S(i+1) overwrites it only after that product read it
+          if (!mbar_wait_bounded(&k_full[(i + 1) % SK], uint32_t(((i + 1) / SK) & 1), abort_flag)) break;
           fence_after();
           issue_s(i + 1);
         }
@@ -367,15 +372,25 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       const uint32_t* vss2 = reinterpret_cast<const uint32_t*>(kss + BKV);  // value scales in pairs
       // keys: task (token t, word w) -> 16 bytes (dims 8w .. 8w+7) of row t,
       // exact codes; the lanes of one load cover 16 words x 2 tokens (all 32
-      // banks), the 8 lanes of a quarter warp store 8 distinct 16-byte chunks
+      // banks), the 8 lanes of a quarter warp store 8 distinct 16-byte chunks.
+      // Four words per step are loaded before any of their stores (the stores
+      // may alias the loads as far as the compiler knows); the loop stays
+      // rolled so the converters' code shares the instruction cache with the
+      // softmax's.
       unsigned char* kdst = sm + OFF_KV + 2 * kst * TILE16;
-#pragma unroll 4
-      for (int it = 0; it < BKV / 8; ++it) {
-        const int t = 2 * (cw + 4 * it) + half;
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(st + t * (HD / 2) + 4 * w);
-        *reinterpret_cast<uint4*>(kdst + (w >> 3) * 16384 + t * 128 + (((w & 7) ^ (t & 7)) << 4)) =
-            make_uint4(codes_of_byte(word, 0), codes_of_byte(word, 1), codes_of_byte(word, 2),
-                       codes_of_byte(word, 3));
+#pragma unroll 1
+      for (int it0 = 0; it0 < BKV / 8; it0 += 4) {
+        uint32_t words[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          words[u] = *reinterpret_cast<const uint32_t*>(st + (2 * (cw + 4 * (it0 + u)) + half) * (HD / 2) + 4 * w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = 2 * (cw + 4 * (it0 + u)) + half;
+          *reinterpret_cast<uint4*>(kdst + (w >> 3) * 16384 + t * 128 + (((w & 7) ^ (t & 7)) << 4)) =
+              make_uint4(codes_of_byte(words[u], 0), codes_of_byte(words[u], 1), codes_of_byte(words[u], 2),
+                         codes_of_byte(words[u], 3));
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -397,13 +412,11 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       const unsigned char* vsrc = st + PK_CODES;
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
-        const int delta = cw + 4 * pass;
-        const int c = ((w + delta) & 7) + 8 * half;
-        uint32_t W[8];
+        const int c = ((w + cw + 4 * pass) & 7) + 8 * half;
+        uint32_t W[8], s2[4];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
           W[jj] = *reinterpret_cast<const uint32_t*>(vsrc + (8 * c + jj) * (HD / 2) + 4 * w);
-        uint32_t s2[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) s2[u] = vss2[4 * c + u];
         unsigned char* cbase = vdst + (c >> 3) * 16384;
@@ -438,18 +451,18 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
     // lanes (natural-order FWHT: lower index a + b, upper a - b).  Rows go to
     // an fp32 staging area, 16-byte chunk m of row r at chunk m ^ (r & 7).
     float* qs = reinterpret_cast<float*>(sm + OFF_QS);
+    uint2 raw[32];  // all 32 rows' loads in flight at once
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) {
+      const int tok = q0 + 32 * qd + rr;
+      raw[rr] = tok < T ? __ldg(reinterpret_cast<const uint2*>(q + ((int64_t(b) * T + tok) * Hq + h) * HD + 4 * lane))
+                        : make_uint2(0u, 0u);
+    }
+#pragma unroll
     for (int rr = 0; rr < 32; ++rr) {
       const int row = 32 * qd + rr;
-      const int tok = q0 + row;
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (tok < T) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(q + ((int64_t(b) * T + tok) * Hq + h) * HD + 4 * lane);
-        const float2 a01 = h2_to_f2(raw.x), a23 = h2_to_f2(raw.y);
-        x[0] = a01.x;
-        x[1] = a01.y;
-        x[2] = a23.x;
-        x[3] = a23.y;
-      }
+      const float2 a01 = h2_to_f2(raw[rr].x), a23 = h2_to_f2(raw[rr].y);
+      float x[4] = {a01.x, a01.y, a23.x, a23.y};
       float u0 = x[0], u1 = x[1];
       x[0] = u0 + u1;
       x[1] = u0 - u1;
@@ -530,19 +543,27 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
         wait_ld();
         // scores in log2 units: the fp32 product times the key's scale
 #pragma unroll
-        for (int e4 = 0; e4 < 32; ++e4) {
-          float kk[4];
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(kk[0]), "=f"(kk[1]), "=f"(kk[2]), "=f"(kk[3])
-                       : "r"(kf_s + 16u * e4));
+        for (int e8 = 0; e8 < 16; ++e8) {
+          // 8 scales per batch: two loads in flight, then their 8 products
+          float kk[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) v[4 * e4 + u] = __float_as_uint(__uint_as_float(v[4 * e4 + u]) * kk[u]);
+          for (int j = 0; j < 2; ++j)
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(kk[4 * j]), "=f"(kk[4 * j + 1]), "=f"(kk[4 * j + 2]), "=f"(kk[4 * j + 3])
+                         : "r"(kf_s + 32u * e8 + 16u * j));
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[8 * e8 + u] = __float_as_uint(__uint_as_float(v[8 * e8 + u]) * kk[u]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ks_empty[sb]);
-        float mx = __uint_as_float(v[0]);
+        float mp[8];
 #pragma unroll
-        for (int e = 1; e < 128; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        for (int j = 0; j < 8; ++j) mp[j] = __uint_as_float(v[j]);
+#pragma unroll
+        for (int e = 8; e < 128; e += 16)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mp[j] = max3f(mp[j], __uint_as_float(v[e + j]), __uint_as_float(v[e + 8 + j]));
+        const float mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
         // ---- lazy rescale: raise the running max only when the tile exceeds
         // it by more than 8 (log2 units); otherwise p <= 2^8
         raise = mx > m_run + 8.0f;
@@ -552,13 +573,15 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
           m_run = mx;
         }
         // ---- p = 2^(s - m) -> fp16 pairs into columns [0, 64) of the buffer
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 128; e += 2) {
           const float p0 = ex2(__uint_as_float(v[e]) - m_run);
           const float p1 = ex2(__uint_as_float(v[e + 1]) - m_run);
-          l_run += p0 + p1;
+          ls[(e >> 1) & 3] += p0 + p1;
           v[e >> 1] = pack_f2h2(p0, p1);
         }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st32(s_t, v);
         tmem_st32(s_t + 32, v + 32);
       } else {
@@ -673,7 +696,7 @@ extern "C" int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void
   if (B > 65535 || Hq > 1024 || T > (1 << 24) || T_max > (int64_t(1) << 30)) return QUAROT_ERR_UNSUPPORTED;
   if (q == nullptr || k_q == nullptr || k_s == nullptr || v_q == nullptr || v_s == nullptr || out == nullptr)
     return QUAROT_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(q) & 7) || (reinterpret_cast<uintptr_t>(k_q) & 15) ||
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(k_q) & 15) ||
       (reinterpret_cast<uintptr_t>(v_q) & 15) || (reinterpret_cast<uintptr_t>(k_s) & 1) ||
       (reinterpret_cast<uintptr_t>(v_s) & 1) || (reinterpret_cast<uintptr_t>(out) & 15))
     return QUAROT_ERR_ALIGNMENT;
