@@ -29,6 +29,9 @@ Sources (page title, section):
 Readings where the pages are silent or disagree (each also listed in the
 design notes):
   * rotation is x~ = (x * s) @ H / sqrt(d), row-vector convention, signs first;
+  * FP16 rotation variant: scale by fp16(1/sqrt(d)) first, then butterflies of
+    span 1, 2, ..., P/2 and (for 12 * 2^n) the Paley-12 sums in index order,
+    every result rounded to fp16;
   * H_12288 = H12 (+) H1024 (Kronecker, index k = a*1024 + b), H12 = Paley I
     with q = 11: Jacobsthal Q_ij = chi(j - i), S = [[0, 1^T], [-1, Q]], H = I + S;
   * activation scale S = max(clip * max|x~|, 1e-5) / 7, stored as fp16
@@ -216,6 +219,70 @@ def rotate_quant(x: np.ndarray, signs: np.ndarray | None, clip_ratio: float = 1.
     Transformation": W~ = W H^T, one scale per output row).
     """
     r = rotate(x, signs)
+    q, S = quantize_rows(r, clip_ratio)
+    return pack_int4(q), S, r
+
+
+# ---------------------------------------------------------------------------
+# FP16 online Hadamard ([S] "Kernel Implementation and Hardware Efficiency",
+# online Hadamard transforms: FP32 arithmetic is the default, FP16 arithmetic
+# the tested alternative with nearly identical accuracy, Appendix A.7 /
+# Table 10)
+# ---------------------------------------------------------------------------
+def _f16(a) -> np.ndarray:
+    """Round to the nearest fp16 value (ties to even), returned as float64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def rotate_fp16_arith(x: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
+    """The rotation x~ = (x * s) @ H_d / sqrt(d) computed in fp16 arithmetic.
+
+    The pages name the variant but not its operation order; this library's
+    reading (every step rounds to fp16, round-to-nearest-even):
+      1. y = fp16(s * x * c) with c = fp16(1 / sqrt(d)) (the scaling comes first
+         so no intermediate exceeds the row's l1 norm times c);
+      2. the Sylvester part, d = NA * P with P a power of two: butterflies of
+         span h = 1, 2, 4, ..., P/2 within each length-P segment, pairing
+         indices i and i + h (i & h == 0) into (fp16(a + b), fp16(a - b));
+      3. for d = 12 P, the Paley-12 part across the segments: for each column
+         c and in-segment index j, acc = 0 then acc = fp16(acc + H12[a, c] *
+         y[a P + j]) for a = 0, 1, ..., 11.
+    Returns float64 [..., d] holding the fp16 values.
+    """
+    x = np.asarray(x)
+    d = x.shape[-1]
+    na = 12 if (d % 12 == 0 and (d // 12) & (d // 12 - 1) == 0) else 1
+    P = d // na
+    if P < 1 or P & (P - 1):
+        raise ValueError(f"no Hadamard construction for d = {d} (need 2^n or 12*2^n)")
+    xs = x.reshape(-1, d).astype(np.float64)
+    if signs is not None:
+        xs = xs * np.asarray(signs, dtype=np.float64)[None, :]
+    c = float(np.float16(1.0 / math.sqrt(d)))
+    y = _f16(xs * c).reshape(-1, na, P)
+    h = 1
+    while h < P:
+        v = y.reshape(y.shape[0], na, P // (2 * h), 2, h)
+        a, b = v[:, :, :, 0, :], v[:, :, :, 1, :]
+        y = np.stack([_f16(a + b), _f16(a - b)], axis=3).reshape(y.shape[0], na, P)
+        h *= 2
+    if na == 12:
+        H12 = paley12().astype(np.float64)
+        out = np.empty_like(y)
+        for col in range(12):
+            acc = np.zeros((y.shape[0], P))
+            for a in range(12):
+                acc = _f16(acc + H12[a, col] * y[:, a, :])
+            out[:, col, :] = acc
+        y = out
+    return y.reshape(x.shape)
+
+
+def rotate_quant_fp16(x: np.ndarray, signs: np.ndarray | None, clip_ratio: float = 1.0):
+    """The FP16-arithmetic rotation followed by the same per-row INT4
+    quantize-and-pack as ``rotate_quant``.  Returns (packed, scale fp16, rotated
+    fp32 holding fp16 values)."""
+    r = rotate_fp16_arith(x, signs).astype(np.float32)
     q, S = quantize_rows(r, clip_ratio)
     return pack_int4(q), S, r
 

@@ -490,6 +490,95 @@ def test_decode_brute_force_tiny():
         assert np.allclose(out[0, h], o_un, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- FP16 online Hadamard (next row f4)
+def test_fp16_hadamard_worked_example(golden):
+    g = golden("fp16_hadamard_worked.txt")
+    x = np.array([[float(v) for v in g["x"]]], dtype=np.float16)
+    r = O.rotate_fp16_arith(x, None)
+    assert np.array_equal(r[0], [float(v) for v in g["rot16"]])
+    assert np.array_equal(O.rotate_f64(x, None)[0], [float(v) for v in g["exact"]])
+    packed, S, rr = O.rotate_quant_fp16(x, None)
+    assert float(S[0]) == float(g["scale"][0])
+    assert O.quantize_rows(rr)[0][0].tolist() == [int(v) for v in g["codes"]]
+    assert packed[0].tolist() == [int(v) for v in g["packed"]]
+
+
+def test_fp16_hadamard_exact_when_representable():
+    # small integers scaled by 1/4: every partial sum is an integer / 4 below 2^10
+    rng = np.random.default_rng(31)
+    x = (4 * rng.integers(-3, 4, (5, 16))).astype(np.float16)
+    s = W.random_signs(16, 32)
+    assert np.array_equal(O.rotate_fp16_arith(x, s), O.rotate_f64(x, s))
+
+
+@pytest.mark.parametrize("d", [256, 4096, 3072])
+def test_fp16_hadamard_error_bound(d):
+    # after the fp16 scaling by c the row norm is |x| c sqrt(d) ~ |x|; each
+    # butterfly stage is sqrt(2) times an orthogonal map plus a rounding of at
+    # most u = 2^-11 relative per element, so ||r16 - r|| <= (log2 P + 2) u ||x||
+    # (one more u for c itself); the Paley stage's 12 sequential sums add at
+    # most 11 u sqrt(12) ||x||
+    x, _, s = W.layer_inputs("rotq4096")
+    x = x[:64, :d]
+    s = s[:d]
+    r16 = O.rotate_fp16_arith(x, s)
+    r = O.rotate_f64(x, s)
+    na = 12 if d % 12 == 0 else 1
+    L = int(math.log2(d // na))
+    u = 2.0 ** -11
+    bound = (L + 2) * u + (11 * math.sqrt(12) * u if na == 12 else 0.0)
+    err = np.linalg.norm(r16 - r, axis=1)
+    nx = np.linalg.norm(x.astype(np.float64), axis=1)
+    assert np.all(err <= bound * nx)
+    # and it really is fp16 arithmetic, far above fp32 round-off
+    assert np.median(err / nx) > 1e-5
+
+
+def test_fp16_hadamard_brute_force_d8():
+    # independent fp16 rounding through the IEEE binary16 codec of struct
+    import struct
+
+    def r16(v):
+        return struct.unpack("<e", struct.pack("<e", v))[0]
+
+    rng = np.random.default_rng(33)
+    d = 8
+    for _ in range(20):
+        x = rng.standard_normal(d).astype(np.float16) * np.float16(300)
+        s = rng.choice([-1, 1], d).astype(np.int8)
+        c = r16(1.0 / math.sqrt(d))
+        v = [r16(float(x[i]) * float(s[i]) * c) for i in range(d)]
+        h = 1
+        while h < d:
+            for i in range(d):
+                if i & h == 0:
+                    a, b = v[i], v[i + h]
+                    v[i], v[i + h] = r16(a + b), r16(a - b)
+            h *= 2
+        assert np.array_equal(O.rotate_fp16_arith(x[None, :], s)[0], v)
+
+
+def test_fp16_hadamard_paley_sequence_d12():
+    # d = 12 (P = 1): only the Paley-12 sums, accumulated in index order
+    import struct
+
+    def r16(v):
+        return struct.unpack("<e", struct.pack("<e", v))[0]
+
+    rng = np.random.default_rng(34)
+    x = (rng.standard_normal(12) * 1000).astype(np.float16)
+    c = r16(1.0 / math.sqrt(12))
+    y = [r16(float(v) * c) for v in x]
+    H = O.paley12()
+    want = []
+    for col in range(12):
+        acc = 0.0
+        for a in range(12):
+            acc = r16(acc + int(H[a, col]) * y[a])
+        want.append(acc)
+    assert np.array_equal(O.rotate_fp16_arith(x[None, :], None)[0], want)
+
+
 # ---------------------------------------------------------------- prefill attention (next row f4)
 def _prefill_case(B, T, Hkv, G, d, seed):
     k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, seed)
