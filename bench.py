@@ -435,6 +435,10 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     nbytes = M * d * 2 + M * d // 2 + M * 2
     res["rmsnorm_rotate_quant_2048x12288"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
                                               "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
+    # the FP16-arithmetic rotation variant on the same 2048 x 12288 rows
+    ms = timed(lambda: q.quarot_rotate_quant_fp16(xt, st, q_out=qo, scale_out=so, stream=stream))
+    res["rotate_quant_fp16_2048x12288"] = {"ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                           "frac_hbm": nbytes / (ms / 1e3) / 1e9 / hbm_peak}
     del xt, qo, so
     # cross-head Hadamard + INT4 of a prefill-sized attention output (2048 tokens x 32 heads x 128)
     zt = torch.from_numpy(W.query(2048, 32, 128, 77).reshape(2048, 4096)).to(dev)

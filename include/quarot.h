@@ -91,6 +91,26 @@ int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, const
                         void* stream);
 
 /*
+ * quarot_rotate_quant_fp16 -- quarot_rotate_quant with the rotation carried
+ * out in fp16 arithmetic.  [S] "Kernel Implementation and Hardware
+ * Efficiency", online Hadamard transforms: FP32 arithmetic is the default and
+ * FP16 the tested alternative with nearly identical accuracy (Appendix A.7,
+ * Table 10).  The pages fix no operation order; this library's:
+ *   y = fp16(s * x * fp16(1/sqrt(d)))
+ *   butterflies of span 1, 2, ..., P/2 (P the power-of-two factor of d),
+ *   pairing i and i + h (i & h == 0) into (fp16(a + b), fp16(a - b))
+ *   for d = 12 P: out[c P + j] = fp16 running sum over a = 0 .. 11 of
+ *   H12[a][c] * y[a P + j], rounded after every term
+ * then the quantizer of quarot_rotate_quant on the fp16 values (rot_out
+ * receives them).  The sums stay below sqrt(d) max|x|, so inputs above
+ * 65504 / sqrt(d) in magnitude may overflow to inf.  Arguments, widths and
+ * errors as quarot_rotate_quant.
+ */
+int quarot_rotate_quant_fp16(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                             float clip_ratio, uint8_t* q_out, void* scale_out, float* rot_out,
+                             void* stream);
+
+/*
  * quarot_rmsnorm_rotate_quant -- quarot_rotate_quant preceded by a scale-free
  * RMSNorm of each row, fused in the same kernel.  [G] "Deep Dive: The
  * End-to-End QuaRot Layer Lifecycle", 2 "Online Activation Rotation Fused into

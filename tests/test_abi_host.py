@@ -61,6 +61,17 @@ def test_rotate_quant_validation(lib):
     assert f(FAKE, 4, 4104, 4104, None, 1.0, FAKE, FAKE, None, None) == 2  # no construction
 
 
+def test_rotate_quant_fp16_validation(lib):
+    f = lib.quarot_rotate_quant_fp16
+    assert f(FAKE, 0, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 0  # M = 0 no-op
+    assert f(FAKE, 4, 24, 24, None, 1.0, FAKE, FAKE, None, None) == 2  # no construction for 24
+    assert f(FAKE, 4, 4096, 4000, None, 1.0, FAKE, FAKE, None, None) == 1  # ld < d
+    assert f(FAKE, 4, 4096, 4096, None, 0.0, FAKE, FAKE, None, None) == 1  # clip
+    assert f(None, 4, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(P(0x10002), 4, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 3  # misaligned x
+    assert f(FAKE, 4, 4096, 4100, None, 1.0, FAKE, FAKE, None, None) == 3  # ld % 8
+
+
 def test_rmsnorm_rotate_quant_validation(lib):
     f = lib.quarot_rmsnorm_rotate_quant
     assert f(FAKE, 0, 4096, 4096, 1e-6, None, 1.0, FAKE, FAKE, None, None) == 0  # M = 0 no-op

@@ -128,6 +128,46 @@ def test_rotate_quant_config_down_proj_sampled(q):
 
 
 # ---------------------------------------------------------------- fused RMSNorm + rotate + quant
+# ---------------------------------------------------------------- FP16 online Hadamard (next row f4)
+def _check_fp16_rotation(q, x, s, clip=1.0):
+    gq, gs, grot = q.quarot_rotate_quant_fp16(_t(x), None if s is None else _t(s), clip_ratio=clip, want_rot=True)
+    gq, gs, grot = gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy()
+    r16 = O.rotate_fp16_arith(x, s).astype(np.float32)
+    # every step is a correctly rounded fp16 operation in the same order:
+    # the rotated values are bit-identical
+    assert np.array_equal(grot, r16)
+    check_quant(gq, gs, grot, r16, clip)
+    return grot
+
+
+@pytest.mark.parametrize("d", [16, 128, 256, 1024, 2048, 4096, 8192, 3072, 6144, 12288])
+def test_rotate_quant_fp16_widths(q, d):
+    M = 37  # ragged: not a multiple of the rows per CTA
+    x = W.activations(M, d, W.outlier_channels(d, max(1, d // 512), 5 + d), 100.0, 11 + d)
+    _check_fp16_rotation(q, x, W.random_signs(d, 21 + d))
+
+
+def test_rotate_quant_fp16_no_signs_clip_and_close_to_fp32(q):
+    x, _, s = W.layer_inputs("rotq4096", M=64)
+    _check_fp16_rotation(q, x, None, clip=0.9)
+    # the variant's rotation stays within its error bound of the exact one:
+    # (log2 4096 + 2) * 2^-11 * |x|
+    grot = _check_fp16_rotation(q, x, s)
+    err = np.linalg.norm(grot.astype(np.float64) - O.rotate_f64(x, s), axis=1)
+    assert np.all(err <= 14 * 2.0 ** -11 * np.linalg.norm(x.astype(np.float64), axis=1))
+
+
+def test_rotate_quant_fp16_down_proj_full(q):
+    """The 2048 x 12288 down_proj activations at full size, rows sampled by the oracle."""
+    x, _, s = W.layer_inputs("down_proj", N=0)
+    gq, gs, grot = q.quarot_rotate_quant_fp16(_t(x), _t(s), want_rot=True)
+    rows = [0, 1, 777, 2047]
+    r16 = O.rotate_fp16_arith(x[rows], s).astype(np.float32)
+    grot = grot.cpu().numpy()[rows]
+    assert np.array_equal(grot, r16)
+    check_quant(gq.cpu().numpy()[rows], gs.cpu().numpy()[rows], grot, r16)
+
+
 @pytest.mark.parametrize("d", [16, 256, 1024, 3072, 4096, 8192, 12288])
 def test_rmsnorm_rotate_quant_widths(q, d):
     M = 37

@@ -33,6 +33,7 @@ _SIGS = {
     "quarot_version": (ctypes.c_int, []),
     "quarot_check_error": (ctypes.c_int, [_P]),
     "quarot_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "quarot_rotate_quant_fp16": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_rmsnorm_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, ctypes.c_float, _P, ctypes.c_float, _P, _P,
                                                    _P, _P]),
     "quarot_crosshead_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P, _P]),
@@ -182,6 +183,18 @@ def quarot_rotate_quant(x, signs=None, clip_ratio: float = 1.0, q_out=None, scal
     st = load().quarot_rotate_quant(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(q_out),
                                     _ptr(scale_out), _ptr(rot_out), _stream(stream, dev))
     _check(st, "quarot_rotate_quant")
+    return q_out, scale_out, rot_out
+
+
+def quarot_rotate_quant_fp16(x, signs=None, clip_ratio: float = 1.0, q_out=None, scale_out=None, rot_out=None,
+                             stream=None, want_rot: bool = False):
+    """quarot_rotate_quant with the rotation in fp16 arithmetic (the pages'
+    FP16 online-Hadamard variant); rot_out receives the fp16 values as fp32."""
+    q_out, scale_out, rot_out = _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot)
+    M, d = x.shape
+    st = load().quarot_rotate_quant_fp16(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(q_out),
+                                         _ptr(scale_out), _ptr(rot_out), _stream(stream, x.device))
+    _check(st, "quarot_rotate_quant_fp16")
     return q_out, scale_out, rot_out
 
 

@@ -41,8 +41,15 @@ __host__ __device__ constexpr int paley12_entry(int i, int j) {
 
 __device__ __forceinline__ int pad_idx(int i) { return i + 4 * (i >> 7); }
 
-// In-register FWHT of N values (natural order, unnormalized).
-template <int N>
+// Nearest fp16 value (ties to even), kept in fp32.  For two fp16 operands
+// the fp32 sum or product rounded this way equals the fp16 operation
+// (fp32 carries more than 2 * 11 + 2 significand bits, so the double rounding
+// is harmless).
+__device__ __forceinline__ float r16(float x) { return __half2float(__float2half_rn(x)); }
+
+// In-register FWHT of N values (natural order, unnormalized).  H16: the FP16
+// arithmetic variant, every butterfly output rounded to fp16.
+template <int N, bool H16 = false>
 __device__ __forceinline__ void fwht_regs(float* v) {
 #pragma unroll
   for (int h = 1; h < N; h <<= 1) {
@@ -50,8 +57,13 @@ __device__ __forceinline__ void fwht_regs(float* v) {
     for (int i = 0; i < N; ++i) {
       if ((i & h) == 0) {
         const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
+        if constexpr (H16) {
+          v[i] = r16(a + b);
+          v[i + h] = r16(a - b);
+        } else {
+          v[i] = a + b;
+          v[i + h] = a - b;
+        }
       }
     }
   }
@@ -78,11 +90,16 @@ struct RQPlan {
   static_assert(GPT * GROUP <= 64, "final pass register budget");
 };
 
-template <int LOGP, bool M12, bool RMS>
+// H16: the FP16-arithmetic rotation ([S] "Kernel Implementation and Hardware
+// Efficiency": FP32 online Hadamard by default, FP16 as the alternative):
+// y = fp16(s x h16_c) with h16_c = fp16(1/sqrt(d)), then every butterfly and
+// every Paley-12 partial sum (in index order) rounded to fp16.
+template <int LOGP, bool M12, bool RMS, bool H16 = false>
 __global__ void __launch_bounds__(RQPlan<LOGP, M12>::NT)
 rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
                     const int8_t* __restrict__ signs, float clip_ratio, float rms_eps, uint8_t* __restrict__ q_out,
-                    __half* __restrict__ scale_out, float* __restrict__ rot_out) {
+                    __half* __restrict__ scale_out, float* __restrict__ rot_out, float h16_c) {
+  static_assert(!(RMS && H16), "the FP16 variant has no fused RMSNorm");
   using PL = RQPlan<LOGP, M12>;
   constexpr int D = PL::D, P = PL::P, TPR = PL::TPR;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -121,11 +138,15 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
           v[i] = s < 0 ? -v[i] : v[i];
         }
       }
+      if constexpr (H16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = r16(v[i] * h16_c);
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = 0.f;
     }
-    fwht_regs<8>(v);
+    fwht_regs<8, H16>(v);
     float4* dst = reinterpret_cast<float4*>(buf + pad_idx(8 * c));
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
     dst[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -147,7 +168,7 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = buf[pad_idx(base + 8 * j)];
-      fwht_regs<32>(v);
+      fwht_regs<32, H16>(v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) buf[pad_idx(base + 8 * j)] = v[j];
     }
@@ -165,7 +186,7 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
     for (int a = 0; a < NA; ++a) {
 #pragma unroll
       for (int j = 0; j < FJ; ++j) v[g][a][j] = buf[pad_idx(base + (j << FLO) + a * P)];
-      if constexpr (FJ > 1) fwht_regs<FJ>(v[g][a]);
+      if constexpr (FJ > 1) fwht_regs<FJ, H16>(v[g][a]);
     }
     if constexpr (M12) {
 #pragma unroll
@@ -177,7 +198,10 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
         for (int c = 0; c < 12; ++c) {
           float acc = 0.f;
 #pragma unroll
-          for (int a = 0; a < 12; ++a) acc = paley12_entry(a, c) > 0 ? acc + in[a] : acc - in[a];
+          for (int a = 0; a < 12; ++a) {
+            acc = paley12_entry(a, c) > 0 ? acc + in[a] : acc - in[a];
+            if constexpr (H16) acc = r16(acc);
+          }
           out[c] = acc;
         }
 #pragma unroll
@@ -192,7 +216,7 @@ rotate_quant_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x,
   float inv_sqrt_d;
   if constexpr (!M12 && (LOGP % 2 == 0)) inv_sqrt_d = 1.0f / float(1 << (LOGP / 2));
   else inv_sqrt_d = 1.0f / sqrtf(float(D));
-  float post = inv_sqrt_d;
+  float post = H16 ? 1.0f : inv_sqrt_d;  // the FP16 variant scaled on load
   if constexpr (RMS) {
     float tot = sq;
     if constexpr (TPR > 32) {
@@ -585,11 +609,13 @@ static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* si
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
 
-template <int LOGP, bool M12, bool RMS>
+template <int LOGP, bool M12, bool RMS, bool H16 = false>
 static int launch_rq_t(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps,
                      uint8_t* q, void* s, float* rot, cudaStream_t st) {
   using PL = RQPlan<LOGP, M12>;
-  auto kern = rotate_quant_kernel<LOGP, M12, RMS>;
+  auto kern = rotate_quant_kernel<LOGP, M12, RMS, H16>;
+  // fp16(1/sqrt(d)), rounded once from double (used by the FP16 variant)
+  const float h16_c = __half2float(__double2half(1.0 / sqrt(double(PL::D))));
   static bool attr_set = false;  // per-process; sizes are below the opt-in limit
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PL::SMEM)) !=
@@ -600,7 +626,7 @@ static int launch_rq_t(const void* x, int64_t M, int64_t ld_x, const int8_t* sig
   const int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(
-      static_cast<const __half*>(x), M, ld_x, signs, clip, eps, q, static_cast<__half*>(s), rot);
+      static_cast<const __half*>(x), M, ld_x, signs, clip, eps, q, static_cast<__half*>(s), rot, h16_c);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
 
@@ -659,6 +685,37 @@ extern "C" int quarot_rotate_quant(const void* x, int64_t M, int64_t d, int64_t 
                                    const int8_t* signs, float clip_ratio, uint8_t* q_out,
                                    void* scale_out, float* rot_out, void* stream) {
   return rotate_quant_dispatch(x, M, d, ld_x, signs, clip_ratio, -1.0f, q_out, scale_out, rot_out, stream);
+}
+
+extern "C" int quarot_rotate_quant_fp16(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                                        float clip_ratio, uint8_t* q_out, void* scale_out, float* rot_out,
+                                        void* stream) {
+  if (M < 0 || d <= 0 || ld_x < d) return QUAROT_ERR_INVALID_ARG;
+  if (!(clip_ratio > 0.f && clip_ratio <= 1.f)) return QUAROT_ERR_INVALID_ARG;
+  if (M == 0) return QUAROT_OK;
+  if (x == nullptr || q_out == nullptr || scale_out == nullptr) return QUAROT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (ld_x % 8) || (reinterpret_cast<uintptr_t>(q_out) & 15) ||
+      (reinterpret_cast<uintptr_t>(scale_out) & 1) || (signs && (reinterpret_cast<uintptr_t>(signs) & 7)) ||
+      (rot_out && (reinterpret_cast<uintptr_t>(rot_out) & 15)))
+    return QUAROT_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float c = clip_ratio;
+  switch (d) {
+    case 16: return launch_rq_t<4, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 32: return launch_rq_t<5, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 64: return launch_rq_t<6, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 128: return launch_rq_t<7, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 256: return launch_rq_t<8, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 512: return launch_rq_t<9, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 1024: return launch_rq_t<10, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 2048: return launch_rq_t<11, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 4096: return launch_rq_t<12, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 8192: return launch_rq_t<13, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 3072: return launch_rq_t<8, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 6144: return launch_rq_t<9, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 12288: return launch_rq_t<10, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    default: return QUAROT_ERR_UNSUPPORTED;
+  }
 }
 
 extern "C" int quarot_rmsnorm_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, float eps,
