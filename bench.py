@@ -476,6 +476,20 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
     tf = 4.0 * B * Hq * d * (T * (T + 1) / 2) / (ms / 1e3) / 1e12
     res["prefill_attn_4x2048_h32kv8"] = {"ms": ms, "TFLOP/s": tf, "frac_f16_peak": tf / (fp8_peak / 2)}
     del pc, qp, op
+    # rotate+quant of the sweep's activations (M x 4096, 8 outlier channels),
+    # for the layer rate M / (t_rotate_quant + t_gemm) of each sweep shape
+    xs, _, ss = W.layer_inputs("sweep", M=8192)
+    rot_ms = {}
+    sst = torch.from_numpy(ss).to(dev)
+    for M in (512, 2048, 8192):
+        xt = torch.from_numpy(np.ascontiguousarray(xs[:M])).to(dev)
+        qo = torch.empty((M, 2048), dtype=torch.uint8, device=dev)
+        so = torch.empty((M,), dtype=torch.float16, device=dev)
+        rot_ms[M] = timed(lambda: q.quarot_rotate_quant(xt, sst, q_out=qo, scale_out=so, stream=stream))
+        nb = M * 4096 * 2 + M * 2048 + M * 2
+        res[f"rotate_quant_{M}x4096"] = {"ms": rot_ms[M], "GB/s": nb / (rot_ms[M] / 1e3) / 1e9,
+                                         "frac_hbm": nb / (rot_ms[M] / 1e3) / 1e9 / hbm_peak}
+        del xt, qo, so
     g = torch.Generator(device="cpu").manual_seed(1234)
     K = 4096
     for N in (4096, 12288):
@@ -487,7 +501,8 @@ def _other_configs(q, W, dev, stream, flush, hbm_peak, fp8_peak, reps=20):
             y = torch.empty((M, N), dtype=torch.float16, device=dev)
             ms = timed(lambda: q.quarot_w4a4_gemm(aq, as_, wq, ws_, y=y, stream=stream))
             tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
-            res[f"w4a4_gemm_{M}x{K}x{N}"] = {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak}
+            res[f"w4a4_gemm_{M}x{K}x{N}"] = {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak,
+                                               "layer_tokens_per_s": M / ((ms + rot_ms[M]) / 1e3)}
             del aq, as_, y
         del wq, ws_
     return res
