@@ -116,6 +116,25 @@ def _dist():
     return ws, rank, local
 
 
+def _job_time_ms(local_ms: float, ws: int, device) -> float:
+    """The job's time for the timed region: the slowest rank's (every rank
+    enters and leaves the region at a barrier).  One all-reduce (MAX)."""
+    if ws <= 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(tokens_per_rank_step: int, steps: int, ws: int, job_ms: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the job's time
+    (replicas, weak scaling: every rank runs the full per-GPU workload)."""
+    return ws * tokens_per_rank_step * steps / (job_ms / 1000.0)
+
+
 def cpu_oracle_sample(rows: int = 8, seqs: int = 1):
     """Times the oracle on a bounded sample of one step; returns (tokens/s, seconds, description)."""
     import oracle as O
@@ -282,13 +301,10 @@ def run_ours(args):
             torch.cuda.synchronize()
     q.quarot_check_error(stream)
     step_ms = np.array([a.elapsed_time(b) for a, b in evs])
-    total_ms = float(step_ms.sum())
+    total_ms = _job_time_ms(float(step_ms.sum()), ws, dev)
     if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
-    value = ws * M_TOK * args.steps / (total_ms / 1000.0)
+    value = _job_rate(M_TOK, args.steps, ws, total_ms)
 
     # per-stage device times (same cold-L2 protocol, each stage replayed alone)
     reps = max(10, min(args.steps, 100))
@@ -364,12 +380,8 @@ def run_ours(args):
     e_end.record(stream)
     e_end.synchronize()
     q.quarot_check_error(stream)
-    e2e_total = float(e_start.elapsed_time(e_end))
-    if ws > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_val = ws * M_TOK * args.steps / (e2e_total / 1000.0)
+    e2e_total = _job_time_ms(float(e_start.elapsed_time(e_end)), ws, dev)
+    e2e_val = _job_rate(M_TOK, args.steps, ws, e2e_total)
     h2d = (xd[0].numel() * 2 + kd[0].numel() * 2 + vd[0].numel() * 2 + qd[0].numel() * 2)
     d2h = y.numel() * 2 + out.numel() * 2
     # the results of the last step match the device-only path's
