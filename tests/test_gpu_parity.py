@@ -440,6 +440,16 @@ def test_prefill_last_row_is_decode(q):
     assert O.rel_fro(out[:, -1].cpu().numpy(), dec.cpu().numpy().astype(np.float64)) <= 2 * OUT_TOL
 
 
+def test_prefill_long_context_g8(q):
+    """One 4096-token prompt, 8 query heads on one KV head (32 key tiles for the
+    last query tile): long causal rows, many lazy-rescale decisions."""
+    qq, oc = _prefill_case(1, 4096, 1, 8, 91)
+    out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc])
+    q.quarot_check_error()
+    ref = O.prefill_attn(qq, *oc, T=4096)
+    assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+
+
 def test_prefill_config_full(q):
     """B4 x T2048 x Hq32/Hkv8 at full size, over a cache the oracle wrote (the
     append kernel is pinned on its own); oracle on the first and last prompt
