@@ -20,7 +20,7 @@
 // probabilities are fp16 (the pages' Init feeds fp16 dequantized values to
 // flash attention); the products accumulate in fp32 in tensor memory.
 //
-// Design: one CTA per (128 query tokens, query head), 320 threads.  Tensor
+// Design: one CTA per (128 query tokens, query head), 448 threads.  Tensor
 // memory (512 columns) holds the query halves (columns [0, 64) hi, [64, 128)
 // lo, the A operand of S = Q K^T), two score buffers (columns 128 and 256) and
 // the output O (columns 384 .. 511).  The tensor cores compute S(i+1) into one
@@ -34,11 +34,13 @@
 //               fp16 code * scale, in the 128-byte swizzled K-major layout
 //               (keys row-wise; values transposed, the B operand of P V is
 //               K-major along the keys); the key scales to fp32
-//   warps 6-9   softmax, one thread per query row: rotate the queries, then per
-//               key tile the whole score row in registers (one tensor memory
-//               round trip), the running max raised lazily (only when a tile
-//               exceeds it by more than 8 in log2 units, so p < 2^8 stays in
-//               fp16 range), O rescaled in tensor memory when it is
+//   warps 6-13  softmax, two warps per tensor memory lane quadrant: each
+//               thread holds one half (64 scores) of its query row per key
+//               tile (one tensor memory round trip), the pair exchanges row
+//               maxima and sums through shared memory; the running max is
+//               raised lazily (only when a tile exceeds it by more than 8 in
+//               log2 units, so p < 2^8 stays in fp16 range), O rescaled in
+//               tensor memory when it is; the warps also rotate the queries
 // Every wait is bounded; an expired wait records QUAROT_ERR_TIMEOUT, the CTA
 // drains its copies and MMAs, frees tensor memory and returns.
 #include <math.h>
@@ -60,7 +62,8 @@ constexpr int TILE16 = 128 * HD * 2;                  // one 128 x 128 fp16 oper
 constexpr int PK_CODES = BKV * (HD / 2);              // 8 KB of codes per tensor
 constexpr int PK_BYTES = 2 * PK_CODES + 2 * BKV * 2;  // K codes, V codes, K scales, V scales
 
-constexpr int NTHREADS = 32 * (SM_W0 + 4);  // 320
+constexpr int NSW = 8;     // softmax warps: two per tensor memory lane quadrant, one per half row
+constexpr int NTHREADS = 32 * (SM_W0 + NSW);  // 448
 // Converted stage s holds the keys at OFF_KV + 2 s TILE16 and the values right
 // after them.  Before the first tile the rotated queries are staged in fp32 in
 // stage 1 (64 KB); the converters fill stage 1 only after the queries have
@@ -69,10 +72,11 @@ constexpr int OFF_KV = 0;
 constexpr int OFF_PK = OFF_KV + 2 * SK * TILE16;
 constexpr int OFF_QS = OFF_KV + 2 * TILE16;
 constexpr int OFF_KSF = OFF_PK + SP * PK_BYTES;  // fp32 key scales [2][BKV], one per score buffer
-constexpr int OFF_BAR = OFF_KSF + 2 * BKV * 4;
+constexpr int OFF_XCH = OFF_KSF + 2 * BKV * 4;    // fp32 [2 buffers][2 halves][BQ] row maxima, then [2 halves][BQ] row sums
+constexpr int OFF_BAR = OFF_XCH + 3 * 2 * BQ * 4;
 // pk_full[SP] pk_empty[SP] k_full[SK] k_empty[SK] v_full[SV] v_empty[SV]
-// q_full s_full[2] p_full[2] ks_full[2] ks_empty[2] o_done drain
-constexpr int NBAR = 2 * SP + 2 * SK + 2 * SV + 1 + 8 + 1 + 1;
+// q_full s_full[2] p_full[2] ks_full[2] ks_empty[2] o_done drain xbar[4][2] lbar[4]
+constexpr int NBAR = 2 * SP + 2 * SK + 2 * SV + 1 + 8 + 1 + 1 + 8 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 constexpr uint32_t TMEM_COLS = 512;
@@ -215,6 +219,8 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
   uint64_t* ks_empty = ks_full + 2;  // [2]
   uint64_t* o_done = ks_empty + 2;   // one phase per O += P V
   uint64_t* drain = o_done + 1;
+  uint64_t* xbar = drain + 1;      // [4 quadrants][2 buffers]: the half-row pair's max exchange
+  uint64_t* lbar = xbar + 8;       // [4 quadrants]: the pair's row-sum exchange
   float* ksf = reinterpret_cast<float*>(sm + OFF_KSF);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
@@ -244,15 +250,17 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       mbar_init(&v_full[s], NCW);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(q_full, 4);
+    mbar_init(q_full, NSW);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 4);
+      mbar_init(&p_full[s], NSW);
       mbar_init(&ks_full[s], NCW);
-      mbar_init(&ks_empty[s], 4);
+      mbar_init(&ks_empty[s], NSW);
     }
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    for (int k = 0; k < 8; ++k) mbar_init(&xbar[k], 2);
+    for (int k = 0; k < 4; ++k) mbar_init(&lbar[k], 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -445,22 +453,37 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int qd = warp & 3;  // tensor memory lane quadrant: rows 32 qd .. 32 qd + 31
-    // ---- q~ = q H / sqrt(d): one warp per query row, lane l holds dims
-    // 4l .. 4l+3; butterflies of spans 1 and 2 in registers, 4 .. 64 across
-    // lanes (natural-order FWHT: lower index a + b, upper a - b).  Rows go to
-    // an fp32 staging area, 16-byte chunk m of row r at chunk m ^ (r & 7).
+    // Two warps per tensor memory lane quadrant: warp v (0..7) serves rows
+    // 32 qd .. 32 qd + 31 and columns 64 hh .. 64 hh + 63 of every tile; the
+    // pair exchanges row maxima (per tile) and row sums (at the end) through
+    // shared memory behind an mbarrier of the pair (bounded waits, so a pair
+    // in which one warp gave up cannot hang the other).
+    const int v8 = warp - SM_W0;
+    const int qd = warp & 3;
+    const int hh = v8 >> 2;
+    float* xch = reinterpret_cast<float*>(sm + OFF_XCH);
+    // publish this warp's values (written before the call), wait for the partner's
+    auto pair_exchange = [&](uint64_t* bar, uint32_t parity) -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+      return warp_ok(mbar_wait_bounded(bar, parity, abort_flag));
+    };
+    // ---- q~ = q H / sqrt(d): one warp per query row (rows 16 v8 .. 16 v8 + 15),
+    // lane l holds dims 4l .. 4l+3; butterflies of spans 1 and 2 in registers,
+    // 4 .. 64 across lanes (natural-order FWHT: lower index a + b, upper
+    // a - b).  Rows go to an fp32 staging area, 16-byte chunk m of row r at
+    // chunk m ^ (r & 7).
     float* qs = reinterpret_cast<float*>(sm + OFF_QS);
-    uint2 raw[32];  // all 32 rows' loads in flight at once
+    uint2 raw[16];  // all 16 rows' loads in flight at once
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-      const int tok = q0 + 32 * qd + rr;
+    for (int rr = 0; rr < 16; ++rr) {
+      const int tok = q0 + 16 * v8 + rr;
       raw[rr] = tok < T ? __ldg(reinterpret_cast<const uint2*>(q + ((int64_t(b) * T + tok) * Hq + h) * HD + 4 * lane))
                         : make_uint2(0u, 0u);
     }
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-      const int row = 32 * qd + rr;
+    for (int rr = 0; rr < 16; ++rr) {
+      const int row = 16 * v8 + rr;
       const float2 a01 = h2_to_f2(raw[rr].x), a23 = h2_to_f2(raw[rr].y);
       float x[4] = {a01.x, a01.y, a23.x, a23.y};
       float u0 = x[0], u1 = x[1];
@@ -489,14 +512,15 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       }
       *reinterpret_cast<float4*>(qs + row * HD + 4 * (lane ^ (row & 7))) = make_float4(x[0], x[1], x[2], x[3]);
     }
-    __syncwarp();
-    // ---- this thread's row -> fp16 hi and lo halves of q~ * scale -> tensor memory
+    asm volatile("bar.sync 5, %0;" ::"r"(32 * NSW) : "memory");  // every staged row is written
+    // ---- this thread's half row -> fp16 hi and lo halves of q~ * scale -> tensor memory
     const int r = 32 * qd + lane;
     const int tok = q0 + r;
     const uint32_t lane_off = uint32_t(32 * qd) << 16;
     const float qsc = qscale * QUP;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int c = 2 * hh + c2;  // 32-dim chunk of the row
       uint32_t hi[16], lo[16];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -504,7 +528,7 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
         const float xs[4] = {v4.x * qsc, v4.y * qsc, v4.z * qsc, v4.w * qsc};
         float hv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hv[e] = __half2float(__float2half_rn(xs[e]));
+        for (int e2 = 0; e2 < 4; ++e2) hv[e2] = __half2float(__float2half_rn(xs[e2]));
         hi[2 * m] = pack_f2h2(hv[0], hv[1]);
         hi[2 * m + 1] = pack_f2h2(hv[2], hv[3]);
         lo[2 * m] = pack_f2h2(xs[0] - hv[0], xs[1] - hv[1]);
@@ -518,7 +542,7 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
     __syncwarp();
     if (lane == 0) mbar_arrive(q_full);
 
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this half's sum
     bool ok = true;
     for (int i = 0; i < nkt; ++i) {
       const int sb = i & 1;
@@ -530,110 +554,81 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       }
       fence_after();
       const uint32_t s_t = tmem + lane_off + COL_S + uint32_t(128 * sb);
-      const uint32_t kf_s = smem_u32(ksf + sb * BKV);
-      bool raise;
-      float alpha = 1.f;
-      if (i < nkt - 1) {
-        // ---- interior tile: the whole score row in registers, one round trip
-        uint32_t v[128];
-        tmem_ld32(s_t, v);
-        tmem_ld32(s_t + 32, v + 32);
-        tmem_ld32(s_t + 64, v + 64);
-        tmem_ld32(s_t + 96, v + 96);
-        wait_ld();
-        // scores in log2 units: the fp32 product times the key's scale
+      uint32_t v[64];
+      tmem_ld32(s_t + uint32_t(64 * hh), v);
+      tmem_ld32(s_t + uint32_t(64 * hh + 32), v + 32);
+      wait_ld();
+      // scores in log2 units: the fp32 product times the key's scale
+      const uint32_t kf_s = smem_u32(ksf + sb * BKV + 64 * hh);
 #pragma unroll
-        for (int e8 = 0; e8 < 16; ++e8) {
-          // 8 scales per batch: two loads in flight, then their 8 products
-          float kk[8];
+      for (int e8 = 0; e8 < 8; ++e8) {
+        float kk[8];
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(kk[4 * j]), "=f"(kk[4 * j + 1]), "=f"(kk[4 * j + 2]), "=f"(kk[4 * j + 3])
-                         : "r"(kf_s + 32u * e8 + 16u * j));
+        for (int j = 0; j < 2; ++j)
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(kk[4 * j]), "=f"(kk[4 * j + 1]), "=f"(kk[4 * j + 2]), "=f"(kk[4 * j + 3])
+                       : "r"(kf_s + 32u * e8 + 16u * j));
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[8 * e8 + u] = __float_as_uint(__uint_as_float(v[8 * e8 + u]) * kk[u]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ks_empty[sb]);
-        float mp[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mp[j] = __uint_as_float(v[j]);
-#pragma unroll
-        for (int e = 8; e < 128; e += 16)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) mp[j] = max3f(mp[j], __uint_as_float(v[e + j]), __uint_as_float(v[e + 8 + j]));
-        const float mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
-        // ---- lazy rescale: raise the running max only when the tile exceeds
-        // it by more than 8 (log2 units); otherwise p <= 2^8
-        raise = mx > m_run + 8.0f;
-        if (raise) {
-          alpha = ex2(m_run - mx);  // 0 while m_run is -inf
-          l_run *= alpha;
-          m_run = mx;
-        }
-        // ---- p = 2^(s - m) -> fp16 pairs into columns [0, 64) of the buffer
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 128; e += 2) {
-          const float p0 = ex2(__uint_as_float(v[e]) - m_run);
-          const float p1 = ex2(__uint_as_float(v[e + 1]) - m_run);
-          ls[(e >> 1) & 3] += p0 + p1;
-          v[e >> 1] = pack_f2h2(p0, p1);
-        }
-        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        tmem_st32(s_t, v);
-        tmem_st32(s_t + 32, v + 32);
-      } else {
-        // ---- the diagonal (causal) or ragged last tile: columns past this
-        // row's last key are masked; two passes of 32-column chunks
-        const int lim = causal ? min(tok, T - 1) - i * BKV : T - 1 - i * BKV;
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(s_t + uint32_t(32 * c), v);
-          wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (32 * c + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]) * ksf[sb * BKV + 32 * c + e]);
-        }
-        raise = mx > m_run + 8.0f;
-        if (raise) {
-          alpha = ex2(m_run - mx);
-          l_run *= alpha;
-          m_run = mx;
-        }
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32], pk[16];
-          tmem_ld32(s_t + uint32_t(32 * c), v);
-          wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = 32 * c + e;
-            const float p0 = col <= lim ? ex2(__uint_as_float(v[e]) * ksf[sb * BKV + col] - m_use) : 0.f;
-            const float p1 = col + 1 <= lim ? ex2(__uint_as_float(v[e + 1]) * ksf[sb * BKV + col + 1] - m_use) : 0.f;
-            l_run += p0 + p1;
-            pk[e >> 1] = pack_f2h2(p0, p1);
-          }
-          tmem_st16(s_t + uint32_t(16 * c), pk);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ks_empty[sb]);
+        for (int u = 0; u < 8; ++u) v[8 * e8 + u] = __float_as_uint(__uint_as_float(v[8 * e8 + u]) * kk[u]);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ks_empty[sb]);
+      if (i == nkt - 1) {
+        // the diagonal (causal) or ragged last tile: columns past this row's
+        // last key are -inf
+        const int lim = (causal ? min(tok, T - 1) - i * BKV : T - 1 - i * BKV) - 64 * hh;
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e > lim) v[e] = __float_as_uint(-INFINITY);
+      }
+      float mp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mp[j] = __uint_as_float(v[j]);
+#pragma unroll
+      for (int e = 8; e < 64; e += 16)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mp[j] = max3f(mp[j], __uint_as_float(v[e + j]), __uint_as_float(v[e + 8 + j]));
+      float mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+      // the row max over both halves; after the barrier both halves' scores
+      // are in registers, so the probabilities may overwrite the score columns
+      xch[(sb * 2 + hh) * BQ + r] = mx;
+      if (!pair_exchange(&xbar[qd * 2 + sb], par)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(xch[(sb * 2) * BQ + r], xch[(sb * 2 + 1) * BQ + r]);
+      // ---- lazy rescale: raise the running max only when the tile exceeds
+      // it by more than 8 (log2 units); otherwise p <= 2^8
+      const bool raise = mx > m_run + 8.0f;
+      float alpha = 1.f;
+      if (raise) {
+        alpha = ex2(m_run - mx);  // 0 while m_run is -inf
+        l_run *= alpha;
+        m_run = mx;
+      }
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      // ---- p = 2^(s - m) -> fp16 pairs into columns [32 hh, 32 hh + 32) of the buffer
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        const float p0 = ex2(__uint_as_float(v[e]) - m_use);
+        const float p1 = ex2(__uint_as_float(v[e + 1]) - m_use);
+        ls[(e >> 1) & 3] += p0 + p1;
+        v[e >> 1] = pack_f2h2(p0, p1);
+      }
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_st32(s_t + uint32_t(32 * hh), v);
       if (i > 0 && __any_sync(0xffffffffu, raise)) {
-        // O += P(i-1) V may still run: wait for it, then rescale O in place
-        // (before O += P(i) V, which the arrival below releases)
+        // O += P(i-1) V may still run: wait for it, then rescale this half of O
+        // in place (before O += P(i) V, which the arrival below releases)
         if (!warp_ok(mbar_wait_bounded(o_done, uint32_t((i - 1) & 1), abort_flag))) {
           ok = false;
           break;
         }
         fence_after();
-        const uint32_t o_t = tmem + lane_off + COL_O;
+        const uint32_t o_t = tmem + lane_off + COL_O + uint32_t(64 * hh);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
           tmem_ld32(o_t + uint32_t(32 * c), o);
           wait_ld();
@@ -647,13 +642,19 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
     }
+    // the row sum over both halves (own slots: the partner may still read
+    // the last tile's maxima)
+    float* xl = xch + 4 * BQ;
+    xl[hh * BQ + r] = l_run;
+    ok = ok && pair_exchange(&lbar[qd], 0);
+    const float l_tot = xl[r] + xl[BQ + r];
     if (ok && warp_ok(mbar_wait_bounded(o_done, uint32_t((nkt - 1) & 1), abort_flag))) {
       fence_after();
-      const float inv_l = 1.0f / l_run;
-      const uint32_t o_t = tmem + lane_off + COL_O;
-      __half* orow = out + ((int64_t(b) * T + tok) * Hq + h) * HD;
+      const float inv_l = 1.0f / l_tot;
+      const uint32_t o_t = tmem + lane_off + COL_O + uint32_t(64 * hh);
+      __half* orow = out + ((int64_t(b) * T + tok) * Hq + h) * HD + 64 * hh;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         tmem_ld32(o_t + uint32_t(32 * c), o);
         wait_ld();
