@@ -487,7 +487,7 @@ namespace pair {
 // and four converter warps per scheduler to hide it.
 constexpr int BM = 128;          // rows per CTA (256 per pair)
 constexpr int BNH_MAX = 112;     // weight rows per CTA (BN <= 224)
-constexpr int SP = 4;            // packed ring stages
+constexpr int SP = 6;            // packed ring stages (6 lets the loads run ~1.5 us ahead)
 constexpr int S = 8;             // converted stages (A in tensor memory, W in shared memory)
 constexpr int NAW = 8, NBW = 8;  // A / W converter warps
 constexpr int NCW = NAW + NBW;
