@@ -37,7 +37,7 @@ M_TOK, K_DIM, N_OUT = 2048, 12288, 4096
 # DRAM bytes (read + write) of one launch of the down_proj GEMM, from an ncu
 # capture of this bench (profiles/w4a4_gemm_pair_down_proj_2048x4096x12288.md);
 # None whenever the kernel has changed since that capture.
-GEMM_TRAFFIC_BYTES = 38_789_632  # 37.809920 MB read + 0.979712 MB written
+GEMM_TRAFFIC_BYTES = 38_763_008  # 37.808384 MB read + 0.954624 MB written
 KV = W.CONFIGS["kv4"]
 METRIC = "W4A4 layer tokens/s"
 WORKLOAD = ("down_proj W4A4 layer 2048x12288->4096 (H12(x)H1024 rotate+quant, INT4 GEMM, fp16 out) "

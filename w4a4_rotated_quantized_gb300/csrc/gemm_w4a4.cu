@@ -69,7 +69,7 @@ constexpr int OFF_BAR = OFF_BP + SP * B_PK;
 constexpr int NBAR = 2 * SP + 2 * SU + 8 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int OFF_RSA = OFF_MISC + 16;             // int [2][BM]
-constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;      // int [2][BN_MAX]
+constexpr int OFF_RSB = OFF_RSA + 2 * BM * 4;      // float [2][BN_MAX]: -8 x the W row sums (exact)
 constexpr int SMEM_USED = OFF_RSB + 2 * BN_MAX * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 constexpr uint32_t TMEM_COLS = 512;           // accumulator (up to 224 columns) + A stages
@@ -226,7 +226,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
   int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
-  int* rsB = reinterpret_cast<int*>(sm + OFF_RSB);
+  float* rsB = reinterpret_cast<float*>(sm + OFF_RSB);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = K / BK;
@@ -359,7 +359,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       const int a = ti & 1;
       if (!mbar_wait_bounded(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
       if (is_a) rsA[a * BM + r] = int(sum);
-      else if (r < BN_MAX) rsB[a * BN_MAX + r] = int(sum);
+      else if (r < BN_MAX) rsB[a * BN_MAX + r] = -8.0f * float(int(sum));  // exact: |8 sum| < 2^24
       __syncwarp();
       if (lane == 0) mbar_arrive(&rs_full[a]);
     }
@@ -380,7 +380,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       const int gm = m0 + r;
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
       const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[a * BM + r]);
-      const int* rsb = rsB + a * BN_MAX;
+      const float* rsb = rsB + a * BN_MAX;
       const uint32_t tmem_row = tmem_base + (uint32_t(32 * q) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -393,7 +393,7 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
           float acc[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            acc[j] = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(rsb[c0 + j])) + bias_r;
+            acc[j] = __fadd_rn(__fmaf_rn(__uint_as_float(v[j]), 262144.0f, rsb[c0 + j]), bias_r);
           __half* yrow = y + size_t(gm) * N + gn;
           if (vec_ok && gn + 32 <= N) {
 #pragma unroll
@@ -404,9 +404,9 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const float2 wsc = h2_to_f2(sws[e]);
-                const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x));
-                const __half hi = __float2half_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
-                o[e] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+                const __half2 hv = __floats2half2_rn(__fmul_rn(__fmul_rn(acc[j + 2 * e], sxr), wsc.x),
+                                                     __fmul_rn(__fmul_rn(acc[j + 2 * e + 1], sxr), wsc.y));
+                o[e] = *reinterpret_cast<const uint32_t*>(&hv);
               }
               *reinterpret_cast<uint4*>(yrow + j) = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -505,7 +505,7 @@ constexpr int OFF_BAR = ((OFF_BP + SP * B_PK) + 1023) / 1024 * 1024;
 constexpr int NBAR = 2 * SP + 2 * S + 2 + 4 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int OFF_RSA = (OFF_MISC + 16 + 127) / 128 * 128;  // int [2][2][BM]: per half row
-constexpr int OFF_RSB = OFF_RSA + 4 * BM * 4;      // int [2][BN_MAX]: the whole tile's W row sums
+constexpr int OFF_RSB = OFF_RSA + 4 * BM * 4;      // float [2][BN_MAX]: -8 x the tile's W row sums (exact)
 constexpr int OFF_SW = OFF_RSB + 2 * BN_MAX * 4;   // float [NEW][BN_MAX]: each epilogue warp's weight scales
 constexpr int SMEM_USED = OFF_SW + NEW * BN_MAX * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
@@ -690,7 +690,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
   int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
-  int* rsB = reinterpret_cast<int*>(sm + OFF_RSB);
+  float* rsB = reinterpret_cast<float*>(sm + OFF_RSB);
   float* swS = reinterpret_cast<float*>(sm + OFF_SW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -918,9 +918,10 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       if (is_a) {
         rsA[(2 * a + int(part)) * BM + r] = int(sum);
       } else if (part == 0 && r < BNH) {
-        int* dst = rsB + a * BN_MAX + int(rank) * BNH + r;
-        *dst = int(sum);
-        st_cluster_s32(mapa(smem_u32(dst), rank ^ 1u), int(sum));
+        float* dst = rsB + a * BN_MAX + int(rank) * BNH + r;
+        const float g = -8.0f * float(int(sum));  // exact: |8 sum| < 2^24
+        *dst = g;
+        st_cluster_s32(mapa(smem_u32(dst), rank ^ 1u), __float_as_int(g));
       }
       __syncwarp();
       if (lane == 0) {
@@ -952,7 +953,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         break;
       fence_after_sync();
       const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[2 * a * BM + r] + rsA[(2 * a + 1) * BM + r]);
-      const int* rsb = rsB + a * BN_MAX;
+      const float* rsb = rsB + a * BN_MAX;
       const uint32_t tmem_row = tmem_base + (uint32_t(32 * q) << 16);
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
@@ -974,10 +975,10 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             const uint4 r4 = lds128(rs_addr + 4u * uint32_t(j));
-            v[j] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j]), 262144.0f), 8.0f * float(int(r4.x))) + bias_r);
-            v[j + 1] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j + 1]), 262144.0f), 8.0f * float(int(r4.y))) + bias_r);
-            v[j + 2] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j + 2]), 262144.0f), 8.0f * float(int(r4.z))) + bias_r);
-            v[j + 3] = __float_as_uint(__fsub_rn(__fmul_rn(__uint_as_float(v[j + 3]), 262144.0f), 8.0f * float(int(r4.w))) + bias_r);
+            v[j] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j]), 262144.0f, __uint_as_float(r4.x)), bias_r));
+            v[j + 1] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 1]), 262144.0f, __uint_as_float(r4.y)), bias_r));
+            v[j + 2] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 2]), 262144.0f, __uint_as_float(r4.z)), bias_r));
+            v[j + 3] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 3]), 262144.0f, __uint_as_float(r4.w)), bias_r));
           }
           __half* yrow = y + size_t(gm) * N + gn;
           if (vec_ok && gn + 32 <= N) {
@@ -992,10 +993,9 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                   const int jj = j + 2 * (t + u);
-                  const __half lo = __float2half_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), sxr), sv[2 * u]));
-                  const __half hi =
-                      __float2half_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj + 1]), sxr), sv[2 * u + 1]));
-                  o[t + u] = uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
+                  const __half2 hv = __floats2half2_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), sxr), sv[2 * u]),
+                                                       __fmul_rn(__fmul_rn(__uint_as_float(v[jj + 1]), sxr), sv[2 * u + 1]));
+                  o[t + u] = *reinterpret_cast<const uint32_t*>(&hv);
                 }
               }
               st_global_v8(yrow + j, o);
