@@ -569,7 +569,12 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
                        : "=f"(kk[4 * j]), "=f"(kk[4 * j + 1]), "=f"(kk[4 * j + 2]), "=f"(kk[4 * j + 3])
                        : "r"(kf_s + 32u * e8 + 16u * j));
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[8 * e8 + u] = __float_as_uint(__uint_as_float(v[8 * e8 + u]) * kk[u]);
+        for (int u = 0; u < 8; u += 2) {
+          const float2 sc = __fmul2_rn(make_float2(__uint_as_float(v[8 * e8 + u]), __uint_as_float(v[8 * e8 + u + 1])),
+                                       make_float2(kk[u], kk[u + 1]));
+          v[8 * e8 + u] = __float_as_uint(sc.x);
+          v[8 * e8 + u + 1] = __float_as_uint(sc.y);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ks_empty[sb]);
@@ -608,15 +613,17 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       }
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       // ---- p = 2^(s - m) -> fp16 pairs into columns [32 hh, 32 hh + 32) of the buffer
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // packed f32x2 subtract and sums: one instruction per two scores
+      const float2 m_neg = make_float2(-m_use, -m_use);
+      float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
-        const float p0 = ex2(__uint_as_float(v[e]) - m_use);
-        const float p1 = ex2(__uint_as_float(v[e + 1]) - m_use);
-        ls[(e >> 1) & 3] += p0 + p1;
+        const float2 d = __fadd2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), m_neg);
+        const float p0 = ex2(d.x), p1 = ex2(d.y);
+        ls[(e >> 1) & 1] = __fadd2_rn(ls[(e >> 1) & 1], make_float2(p0, p1));
         v[e >> 1] = pack_f2h2(p0, p1);
       }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l_run += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
       tmem_st32(s_t + uint32_t(32 * hh), v);
       if (i > 0 && __any_sync(0xffffffffu, raise)) {
         // O += P(i-1) V may still run: wait for it, then rescale this half of O
