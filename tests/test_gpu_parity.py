@@ -423,6 +423,26 @@ def test_prefill_ignores_cache_past_T(q):
         assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
 
 
+def test_prefill_causal_rows_ignore_later_tokens(q):
+    """Causal row i reads tokens 0..i: rewriting every cached token after t
+    (codes and scales, finite) leaves rows 0..t bit-identical, since masked
+    keys enter the diagonal tile with probability exactly 0."""
+    B, T, Hkv, G, t = 2, 300, 2, 4, 150
+    qq, oc = _prefill_case(B, T, Hkv, G, 91)
+    base = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc]).cpu().numpy()
+    rng = np.random.default_rng(92)
+    oc2 = [c.copy() for c in oc]
+    for c in (oc2[0], oc2[2]):
+        c[:, :, t + 1:] = rng.integers(0, 256, c[:, :, t + 1:].shape, dtype=np.uint8)
+    oc2[1][:, :, t + 1:] *= np.float16(3.0)
+    oc2[3][:, :, t + 1:] *= np.float16(0.5)
+    assert np.isfinite(oc2[1]).all() and np.isfinite(oc2[3]).all()
+    out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc2]).cpu().numpy()
+    q.quarot_check_error()
+    assert np.array_equal(out[:, :t + 1], base[:, :t + 1])
+    assert not np.array_equal(out[:, T - 1], base[:, T - 1])
+
+
 def test_prefill_custom_scale_and_empty(q):
     qq, oc = _prefill_case(1, 150, 2, 4, 71)
     out = q.quarot_prefill_attn(_t(qq), *[_t(c) for c in oc], sm_scale=0.05)

@@ -626,6 +626,38 @@ def test_prefill_brute_force_tiny():
             assert np.allclose(out[0, i, h], o, rtol=1e-12, atol=1e-12)
 
 
+def test_prefill_noncausal_is_invariant_to_key_order():
+    # without the mask attention is a sum over keys: permuting the cached
+    # tokens (codes and scales together) leaves every output row unchanged
+    B, T, Hkv, G, d = 1, 11, 2, 2, 128
+    qq, kc, ks, vc, vs = _prefill_case(B, T, Hkv, G, d, 23)
+    perm = np.random.default_rng(24).permutation(T)
+    base = O.prefill_attn(qq, kc, ks, vc, vs, T, causal=False)
+    shuf = O.prefill_attn(qq, kc[:, :, perm], ks[:, :, perm], vc[:, :, perm], vs[:, :, perm], T, causal=False)
+    assert np.allclose(shuf, base, rtol=1e-12, atol=1e-12)
+    # the causal form is not: row 0 then sees the token that moved to slot 0
+    caus = O.prefill_attn(qq, kc[:, :, perm], ks[:, :, perm], vc[:, :, perm], vs[:, :, perm], T)
+    v_moved = O.unpack_int4(vc[:, :, perm[0]]).astype(np.float64) * vs[:, :, perm[0]].astype(np.float64)[..., None]
+    assert np.allclose(caus[:, 0], np.repeat(v_moved, G, axis=1), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_causal_rows_ignore_later_tokens():
+    # causal row i reads tokens 0..i only: rewriting every token after t
+    # leaves rows 0..t exactly as they were, and changes a later row
+    B, T, Hkv, G, d, t = 1, 10, 1, 4, 128, 5
+    qq, kc, ks, vc, vs = _prefill_case(B, T, Hkv, G, d, 25)
+    base = O.prefill_attn(qq, kc, ks, vc, vs, T)
+    rng = np.random.default_rng(26)
+    kc2, vc2, ks2, vs2 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
+    kc2[:, :, t + 1:] = rng.integers(0, 256, kc2[:, :, t + 1:].shape, dtype=np.uint8)
+    vc2[:, :, t + 1:] = rng.integers(0, 256, vc2[:, :, t + 1:].shape, dtype=np.uint8)
+    ks2[:, :, t + 1:] = ks2[:, :, t + 1:] * np.float16(3.0)
+    vs2[:, :, t + 1:] = vs2[:, :, t + 1:] * np.float16(0.5)
+    out = O.prefill_attn(qq, kc2, ks2, vc2, vs2, T)
+    assert np.array_equal(out[:, :t + 1], base[:, :t + 1])
+    assert not np.allclose(out[:, T - 1], base[:, T - 1])
+
+
 # ---------------------------------------------------------------- asymmetric KV quantizer (next row f1)
 @pytest.mark.parametrize("ex", ["A", "B"])
 def test_kv_asym_quantizer_worked_examples(golden, ex):
