@@ -64,26 +64,36 @@ constexpr int PK_BYTES = 2 * PK_CODES + 2 * BKV * 2;  // K codes, V codes, K sca
 
 constexpr int NSW = 8;     // softmax warps: two per tensor memory lane quadrant, one per half row
 constexpr int NTHREADS = 32 * (SM_W0 + NSW);  // 448
-// Converted stage s holds the keys at OFF_KV + 2 s TILE16 and the values right
-// after them.  Before the first tile the rotated queries are staged in fp32 in
-// stage 1 (64 KB); the converters fill stage 1 only after the queries have
-// moved to tensor memory.
-constexpr int OFF_KV = 0;
-constexpr int OFF_PK = OFF_KV + 2 * SK * TILE16;
-constexpr int OFF_QS = OFF_KV + 2 * TILE16;
-constexpr int OFF_KSF = OFF_PK + SP * PK_BYTES;  // fp32 key scales [2][BKV], one per score buffer
-constexpr int OFF_XCH = OFF_KSF + 2 * BKV * 4;    // fp32 [2 buffers][2 halves][BQ] row maxima, then [2 halves][BQ] row sums
-constexpr int OFF_BAR = OFF_XCH + 3 * 2 * BQ * 4;
-// pk_full[SP] pk_empty[SP] k_full[SK] k_empty[SK] v_full[SV] v_empty[SV]
-// q_full s_full[2] p_full[2] ks_full[2] ks_empty[2] o_done drain xbar[4][2] lbar[4]
-constexpr int NBAR = 2 * SP + 2 * SK + 2 * SV + 1 + 8 + 1 + 1 + 8 + 4;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+// Shared memory of one CTA.  Converted stage s holds the keys at
+// OFF_KV + 2 s STG and the values right after them.
+//   single CTA: a stage is a whole 128 x 128 fp16 tile; before the first tile
+//     the rotated queries are staged in fp32 in stage 1 (64 KB), which the
+//     converters fill only after the queries have moved to tensor memory;
+//   CTA pair (cta_group::2, M = 256): CTA r holds keys [64 r, 64 r + 64) of
+//     each key tile and dims [64 r, 64 r + 64) of each value tile, the halves
+//     of the B operands of S = Q K^T and O += P V; the query staging has its
+//     own 64 KB.
+template <bool PAIR>
+struct Plan {
+  static constexpr int ATOM = PAIR ? 8192 : 16384;  // 64 K-elements of every operand row, 128-byte swizzled
+  static constexpr int STG = 2 * ATOM;              // one converted key or value stage
+  static constexpr int OFF_KV = 0;
+  static constexpr int OFF_PK = OFF_KV + 2 * SK * STG;
+  static constexpr int OFF_KSF = OFF_PK + SP * PK_BYTES;  // fp32 key scales [2][BKV], one per score buffer
+  static constexpr int OFF_XCH = OFF_KSF + 2 * BKV * 4;    // fp32 [2 buffers][2 halves][BQ] row maxima, then [2 halves][BQ] row sums
+  static constexpr int OFF_BAR = OFF_XCH + 3 * 2 * BQ * 4;
+  // pk_full[SP] pk_empty[SP] k_full[SK] k_empty[SK] v_full[SV] v_empty[SV]
+  // q_full s_full[2] p_full[2] ks_full[2] ks_empty[2] o_done drain xbar[4][2] lbar[4]
+  static constexpr int NBAR = 2 * SP + 2 * SK + 2 * SV + 1 + 8 + 1 + 1 + 8 + 4;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_QS = PAIR ? (OFF_MISC + 16 + 1023) / 1024 * 1024 : OFF_KV + 2 * STG;
+  static constexpr int SMEM_BYTES = (PAIR ? OFF_QS + BQ * HD * 4 : OFF_MISC + 16) + 1024;  // + alignment slack
+  static_assert(PAIR || (SK == SV && SK == 2 && BQ * HD * 4 == 2 * STG), "query staging fills stage 1");
+  static_assert(OFF_PK % 16 == 0 && OFF_QS % 1024 == 0 && OFF_BAR % 8 == 0 && STG % 1024 == 0, "alignment");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_QHI = 0, COL_QLO = 64, COL_S = 128, COL_O = 384;  // S buffer b at COL_S + 128 b
-static_assert(SK == SV && SK == 2 && BQ * HD * 4 == 2 * TILE16, "query staging fills stage 1");
-static_assert(OFF_PK % 16 == 0 && OFF_QS % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 // The queries are scaled by 2^8 before the hi/lo split (the lo halves stay in
 // fp16's normal range); the key scales carry the 2^-8 back.
 constexpr float QUP = 256.0f;
@@ -91,6 +101,8 @@ constexpr float QUP = 256.0f;
 // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major,
 // N = 128 (bits 17-22, N >> 3), M = 128 (bits 24-28, M >> 4).
 constexpr uint32_t IDESC = (1u << 4) | (uint32_t(128 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+// The same for a CTA pair: M = 256 (128 rows in each CTA's tensor memory).
+constexpr uint32_t IDESC2 = (1u << 4) | (uint32_t(128 >> 3) << 17) | (uint32_t(256 >> 4) << 24);
 
 // Shared-memory descriptor of a K-major operand in the 128-byte swizzle
 // layout: 128-byte rows, 8-row groups 1024 bytes apart.
@@ -110,6 +122,36 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(IDESC), "r"(acc));
+}
+__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(IDESC2), "r"(acc));
+}
+// Completion of the pair's MMAs, signalled on the barrier at this offset in both CTAs.
+__device__ __forceinline__ void commit2(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(uint16_t(3))
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Arrival on the barrier at the same offset in CTA 0 of the pair (release at
+// CTA scope: what the leader's MMAs read was published by its writers, shared
+// memory by fence.proxy.async and tensor memory by tcgen05.wait::st).
+__device__ __forceinline__ void handoff_to_leader(uint64_t* bar) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(smem_u32(bar)));
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -198,10 +240,15 @@ __device__ __forceinline__ void codes_across(uint32_t wa, uint32_t wb, int p, ui
 
 __device__ __forceinline__ bool warp_ok(bool ok) { return __all_sync(0xffffffffu, ok); }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, const __half* __restrict__ ks,
                     const uint8_t* __restrict__ vq, const __half* __restrict__ vs, int B, int Hq, int Hkv, int T,
                     int T_max, float qscale, int causal, __half* __restrict__ out) {
+  using PL = Plan<PAIR>;
+  constexpr int OFF_KV = PL::OFF_KV, OFF_PK = PL::OFF_PK, OFF_QS = PL::OFF_QS, OFF_KSF = PL::OFF_KSF;
+  constexpr int OFF_XCH = PL::OFF_XCH, OFF_BAR = PL::OFF_BAR, OFF_MISC = PL::OFF_MISC;
+  constexpr int STG = PL::STG, ATOM = PL::ATOM;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,34 +273,41 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a pair serves two query heads of one GQA group (same KV head, same rows)
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
   const int G = Hq / Hkv;
   const int n_qt = (T + BQ - 1) / BQ;
-  const int per_qt = B * Hq;
-  const int qt = causal ? n_qt - 1 - int(blockIdx.x) / per_qt : int(blockIdx.x) / per_qt;  // longest rows first
-  const int rem = int(blockIdx.x) % per_qt;
-  const int h = rem % Hq, b = rem / Hq;
+  const int unit = PAIR ? int(blockIdx.x) >> 1 : int(blockIdx.x);
+  const int heads = PAIR ? Hq / 2 : Hq;  // head units per (prompt, query tile)
+  const int per_qt = B * heads;
+  const int qt = causal ? n_qt - 1 - unit / per_qt : unit / per_qt;  // longest rows first
+  const int rem = unit % per_qt;
+  const int h = PAIR ? 2 * (rem % heads) + int(rank) : rem % Hq, b = rem / heads;
   const int g = h / G;
   const int q0 = qt * BQ;
   const int nkt = causal ? qt + 1 : (T + BKV - 1) / BKV;
   const int64_t cache_row0 = (int64_t(b) * Hkv + g) * T_max;
 
   if (threadIdx.x == 0) {
+    // in the pair, the leader's operand barriers also count the peer's relay
+    const int relay = (PAIR && leader) ? 1 : 0;
     for (int s = 0; s < SP; ++s) {
       mbar_init(&pk_full[s], 2);  // expect_tx arrival + the scales' arrival
       mbar_init(&pk_empty[s], NCW);
     }
     for (int s = 0; s < SK; ++s) {
-      mbar_init(&k_full[s], NCW);
+      mbar_init(&k_full[s], NCW + relay);
       mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < SV; ++s) {
-      mbar_init(&v_full[s], NCW);
+      mbar_init(&v_full[s], NCW + relay);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(q_full, NSW);
+    mbar_init(q_full, NSW + relay);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], NSW);
+      mbar_init(&p_full[s], NSW + relay);
       mbar_init(&ks_full[s], NCW);
       mbar_init(&ks_empty[s], NSW);
     }
@@ -265,14 +319,23 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
     fence_barrier_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrival
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -316,24 +379,47 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       for (int j = (issued > SP ? issued - SP : 0); j < issued; ++j)
         mbar_wait_bounded(&pk_full[j % SP], uint32_t((j / SP) & 1), nullptr);
     }
+  } else if (warp == 1 && PAIR && !leader) {
+    // ------------------------------------------------------------ relay (pair, CTA 1)
+    // forward this CTA's completed operands to the leader's barriers, in the
+    // order the leader's MMA issuer consumes them
+    auto fwd = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (!warp_ok(mbar_wait_bounded(bar, parity, abort_flag))) return false;
+      if (lane == 0) handoff_to_leader(bar);
+      __syncwarp();
+      return true;
+    };
+    bool ok = fwd(q_full, 0) && fwd(&k_full[0], 0);
+    for (int i = 0; ok && i < nkt; ++i) {
+      if (i + 1 < nkt) ok = fwd(&k_full[(i + 1) % SK], uint32_t(((i + 1) / SK) & 1));
+      ok = ok && fwd(&v_full[i % SV], uint32_t((i / SV) & 1)) && fwd(&p_full[i & 1], uint32_t((i >> 1) & 1));
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t kv_s = smem_u32(sm + OFF_KV);
+      auto mma = [&](uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t acc) {
+        if constexpr (PAIR) mma2_ts(d, a_tmem, bdesc, acc);
+        else mma_ts(d, a_tmem, bdesc, acc);
+      };
+      auto done = [&](uint64_t* bar) {
+        if constexpr (PAIR) commit2(bar);
+        else commit(bar);
+      };
       // S(i) into buffer i % 2: Q hi and Q lo (tensor memory) times the key codes
       auto issue_s = [&](int i) {
         const int kst = i % SK;
         const uint32_t d = tmem + COL_S + uint32_t(128 * (i & 1));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ts(d, tmem + COL_QHI + uint32_t(8 * kk),
-                 sw128_desc(kv_s + uint32_t(2 * kst * TILE16 + (kk >> 2) * 16384 + (kk & 3) * 32)), kk > 0);
+          mma(d, tmem + COL_QHI + uint32_t(8 * kk),
+              sw128_desc(kv_s + uint32_t(2 * kst * STG + (kk >> 2) * ATOM + (kk & 3) * 32)), kk > 0);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ts(d, tmem + COL_QLO + uint32_t(8 * kk),
-                 sw128_desc(kv_s + uint32_t(2 * kst * TILE16 + (kk >> 2) * 16384 + (kk & 3) * 32)), 1u);
-        commit(&s_full[i & 1]);
-        commit(&k_empty[kst]);
+          mma(d, tmem + COL_QLO + uint32_t(8 * kk),
+              sw128_desc(kv_s + uint32_t(2 * kst * STG + (kk >> 2) * ATOM + (kk & 3) * 32)), 1u);
+        done(&s_full[i & 1]);
+        done(&k_empty[kst]);
       };
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag) && mbar_wait_bounded(&k_full[0], 0, abort_flag);
       if (ok) {
@@ -356,14 +442,14 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
         fence_after();
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk)
-          mma_ts(tmem + COL_O, tmem + COL_S + uint32_t(128 * (i & 1) + 8 * kk),
-                 sw128_desc(kv_s + uint32_t((2 * vst + 1) * TILE16 + (kk >> 2) * 16384 + (kk & 3) * 32)),
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        commit(o_done);
-        commit(&v_empty[vst]);
+          mma(tmem + COL_O, tmem + COL_S + uint32_t(128 * (i & 1) + 8 * kk),
+              sw128_desc(kv_s + uint32_t((2 * vst + 1) * STG + (kk >> 2) * ATOM + (kk & 3) * 32)),
+              (i > 0 || kk > 0) ? 1u : 0u);
+        done(o_done);
+        done(&v_empty[vst]);
       }
       // every issued MMA completes before tensor memory is freed
-      commit(drain);
+      done(drain);
       mbar_wait_bounded(drain, 0, nullptr);
     }
   } else if (warp < SM_W0) {
@@ -374,7 +460,8 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       const int sp = i % SP, kst = i % SK, vst = i % SV;
       if (!warp_ok(mbar_wait_bounded(&pk_full[sp], uint32_t((i / SP) & 1), abort_flag))) break;
       if (!warp_ok(mbar_wait_bounded(&k_empty[kst], uint32_t((i / SK) & 1) ^ 1u, abort_flag))) break;
-      if (i == 1 && !warp_ok(mbar_wait_bounded(q_full, 0, abort_flag))) break;  // stage 1 held the queries
+      // (single CTA) stage 1 held the queries
+      if (!PAIR && i == 1 && !warp_ok(mbar_wait_bounded(q_full, 0, abort_flag))) break;
       const unsigned char* st = sm + OFF_PK + sp * PK_BYTES;
       const __half* kss = reinterpret_cast<const __half*>(st + 2 * PK_CODES);
       const uint32_t* vss2 = reinterpret_cast<const uint32_t*>(kss + BKV);  // value scales in pairs
@@ -385,17 +472,19 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       // may alias the loads as far as the compiler knows); the loop stays
       // rolled so the converters' code shares the instruction cache with the
       // softmax's.
-      unsigned char* kdst = sm + OFF_KV + 2 * kst * TILE16;
+      // (pair) this CTA's 64 keys start at key 64 r of the tile
+      unsigned char* kdst = sm + OFF_KV + 2 * kst * STG;
+      const unsigned char* ksrc = st + (PAIR ? 64 * int(rank) : 0) * (HD / 2);
 #pragma unroll 1
-      for (int it0 = 0; it0 < BKV / 8; it0 += 4) {
+      for (int it0 = 0; it0 < (PAIR ? BKV / 16 : BKV / 8); it0 += 4) {
         uint32_t words[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          words[u] = *reinterpret_cast<const uint32_t*>(st + (2 * (cw + 4 * (it0 + u)) + half) * (HD / 2) + 4 * w);
+          words[u] = *reinterpret_cast<const uint32_t*>(ksrc + (2 * (cw + 4 * (it0 + u)) + half) * (HD / 2) + 4 * w);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int t = 2 * (cw + 4 * (it0 + u)) + half;
-          *reinterpret_cast<uint4*>(kdst + (w >> 3) * 16384 + t * 128 + (((w & 7) ^ (t & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(kdst + (w >> 3) * ATOM + t * 128 + (((w & 7) ^ (t & 7)) << 4)) =
               make_uint4(codes_of_byte(words[u], 0), codes_of_byte(words[u], 1), codes_of_byte(words[u], 2),
                          codes_of_byte(words[u], 3));
         }
@@ -416,18 +505,23 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       // values, transposed: task (key chunk c of 8 tokens, word w) -> for each
       // of the 8 dims of word w, 16 bytes (the 8 tokens) of dim row 8w + e.
       // In one store the 8 lanes of a quarter warp hold 8 distinct chunks c.
-      unsigned char* vdst = sm + OFF_KV + (2 * vst + 1) * TILE16;
+      unsigned char* vdst = sm + OFF_KV + (2 * vst + 1) * STG;
       const unsigned char* vsrc = st + PK_CODES;
+      // pair: 16 key chunks x this CTA's 8 words (dims 64 r .. 64 r + 63), one
+      // task per thread; the 8 lanes of a quarter warp hold 8 distinct chunks
+      const int wl = PAIR ? (lane & 7) : w;                  // word within this CTA's dims
+      const int wsrc = PAIR ? 8 * int(rank) + wl : w;        // word within the packed row
 #pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        const int c = ((w + cw + 4 * pass) & 7) + 8 * half;
+      for (int pass = 0; pass < (PAIR ? 1 : 2); ++pass) {
+        const int c = PAIR ? ((wl + cw + 4 * ((lane >> 3) & 1)) & 7) + 8 * (lane >> 4)
+                           : ((w + cw + 4 * pass) & 7) + 8 * half;
         uint32_t W[8], s2[4];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj)
-          W[jj] = *reinterpret_cast<const uint32_t*>(vsrc + (8 * c + jj) * (HD / 2) + 4 * w);
+          W[jj] = *reinterpret_cast<const uint32_t*>(vsrc + (8 * c + jj) * (HD / 2) + 4 * wsrc);
 #pragma unroll
         for (int u = 0; u < 4; ++u) s2[u] = vss2[4 * c + u];
-        unsigned char* cbase = vdst + (c >> 3) * 16384;
+        unsigned char* cbase = vdst + (c >> 3) * ATOM;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
           uint32_t lo[4], hi[4];
@@ -437,7 +531,7 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
             lo[u] = hmul2(lo[u], s2[u]);
             hi[u] = hmul2(hi[u], s2[u]);
           }
-          const int n0 = 8 * w + 2 * p, n1 = n0 + 1;
+          const int n0 = 8 * wl + 2 * p, n1 = n0 + 1;
           *reinterpret_cast<uint4*>(cbase + n0 * 128 + (((c & 7) ^ (n0 & 7)) << 4)) =
               make_uint4(lo[0], lo[1], lo[2], lo[3]);
           *reinterpret_cast<uint4*>(cbase + n1 * 128 + (((c & 7) ^ (n1 & 7)) << 4)) =
@@ -468,54 +562,48 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       if (lane == 0) mbar_arrive(bar);
       return warp_ok(mbar_wait_bounded(bar, parity, abort_flag));
     };
-    // ---- q~ = q H / sqrt(d): one warp per query row (rows 16 v8 .. 16 v8 + 15),
-    // lane l holds dims 4l .. 4l+3; butterflies of spans 1 and 2 in registers,
-    // 4 .. 64 across lanes (natural-order FWHT: lower index a + b, upper
-    // a - b).  Rows go to an fp32 staging area, 16-byte chunk m of row r at
-    // chunk m ^ (r & 7).
-    float* qs = reinterpret_cast<float*>(sm + OFF_QS);
-    uint2 raw[16];  // all 16 rows' loads in flight at once
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int tok = q0 + 16 * v8 + rr;
-      raw[rr] = tok < T ? __ldg(reinterpret_cast<const uint2*>(q + ((int64_t(b) * T + tok) * Hq + h) * HD + 4 * lane))
-                        : make_uint2(0u, 0u);
-    }
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int row = 16 * v8 + rr;
-      const float2 a01 = h2_to_f2(raw[rr].x), a23 = h2_to_f2(raw[rr].y);
-      float x[4] = {a01.x, a01.y, a23.x, a23.y};
-      float u0 = x[0], u1 = x[1];
-      x[0] = u0 + u1;
-      x[1] = u0 - u1;
-      u0 = x[2];
-      u1 = x[3];
-      x[2] = u0 + u1;
-      x[3] = u0 - u1;
-      u0 = x[0];
-      u1 = x[2];
-      x[0] = u0 + u1;
-      x[2] = u0 - u1;
-      u0 = x[1];
-      u1 = x[3];
-      x[1] = u0 + u1;
-      x[3] = u0 - u1;
-#pragma unroll
-      for (int s = 1; s < 32; s <<= 1) {
-        const bool upper = (lane & s) != 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[k], s);
-          x[k] = upper ? other - x[k] : x[k] + other;
-        }
-      }
-      *reinterpret_cast<float4*>(qs + row * HD + 4 * (lane ^ (row & 7))) = make_float4(x[0], x[1], x[2], x[3]);
-    }
-    asm volatile("bar.sync 5, %0;" ::"r"(32 * NSW) : "memory");  // every staged row is written
-    // ---- this thread's half row -> fp16 hi and lo halves of q~ * scale -> tensor memory
+    // ---- q~ = q H / sqrt(d) (1/sqrt(d) rides in qsc): this thread's half row.
+    // Natural-order FWHT, lower index a + b, upper a - b: spans 1 .. 32 in
+    // registers, span 64 with the partner thread (same lane, other half)
+    // through the fp32 staging area; a half row sits at [r][64 hh ..] in
+    // 16-byte chunks, chunk m at m ^ (lane & 7).
     const int r = 32 * qd + lane;
     const int tok = q0 + r;
+    float* qs = reinterpret_cast<float*>(sm + OFF_QS);
+    float x[64];
+    {
+      uint4 raw[8];
+      const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t(b) * T + tok) * Hq + h) * HD + 64 * hh);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) raw[m] = tok < T ? __ldg(src + m) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint32_t w4[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = h2_to_f2(w4[k]);
+          x[8 * m + 2 * k] = f.x;
+          x[8 * m + 2 * k + 1] = f.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int s = 1; s < 64; s <<= 1)
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if ((i & s) == 0) {
+          const float u0 = x[i], u1 = x[i + s];
+          x[i] = u0 + u1;
+          x[i + s] = u0 - u1;
+        }
+    float* my = qs + r * HD + 64 * hh;
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      *reinterpret_cast<float4*>(my + 4 * (m ^ (lane & 7))) = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
+    asm volatile("bar.sync 5, %0;" ::"r"(32 * NSW) : "memory");  // both halves of every row are staged
+    // ---- span 64 (both halves re-read from the staging area), then fp16 hi
+    // and lo halves of q~ * scale -> tensor memory
+    const float* other = qs + r * HD + 64 * (1 - hh);
     const uint32_t lane_off = uint32_t(32 * qd) << 16;
     const float qsc = qscale * QUP;
 #pragma unroll
@@ -524,8 +612,13 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       uint32_t hi[16], lo[16];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const float4 v4 = *reinterpret_cast<const float4*>(qs + r * HD + 4 * ((8 * c + m) ^ (r & 7)));
-        const float xs[4] = {v4.x * qsc, v4.y * qsc, v4.z * qsc, v4.w * qsc};
+        const int mm = 8 * c2 + m;  // 16-byte chunk within the half
+        const float4 a4 = *reinterpret_cast<const float4*>(my + 4 * (mm ^ (lane & 7)));
+        const float4 y4 = *reinterpret_cast<const float4*>(other + 4 * (mm ^ (lane & 7)));
+        const float xa[4] = {a4.x, a4.y, a4.z, a4.w}, y[4] = {y4.x, y4.y, y4.z, y4.w};
+        float xs[4];
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) xs[e2] = (hh == 0 ? xa[e2] + y[e2] : y[e2] - xa[e2]) * qsc;
         float hv[4];
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2) hv[e2] = __half2float(__float2half_rn(xs[e2]));
@@ -682,9 +775,13 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
 
   fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still touch its memory
   if (warp == 1) {
     fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
 }
 
@@ -713,15 +810,44 @@ extern "C" int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void
   const float scale = sm_scale > 0.f ? sm_scale : 1.0f / sqrtf(float(HD));
   // q~ carries 1/sqrt(d) of the rotation, the softmax scale and log2(e)
   const float qscale = scale * 1.4426950408889634f / sqrtf(float(HD));
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
-      return QUAROT_ERR_CUDA;
-    attr_set = true;
+  const __half* qh = static_cast<const __half*>(q);
+  const __half* ksh = static_cast<const __half*>(k_s);
+  const __half* vsh = static_cast<const __half*>(v_s);
+  __half* oh = static_cast<__half*>(out);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (G >= 2) {
+    // CTA pairs: two query heads of a GQA group share each converted tile
+    static bool attr2 = false;
+    if (!attr2) {
+      if (cudaFuncSetAttribute(prefill_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Plan<true>::SMEM_BYTES) != cudaSuccess)
+        return QUAROT_ERR_CUDA;
+      attr2 = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));  // Hq is even (G >= 2): whole pairs
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = Plan<true>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_attn_kernel<true>, qh, k_q, ksh, v_q, vsh, int(B),
+                                             int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, oh);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
   }
-  prefill_attn_kernel<<<dim3(unsigned(grid)), dim3(NTHREADS), SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q, static_cast<const __half*>(v_s),
-      int(B), int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, static_cast<__half*>(out));
+  static bool attr1 = false;
+  if (!attr1) {
+    if (cudaFuncSetAttribute(prefill_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Plan<false>::SMEM_BYTES) != cudaSuccess)
+      return QUAROT_ERR_CUDA;
+    attr1 = true;
+  }
+  prefill_attn_kernel<false><<<dim3(unsigned(grid)), dim3(NTHREADS), Plan<false>::SMEM_BYTES, st>>>(
+      qh, k_q, ksh, v_q, vsh, int(B), int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, oh);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
