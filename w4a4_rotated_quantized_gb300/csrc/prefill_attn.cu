@@ -20,7 +20,13 @@
 // probabilities are fp16 (the pages' Init feeds fp16 dequantized values to
 // flash attention); the products accumulate in fp32 in tensor memory.
 //
-// Design: one CTA per (128 query tokens, query head), 448 threads.  Tensor
+// Design: one CTA per (128 query tokens, query head), 448 threads; with
+// Hq / Hkv >= 2 the two query heads of a GQA group that read the same KV head
+// run as a cluster of two CTAs (tcgen05 cta_group::2, M = 256): each CTA
+// converts half of every key tile (64 keys) and half of every value tile (64
+// dims), the two halves of the shared B operands, CTA 1 relays its operand
+// barriers to CTA 0, and CTA 0 issues every MMA and multicasts completions.
+// Per CTA, tensor
 // memory (512 columns) holds the query halves (columns [0, 64) hi, [64, 128)
 // lo, the A operand of S = Q K^T), two score buffers (columns 128 and 256) and
 // the output O (columns 384 .. 511).  The tensor cores compute S(i+1) into one
@@ -29,7 +35,8 @@
 // operand of O += P V (kind::f16, A from tensor memory).
 //   warp 0      producer: the packed K/V codes of 128 keys by bulk copies,
 //               their scales by plain loads, into a 4-stage ring
-//   warp 1      tensor memory allocator and single-thread MMA issuer
+//   warp 1      tensor memory allocator and single-thread MMA issuer (in a
+//               pair: CTA 0 issues, CTA 1 relays)
 //   warps 2-5   converters: key codes -> exact fp16 codes, value codes ->
 //               fp16 code * scale, in the 128-byte swizzled K-major layout
 //               (keys row-wise; values transposed, the B operand of P V is
