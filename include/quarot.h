@@ -60,6 +60,14 @@ int quarot_version(void);
  * QUAROT_ERR_CUDA if the synchronization itself failed. */
 int quarot_check_error(void* stream);
 
+/* Self-test of the bounded wait every kernel relies on: one device thread
+ * waits on a hardware barrier that nothing completes, gives up after the
+ * library's wait limit (one second), records QUAROT_ERR_TIMEOUT in the
+ * device error word and returns.  The call itself returns QUAROT_OK (or
+ * QUAROT_ERR_LAUNCH); the next quarot_check_error() on `stream` returns
+ * QUAROT_ERR_TIMEOUT and clears the word; the context stays usable. */
+int quarot_selftest_wait(void* stream);
+
 /*
  * quarot_rotate_quant -- online randomized Hadamard rotation of each row
  * followed by per-token symmetric INT4 quantization and packing.

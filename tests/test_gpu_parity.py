@@ -69,6 +69,28 @@ def check_quant(gq, gs, grot, r_ref, clip=1.0):
     assert np.all((own == codes) | near)
 
 
+# ---------------------------------------------------------------- bounded waits
+def test_bounded_wait_expires_and_context_survives(q):
+    """A device wait on a barrier that nothing completes gives up after the
+    library's limit (one second), reports QUAROT_ERR_TIMEOUT once, and the
+    context keeps running kernels correctly afterwards (no fault, no hang)."""
+    import time
+
+    q.quarot_check_error()  # start from a clear error word
+    t0 = time.perf_counter()
+    q.quarot_selftest_wait()
+    with pytest.raises(q.QuarotError) as e:
+        q.quarot_check_error()
+    dt = time.perf_counter() - t0
+    assert e.value.status == q.QUAROT_ERR_TIMEOUT
+    assert 0.9 <= dt < 30.0, dt
+    q.quarot_check_error()  # the word was cleared
+    x, _, s = W.layer_inputs("tiny")
+    gq, gs, grot = q.quarot_rotate_quant(_t(x), _t(s), want_rot=True)
+    q.quarot_check_error()
+    check_quant(gq.cpu().numpy(), gs.cpu().numpy(), grot.cpu().numpy(), O.rotate(x, s))
+
+
 # ---------------------------------------------------------------- rotate+quant
 @pytest.mark.parametrize("d", [16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 3072, 6144, 12288])
 @pytest.mark.parametrize("signed", [True, False])

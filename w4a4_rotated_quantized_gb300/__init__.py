@@ -21,6 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libquarot.so")
 
 QUAROT_OK = 0
+QUAROT_ERR_TIMEOUT = 5
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size", 3: "misaligned pointer or leading dimension",
           4: "kernel launch failed", 5: "device-side wait timed out", 6: "CUDA error"}
 
@@ -32,6 +33,7 @@ _SIGS = {
     "quarot_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "quarot_version": (ctypes.c_int, []),
     "quarot_check_error": (ctypes.c_int, [_P]),
+    "quarot_selftest_wait": (ctypes.c_int, [_P]),
     "quarot_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_rotate_quant_fp16": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_rmsnorm_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, ctypes.c_float, _P, ctypes.c_float, _P, _P,
@@ -113,6 +115,13 @@ def quarot_check_error(stream=None, device=None) -> None:
     """Synchronizes the stream and raises if a kernel recorded a device-side error."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _check(load().quarot_check_error(_stream(stream, dev)), "quarot_check_error")
+
+
+def quarot_selftest_wait(stream=None, device=None) -> None:
+    """Launches the bounded-wait self-test (one device thread, about one second);
+    the next quarot_check_error() raises QuarotError with QUAROT_ERR_TIMEOUT."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(load().quarot_selftest_wait(_stream(stream, dev)), "quarot_selftest_wait")
 
 
 def _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot):

@@ -4,7 +4,17 @@
 
 namespace quarot {
 __device__ unsigned int g_error_word = 0;
+
+// One thread waits on a shared-memory barrier that nothing completes: the
+// bounded wait every kernel uses gives up after kWaitLimitNs, records
+// QUAROT_ERR_TIMEOUT and returns, and the kernel ends normally.
+__global__ void selftest_wait_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  mbar_wait_bounded(&bar, 0u, nullptr);
 }
+}  // namespace quarot
 
 extern "C" const char* quarot_status_string(int status) {
   switch (status) {
@@ -29,4 +39,9 @@ extern "C" int quarot_check_error(void* stream) {
     return QUAROT_ERR_CUDA;
   if (word & QUAROT_ERR_TIMEOUT) return QUAROT_ERR_TIMEOUT;
   return word ? QUAROT_ERR_CUDA : QUAROT_OK;
+}
+
+extern "C" int quarot_selftest_wait(void* stream) {
+  quarot::selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
