@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/quarot.h"
 
 namespace quarot {
@@ -17,6 +19,20 @@ extern __device__ unsigned int g_error_word;  // defined in abi.cu (relocatable 
 // ~1 s: far above any legitimate wait, short enough to keep a shared GPU
 // usable if a barrier is never satisfied.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// Dynamic shared memory above 48 KB is an attribute of a kernel on one
+// device: set it the first time the kernel is launched on each device.
+// `done` remembers devices 0..63; a device beyond them sets it every time.
+template <typename Kernel>
+inline bool smem_attr_once(Kernel* kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
+}
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;

@@ -1130,13 +1130,8 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
     const int bn = pick_bn_pair(M, N, pairs);
     CUtensorMap ta, tb;
     if (!make_map(&ta, a_q, M, K, pair::BM) || !make_map(&tb, w_q, N, K, bn / 2)) return QUAROT_ERR_CUDA;
-    static bool pattr = false;
-    if (!pattr) {
-      if (cudaFuncSetAttribute(pair::w4a4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               pair::SMEM_BYTES) != cudaSuccess)
-        return QUAROT_ERR_LAUNCH;
-      pattr = true;
-    }
+    static std::atomic<unsigned long long> pattr{0};
+    if (!smem_attr_once(pair::w4a4_gemm_pair_kernel, pair::SMEM_BYTES, pattr)) return QUAROT_ERR_LAUNCH;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
     const int64_t npairs = tiles < pairs ? tiles : pairs;
     cudaLaunchConfig_t cfg = {};
@@ -1159,13 +1154,8 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   const int bn = pick_bn(M, N, sms);
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_q, M, K, BM) || !make_map(&tb, w_q, N, K, bn)) return QUAROT_ERR_CUDA;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
-      return QUAROT_ERR_LAUNCH;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  if (!smem_attr_once(w4a4_gemm_kernel, SMEM_BYTES, attr)) return QUAROT_ERR_LAUNCH;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
   const unsigned grid = unsigned(tiles < sms ? tiles : sms);
   w4a4_gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(

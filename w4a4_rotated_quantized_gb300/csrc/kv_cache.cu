@@ -769,14 +769,11 @@ static int decode_impl(const void* q, const uint8_t* k_q, const void* k_s, const
                       (!ASYM || (!mis(k_z, 16) && !mis(v_z, 16)));
   int lrc = QUAROT_OK;
   auto args = [&](auto kern, size_t smem) {
-    static bool attr[4] = {false, false, false, false};
+    static std::atomic<unsigned long long> attr[4];  // per group size: the kernels differ
     const int slot = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-    if (!attr[slot]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
-        lrc = QUAROT_ERR_LAUNCH;
-        return;
-      }
-      attr[slot] = true;
+    if (!smem_attr_once(kern, int(smem), attr[slot])) {
+      lrc = QUAROT_ERR_LAUNCH;
+      return;
     }
     kern<<<grid, kv::DT, smem, st>>>(static_cast<const __half*>(q), k_q, static_cast<const __half*>(k_s), v_q,
                                      static_cast<const __half*>(v_s), int(Hq), int(Hkv), int(T), int(T_max),

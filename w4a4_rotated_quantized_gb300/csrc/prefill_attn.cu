@@ -824,13 +824,8 @@ extern "C" int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (G >= 2) {
     // CTA pairs: two query heads of a GQA group share each converted tile
-    static bool attr2 = false;
-    if (!attr2) {
-      if (cudaFuncSetAttribute(prefill_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Plan<true>::SMEM_BYTES) != cudaSuccess)
-        return QUAROT_ERR_CUDA;
-      attr2 = true;
-    }
+    static std::atomic<unsigned long long> attr2{0};
+    if (!quarot::smem_attr_once(prefill_attn_kernel<true>, Plan<true>::SMEM_BYTES, attr2)) return QUAROT_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));  // Hq is even (G >= 2): whole pairs
     cfg.blockDim = dim3(NTHREADS);
@@ -847,13 +842,8 @@ extern "C" int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void
                                              int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, oh);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
   }
-  static bool attr1 = false;
-  if (!attr1) {
-    if (cudaFuncSetAttribute(prefill_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Plan<false>::SMEM_BYTES) != cudaSuccess)
-      return QUAROT_ERR_CUDA;
-    attr1 = true;
-  }
+  static std::atomic<unsigned long long> attr1{0};
+  if (!quarot::smem_attr_once(prefill_attn_kernel<false>, Plan<false>::SMEM_BYTES, attr1)) return QUAROT_ERR_CUDA;
   prefill_attn_kernel<false><<<dim3(unsigned(grid)), dim3(NTHREADS), Plan<false>::SMEM_BYTES, st>>>(
       qh, k_q, ksh, v_q, vsh, int(B), int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, oh);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;

@@ -585,20 +585,21 @@ static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* si
                       void* s, float* rot, cudaStream_t st) {
   using PL = SegPlan<MSEG, STAGED>;
   auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS>;
-  static bool attr_set = false;
-  static int per_sm = 1;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PL::SMEM)) != cudaSuccess)
-      return QUAROT_ERR_LAUNCH;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PL::NT, PL::SMEM) != cudaSuccess || per_sm < 1)
-      per_sm = 1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  static std::atomic<int> per_sm_dev[64];  // resident CTAs per SM on devices 0..63; 0 until measured
+  if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
   int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
   if constexpr (STAGED) {
     int dev = 0, sms = 1;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QUAROT_ERR_CUDA;
+    const bool known = dev >= 0 && dev < 64;
+    int per_sm = known ? per_sm_dev[dev].load(std::memory_order_relaxed) : 0;
+    if (per_sm < 1) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PL::NT, PL::SMEM) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+      if (known) per_sm_dev[dev].store(per_sm, std::memory_order_relaxed);
+    }
     const int64_t cap = int64_t(sms) * per_sm;
     blocks = blocks < cap ? blocks : cap;
     if ((reinterpret_cast<uintptr_t>(x) & 15) || ((ld_x * 2) & 15)) return QUAROT_ERR_ALIGNMENT;
@@ -616,13 +617,8 @@ static int launch_rq_t(const void* x, int64_t M, int64_t ld_x, const int8_t* sig
   auto kern = rotate_quant_kernel<LOGP, M12, RMS, H16>;
   // fp16(1/sqrt(d)), rounded once from double (used by the FP16 variant)
   const float h16_c = __half2float(__double2half(1.0 / sqrt(double(PL::D))));
-  static bool attr_set = false;  // per-process; sizes are below the opt-in limit
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PL::SMEM)) !=
-        cudaSuccess)
-      return QUAROT_ERR_LAUNCH;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
   const int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(
