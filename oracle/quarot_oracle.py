@@ -47,7 +47,11 @@ design notes):
     0, 15), x^ = s (q + z);
   * KV: head-wise H_128 without random signs, per-(token, head) symmetric INT4
     with an fp16 scale; decode softmax in full precision, GQA head h reads KV
-    head h // (Hq / Hkv); output optionally rotated back by the same H_128.
+    head h // (Hq / Hkv); output optionally rotated back by the same H_128;
+  * prefill ("Init"): prompt token i attends to cached tokens t <= i (or to all
+    T tokens without the mask), with the same rotated query, dequantized keys
+    and values and full-precision softmax as the decode; the output stays in
+    the rotated basis.
 """
 from __future__ import annotations
 
