@@ -174,17 +174,28 @@ int quarot_crosshead_rotate_quant(const void* z, int64_t M, int64_t nh, int64_t 
  *   y[i, j]   = fp16(fp32(fp32(acc) * sx[i]) * sw[j])
  *
  *   a_q       uint8 [M, K/2] packed activations (K-major), 16-byte aligned
- *   a_scale   fp16 [M]
+ *   a_scale   fp16 [M], 2-byte aligned
  *   w_q       uint8 [N, K/2] packed weights (K-major, [out, in]), 16-byte aligned
- *   w_scale   fp16 [N]
+ *   w_scale   fp16 [N], 16-byte aligned (the epilogue loads it in 16-byte vectors)
  *   M, N      >= 0 (ragged tails handled); K % 128 == 0, 128 <= K <= 65536
  *             (the bound keeps every partial sum exact in fp32 on the tensor cores)
- *   y         fp16 [M, N]
- *   acc_out   int32 [M, N] (the exact accumulator, for testing), or NULL
+ *   y         fp16 [M, N], 16-byte aligned
+ *   acc_out   int32 [M, N] (the exact accumulator, for testing), or NULL; 4-byte aligned
+ * Misaligned pointers return QUAROT_ERR_ALIGNMENT before any launch.
  */
 int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const uint8_t* w_q,
                      const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
                      int32_t* acc_out, void* stream);
+
+/* quarot_w4a4_gemm_plan -- which kernel and N-tile width quarot_w4a4_gemm
+ * launches for an M x N x K problem on a GPU with `sms` SMs (a host-only
+ * query: it touches no device).  *form = 2 for the CTA-pair kernel (M > 128
+ * and an even number of 128-wide k-blocks), 1 for the one-SM kernel; *bn is
+ * the N-tile width, one of 128, 160, 192, 224.  Returns QUAROT_ERR_INVALID_ARG
+ * for non-positive sizes or null outputs and QUAROT_ERR_UNSUPPORTED for a K
+ * the GEMM rejects.  The pages have no counterpart: it lets tests and tools
+ * see which tile configuration a shape exercises. */
+int quarot_w4a4_gemm_plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn);
 
 /*
  * quarot_kv_write -- "Append": rotate the new keys and values head-wise by
@@ -317,9 +328,16 @@ int quarot_decode_attn_asym(const void* q, const uint8_t* k_q, const void* k_s, 
  * The call allocates nothing.
  *   - Returns QUAROT_ERR_UNSUPPORTED, before touching the device, when
  *     quarot_decode_workspace_bytes(B, Hq, d, T) exceeds that maximum.
- *   - The first call on each device looks up the array's device address
- *     (with that device current) and caches it; make that first call before
- *     any stream capture.  A failed lookup returns QUAROT_ERR_CUDA.
+ *   - The first call in each CUDA context looks up the array's device
+ *     address (with that device current) and caches it with the context's
+ *     id; make that first call before any stream capture.  After a
+ *     cudaDeviceReset (or any re-creation of the context) the library's
+ *     module is loaded again and the array may move: the next call sees a
+ *     new context id and looks the address up again, so the array's old
+ *     contents are gone but no stale address is used.  A failed lookup
+ *     returns QUAROT_ERR_CUDA.
+ *   - Invalid arguments get the status quarot_decode_attn gives them, and
+ *     nothing touches the device for a rejected request.
  *   - Every call on a device shares the one array.  No part of it needs to
  *     start at zero (each call writes every slot it later reads), but two
  *     calls whose executions overlap on the GPU (different streams, no

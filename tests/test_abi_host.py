@@ -165,3 +165,22 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(q, "_lib", None)
     with pytest.raises(q.QuarotError):
         q.load("/nonexistent/libquarot.so")
+
+
+def test_gemm_plan_query(lib):
+    """The launch plan (kernel form, N-tile width) as the host computes it for
+    a 152-SM GB300: the bench shape takes the CTA pair at BN 224, the sweep
+    reaches 160 and 192, small M the one-SM kernel, an odd k-block count the
+    one-SM kernel at any M; bad sizes are rejected."""
+    assert q.quarot_w4a4_gemm_plan(2048, 4096, 12288, 152) == (2, 224)
+    assert q.quarot_w4a4_gemm_plan(8192, 4096, 4096, 152) == (2, 160)
+    assert q.quarot_w4a4_gemm_plan(512, 12288, 4096, 152) == (2, 192)
+    assert q.quarot_w4a4_gemm_plan(16, 256, 256, 152) == (1, 128)
+    assert q.quarot_w4a4_gemm_plan(1156, 2888, 128, 152) == (1, 224)
+    assert q.quarot_w4a4_gemm_plan(1030, 2568, 384, 152)[0] == 1
+    form, bn = ctypes.c_int(0), ctypes.c_int(0)
+    f = lib.quarot_w4a4_gemm_plan
+    assert f(0, 8, 128, 152, ctypes.byref(form), ctypes.byref(bn)) == 1
+    assert f(8, 8, 100, 152, ctypes.byref(form), ctypes.byref(bn)) == 2
+    assert f(8, 8, 131072, 152, ctypes.byref(form), ctypes.byref(bn)) == 2
+    assert f(8, 8, 128, 152, None, ctypes.byref(bn)) == 1

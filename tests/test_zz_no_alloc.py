@@ -6,8 +6,10 @@ inside the library, so it takes no workspace argument.
 
 The GPU test calls it through the C ABI twice in a row, with different sizes
 and inputs, and checks each result against quarot_decode_attn given its own
-caller-allocated workspace, within the decode tolerance of the other tests.
-This file is collected last so that a failure here cannot hide another test.
+caller-allocated workspace.  Both run the same kernels with the same split
+count (the split count does not depend on the workspace size), so the
+outputs must be bit-identical.  This file is collected last so that a
+failure here cannot hide another test.
 """
 import ctypes
 
@@ -48,6 +50,29 @@ def test_static_rejects_oversize_without_touching_the_device():
     assert q.quarot_decode_workspace_bytes(64, 32, 128, 8192) > q.DECODE_STATIC_SCRATCH_BYTES
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,d,T,T_max", [
+    (2, 32, 8, 64, 100, 128),    # head_dim other than 128: unsupported
+    (2, 32, 8, 128, 200, 128),   # T beyond the cache: invalid
+    (2, 32, 2, 128, 100, 128),   # 16 query heads per KV head: unsupported
+    (2, 30, 8, 128, 100, 128),   # Hq not a multiple of Hkv: invalid
+    (-1, 32, 8, 128, 100, 128),  # negative batch: invalid
+])
+def test_static_rejects_like_the_workspace_entry(B, Hq, Hkv, d, T, T_max):
+    """Requests that quarot_decode_attn rejects get the same status from the
+    static entry point, before it looks up its scratch (no GPU needed)."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import w4a4_rotated_quantized_gb300 as q
+
+    lib = q.load()
+    P = ctypes.c_void_p(0x10000)  # never dereferenced
+    ws = ctypes.c_void_p(0x100000)
+    want = lib.quarot_decode_attn(P, P, P, P, P, B, Hq, Hkv, d, T, T_max, 0.0, 0, P, ws, 1 << 30, None)
+    got = lib.quarot_decode_attn_static(P, P, P, P, P, B, Hq, Hkv, d, T, T_max, 0.0, 0, P, None)
+    assert want != 0 and got == want, (want, got)
+
+
 @pytest.mark.gpu
 def test_static_scratch_matches_workspace_entry_twice():
     if not torch.cuda.is_available():
@@ -80,3 +105,5 @@ def test_static_scratch_matches_workspace_entry_twice():
         q.quarot_check_error(stream)
         assert torch.isfinite(out).all()
         assert _rel_fro(out, ref) <= OUT_TOL
+        # same kernels, same split count: the same bits
+        assert torch.equal(out, ref)

@@ -40,6 +40,8 @@ _SIGS = {
                                                    _P, _P]),
     "quarot_crosshead_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_w4a4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "quarot_w4a4_gemm_plan": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_int)]),
     "quarot_kv_write": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "quarot_decode_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "quarot_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
@@ -229,6 +231,14 @@ def quarot_w4a4_gemm(a_q, a_scale, w_q, w_scale, y=None, acc_out=None, stream=No
                                  _ptr(acc_out), _stream(stream, dev))
     _check(st, "quarot_w4a4_gemm")
     return y, acc_out
+
+
+def quarot_w4a4_gemm_plan(M: int, N: int, K: int, sms: int) -> tuple[int, int]:
+    """(form, bn): the kernel quarot_w4a4_gemm launches for M x N x K on a GPU
+    with `sms` SMs (2 = CTA pair, 1 = one SM) and its N-tile width."""
+    form, bn = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().quarot_w4a4_gemm_plan(M, N, K, sms, ctypes.byref(form), ctypes.byref(bn)), "quarot_w4a4_gemm_plan")
+    return form.value, bn.value
 
 
 def quarot_kv_write(k, v, t_start, k_q, k_s, v_q, v_s, stream=None):

@@ -1,9 +1,41 @@
 // Library-wide entry points of libquarot.so: status strings, version, and
 // the device error word shared by all kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
 namespace quarot {
 __device__ unsigned int g_error_word = 0;
+
+namespace {
+PFN_cuCtxGetCurrent_v4000 g_get_ctx = nullptr;
+PFN_cuCtxGetId_v12000 g_get_id = nullptr;
+std::once_flag g_fn_once;
+}  // namespace
+
+// The driver's cuCtxGetCurrent and cuCtxGetId are reached through the
+// runtime's entry-point query (the library links no driver library itself).
+unsigned long long current_context_id() {
+  std::call_once(g_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (g_get_ctx == nullptr || g_get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (g_get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  return g_get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 // One thread waits on a shared-memory barrier that nothing completes: the
 // bounded wait every kernel uses gives up after kWaitLimitNs, records
@@ -37,7 +69,7 @@ extern "C" int quarot_check_error(void* stream) {
   if (cudaMemcpyFromSymbol(&word, quarot::g_error_word, sizeof(word)) != cudaSuccess) return QUAROT_ERR_CUDA;
   if (word != 0 && cudaMemcpyToSymbol(quarot::g_error_word, &zero, sizeof(zero)) != cudaSuccess)
     return QUAROT_ERR_CUDA;
-  if (word & QUAROT_ERR_TIMEOUT) return QUAROT_ERR_TIMEOUT;
+  if (word & (1u << QUAROT_ERR_TIMEOUT)) return QUAROT_ERR_TIMEOUT;
   return word ? QUAROT_ERR_CUDA : QUAROT_OK;
 }
 

@@ -12,25 +12,43 @@
 
 namespace quarot {
 
-// Device error word: kernels OR a QUAROT_ERR_* code into it when a bounded
-// wait expires; quarot_check_error() reads and clears it.
+// Device error word: one bit per status code, bit (1 << code).  A kernel
+// sets the bit of QUAROT_ERR_TIMEOUT when a bounded wait expires;
+// quarot_check_error() reads the word, clears it and maps the bits back.
 extern __device__ unsigned int g_error_word;  // defined in abi.cu (relocatable device code)
 
 // ~1 s: far above any legitimate wait, short enough to keep a shared GPU
 // usable if a barrier is never satisfied.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
-// Dynamic shared memory above 48 KB is an attribute of a kernel on one
-// device: set it the first time the kernel is launched on each device.
-// `done` remembers devices 0..63; a device beyond them sets it every time.
+// Sizes the decode attention supports (quarot_decode_attn and its variants):
+// head_dim 128 and up to 8 query heads per KV head.
+constexpr int kDecodeHeadDim = 128;
+constexpr int kDecodeMaxGroup = 8;
+
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context, or 0
+// when no context is current or the driver cannot say.  Defined in abi.cu.
+unsigned long long current_context_id();
+
+// Dynamic shared memory above 48 KB is an attribute of a kernel in one CUDA
+// context: set it the first time the kernel is launched in each context.
+// ctx[d] remembers the context of device d (0..63) in which it was set; after
+// a cudaDeviceReset (a new context, a new id) it is set again.  A device
+// beyond 64 sets it every time.
+struct AttrCache {
+  std::atomic<unsigned long long> ctx[64];
+};
 template <typename Kernel>
-inline bool smem_attr_once(Kernel* kern, int bytes, std::atomic<unsigned long long>& done) {
+inline bool smem_attr_once(Kernel* kern, int bytes, AttrCache& done) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
-  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached) {
+    const unsigned long long id = current_context_id();
+    if (id != 0 && done.ctx[dev].load(std::memory_order_acquire) == id) return true;
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
-  done.fetch_or(bit, std::memory_order_acq_rel);
+  if (cached) done.ctx[dev].store(current_context_id(), std::memory_order_release);
   return true;
 }
 
@@ -40,7 +58,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-__device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_error_word, code); }
+__device__ __forceinline__ void record_error(unsigned int code) { atomicOr(&g_error_word, 1u << (code & 31u)); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

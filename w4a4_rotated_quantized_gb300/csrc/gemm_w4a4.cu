@@ -1094,6 +1094,19 @@ static int pick_bn_pair(int64_t M, int64_t N, int pairs) {
   return best;
 }
 
+// The launch plan of one GEMM on a GPU with `sms` SMs: the CTA-pair kernel
+// (form 2) for M > 128 with an even k-block count, else the one-SM kernel
+// (form 1), and the N-tile width each would use.
+static void plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn) {
+  if (M > BM && sms >= 2 && (K / BK) % 2 == 0) {
+    *form = 2;
+    *bn = pick_bn_pair(M, N, sms / 2);
+  } else {
+    *form = 1;
+    *bn = pick_bn(M, N, sms);
+  }
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1123,14 +1136,15 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   const int sms = sm_count();
   if (sms <= 0) return QUAROT_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (M > BM && sms >= 2 && (K / BK) % 2 == 0) {
+  int form = 0, bn = 0;
+  plan(M, N, K, sms, &form, &bn);
+  if (form == 2) {
     // 2-SM path: clusters of two CTAs, one 256 x BN tile per pair (its
     // converters take k-blocks in pairs, so K % 256 == 0)
     const int pairs = sms / 2;
-    const int bn = pick_bn_pair(M, N, pairs);
     CUtensorMap ta, tb;
     if (!make_map(&ta, a_q, M, K, pair::BM) || !make_map(&tb, w_q, N, K, bn / 2)) return QUAROT_ERR_CUDA;
-    static std::atomic<unsigned long long> pattr{0};
+    static quarot::AttrCache pattr;
     if (!smem_attr_once(pair::w4a4_gemm_pair_kernel, pair::SMEM_BYTES, pattr)) return QUAROT_ERR_LAUNCH;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
     const int64_t npairs = tiles < pairs ? tiles : pairs;
@@ -1151,10 +1165,9 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
                                              int(M), int(N), int(K), bn, static_cast<__half*>(y), acc_out);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
   }
-  const int bn = pick_bn(M, N, sms);
   CUtensorMap ta, tb;
   if (!make_map(&ta, a_q, M, K, BM) || !make_map(&tb, w_q, N, K, bn)) return QUAROT_ERR_CUDA;
-  static std::atomic<unsigned long long> attr{0};
+  static quarot::AttrCache attr;
   if (!smem_attr_once(w4a4_gemm_kernel, SMEM_BYTES, attr)) return QUAROT_ERR_LAUNCH;
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
   const unsigned grid = unsigned(tiles < sms ? tiles : sms);
@@ -1162,4 +1175,12 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
       ta, tb, static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale), int(M), int(N),
       int(K), bn, static_cast<__half*>(y), acc_out);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+extern "C" int quarot_w4a4_gemm_plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn) {
+  using namespace quarot::gemm;
+  if (M <= 0 || N <= 0 || K <= 0 || sms <= 0 || form == nullptr || bn == nullptr) return QUAROT_ERR_INVALID_ARG;
+  if (K % BK != 0 || K > MAX_K) return QUAROT_ERR_UNSUPPORTED;
+  plan(M, N, K, sms, form, bn);
+  return QUAROT_OK;
 }

@@ -144,8 +144,8 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
 }
 
 // ------------------------------------------------------------------ decode
-constexpr int HD = 128;       // head_dim of the decode kernel
-constexpr int MAXG = 8;       // query heads per KV head
+constexpr int HD = kDecodeHeadDim;     // head_dim of the decode kernel
+constexpr int MAXG = kDecodeMaxGroup;  // query heads per KV head
 constexpr int CHUNK = 256;    // smallest split; the workspace is sized for T / CHUNK splits
 constexpr int DT = 128;       // threads per CTA
 
@@ -769,7 +769,7 @@ static int decode_impl(const void* q, const uint8_t* k_q, const void* k_s, const
                       (!ASYM || (!mis(k_z, 16) && !mis(v_z, 16)));
   int lrc = QUAROT_OK;
   auto args = [&](auto kern, size_t smem) {
-    static std::atomic<unsigned long long> attr[4];  // per group size: the kernels differ
+    static quarot::AttrCache attr[4];  // per group size: the kernels differ
     const int slot = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
     if (!smem_attr_once(kern, int(smem), attr[slot])) {
       lrc = QUAROT_ERR_LAUNCH;

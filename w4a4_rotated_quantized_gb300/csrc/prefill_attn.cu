@@ -435,10 +435,14 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
       }
       for (int i = 0; ok && i < nkt; ++i) {
         if (i + 1 < nkt) {
-          // buffer (i+1) % 2 held P(i-1), the A operand of O += P(i-1) V,
-          // issued before: the tensor pipe runs one thread's MMAs in issue
-          // order, so S(i+1) overwrites it only after that product read it
+          // Buffer (i+1) % 2 holds P(i-1), the A operand of O += P(i-1) V.
+          // The PTX ISA orders two tcgen05.mma of one thread only when they
+          // share the accumulator and the shape; S(i+1) and O += P(i-1) V do
+          // not, so S(i+1) waits for the commit of O += P(i-1) V (phase i-1
+          // of o_done: the wait before S(i) made phase i-2 complete, so the
+          // parity cannot alias an older phase).
           if (!mbar_wait_bounded(&k_full[(i + 1) % SK], uint32_t(((i + 1) / SK) & 1), abort_flag)) break;
+          if (i > 0 && !mbar_wait_bounded(o_done, uint32_t((i - 1) & 1), abort_flag)) break;
           fence_after();
           issue_s(i + 1);
         }
@@ -755,7 +759,12 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
     xl[hh * BQ + r] = l_run;
     ok = ok && pair_exchange(&lbar[qd], 0);
     const float l_tot = xl[r] + xl[BQ + r];
-    if (ok && warp_ok(mbar_wait_bounded(o_done, uint32_t((nkt - 1) & 1), abort_flag))) {
+    // The last O += P V is complete when the issuer's final commit (drain,
+    // one phase per launch) is.  A parity wait on o_done could not tell: the
+    // last score buffer this warp waited for was issued before O += P(nkt-2) V,
+    // so o_done may still be two phases short, and its parity then reads as
+    // phase nkt-1 complete.
+    if (ok && warp_ok(mbar_wait_bounded(drain, 0u, abort_flag))) {
       fence_after();
       const float inv_l = 1.0f / l_tot;
       const uint32_t o_t = tmem + lane_off + COL_O + uint32_t(64 * hh);
@@ -824,8 +833,8 @@ extern "C" int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (G >= 2) {
     // CTA pairs: two query heads of a GQA group share each converted tile
-    static std::atomic<unsigned long long> attr2{0};
-    if (!quarot::smem_attr_once(prefill_attn_kernel<true>, Plan<true>::SMEM_BYTES, attr2)) return QUAROT_ERR_CUDA;
+    static quarot::AttrCache attr2;
+    if (!quarot::smem_attr_once(prefill_attn_kernel<true>, Plan<true>::SMEM_BYTES, attr2)) return QUAROT_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));  // Hq is even (G >= 2): whole pairs
     cfg.blockDim = dim3(NTHREADS);
@@ -842,8 +851,8 @@ extern "C" int quarot_prefill_attn(const void* q, const uint8_t* k_q, const void
                                              int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, oh);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
   }
-  static std::atomic<unsigned long long> attr1{0};
-  if (!quarot::smem_attr_once(prefill_attn_kernel<false>, Plan<false>::SMEM_BYTES, attr1)) return QUAROT_ERR_CUDA;
+  static quarot::AttrCache attr1;
+  if (!quarot::smem_attr_once(prefill_attn_kernel<false>, Plan<false>::SMEM_BYTES, attr1)) return QUAROT_ERR_LAUNCH;
   prefill_attn_kernel<false><<<dim3(unsigned(grid)), dim3(NTHREADS), Plan<false>::SMEM_BYTES, st>>>(
       qh, k_q, ksh, v_q, vsh, int(B), int(Hq), int(Hkv), int(T), int(T_max), qscale, causal, oh);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;

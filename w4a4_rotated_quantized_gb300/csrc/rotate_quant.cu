@@ -585,7 +585,7 @@ static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* si
                       void* s, float* rot, cudaStream_t st) {
   using PL = SegPlan<MSEG, STAGED>;
   auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS>;
-  static std::atomic<unsigned long long> attr_done{0};
+  static quarot::AttrCache attr_done;
   static std::atomic<int> per_sm_dev[64];  // resident CTAs per SM on devices 0..63; 0 until measured
   if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
   int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
@@ -617,7 +617,7 @@ static int launch_rq_t(const void* x, int64_t M, int64_t ld_x, const int8_t* sig
   auto kern = rotate_quant_kernel<LOGP, M12, RMS, H16>;
   // fp16(1/sqrt(d)), rounded once from double (used by the FP16 variant)
   const float h16_c = __half2float(__double2half(1.0 / sqrt(double(PL::D))));
-  static std::atomic<unsigned long long> attr_done{0};
+  static quarot::AttrCache attr_done;
   if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
   const int64_t blocks = (M + PL::RPC - 1) / PL::RPC;
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
