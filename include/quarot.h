@@ -314,6 +314,25 @@ int quarot_decode_attn_asym(const void* q, const uint8_t* k_q, const void* k_s, 
                             int64_t Hkv, int64_t d, int64_t T, int64_t T_max, float sm_scale, int unrotate_out,
                             void* out, void* workspace, size_t ws_bytes, void* stream);
 
+/* quarot_legacy_imma_probe -- a measurement utility: one launch that issues
+ * nothing but the legacy warp-level integer tensor-core instruction,
+ * mma.sync s8 m16n8k32 (bits = 8) or s4 m16n8k64 (bits = 4), from registers,
+ * in eight independent chains per warp on every SM.  [S] "Kernel
+ * Implementation and Hardware Efficiency" runs its 4-bit GEMM on this
+ * instruction class (CUTLASS INT4 on Ampere); the probe measures the rate it
+ * reaches on this GPU, context for the tcgen05 GEMM's throughput.
+ *
+ *   bits     8 or 4
+ *   iters    loop trips per warp (> 0); each trip issues 8 instructions
+ *   sink     int32 device word, 4-byte aligned (written only in a case that
+ *            keeps the compiler from removing the arithmetic)
+ *   ops      host int64: receives the integer operations the launch performs
+ *            (2 per multiply-accumulate); time the launch with events on
+ *            `stream` and divide
+ * Returns QUAROT_ERR_INVALID_ARG for other widths, iters <= 0 or null
+ * pointers.  The pages have no such entry point. */
+int quarot_legacy_imma_probe(int bits, int iters, int32_t* sink, int64_t* ops, void* stream);
+
 /*
  * quarot_decode_attn_static -- quarot_decode_attn for callers that cannot
  * allocate device memory when they run decode (a plain C host without an

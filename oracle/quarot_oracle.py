@@ -7,10 +7,13 @@ and by ``bench.py``'s CPU-baseline leg, and by nothing else: the product path
 module imports nothing from the product.  It shares no code with the CUDA
 path; the only common module is ``workloads`` (seeded random inputs).
 
-Arithmetic is numpy float64 with explicit dense Hadamard matrices (no fast
-transform), an exact integer GEMM, and float32/float16 only where the method
+Arithmetic is numpy float64 with explicit dense Hadamard matrices, an exact
+integer GEMM, and float32/float16 only where the method
 fixes the storage precision (rotated values are compared as fp32, scales are
-stored as fp16, the dequantised output is fp16).
+stored as fp16, the dequantised output is fp16).  ``rotate_fwht`` is a second,
+O(d log d) mode of the same rotation (butterflies instead of the dense
+product), pinned against the dense definition; it exists only so that the
+host baseline can be timed with the fast transform as well.
 
 Sources (page title, section):
   [S]  "QuaRot: Outlier-Free 4-Bit Inference in Rotated LLMs" (paper summary
@@ -161,6 +164,48 @@ def rotate_f64(x: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
     if signs is not None:
         xs = xs * np.asarray(signs, dtype=np.float64)[None, :]
     return (_apply_dense(xs, hadamard(d)) / math.sqrt(d)).reshape(x.shape)
+
+
+def fwht_rows(xs: np.ndarray) -> np.ndarray:
+    """The fast Walsh-Hadamard transform of every row, y = x @ H_{2^n} (Sylvester,
+    unnormalized), in float64: n rounds of butterflies (a + b, a - b) over pairs
+    at distance h = 1, 2, 4, ..., as in [G] "The Fast Walsh-Hadamard Transform".
+    O(d log d) per row; the dense product ``_apply_dense`` is the definition."""
+    y = np.array(xs, dtype=np.float64, copy=True)
+    M, d = y.shape
+    if d < 1 or d & (d - 1):
+        raise ValueError(f"FWHT length must be a power of two, got {d}")
+    h = 1
+    while h < d:
+        v = y.reshape(M, d // (2 * h), 2, h)
+        a = v[:, :, 0, :].copy()
+        b = v[:, :, 1, :]
+        v[:, :, 0, :] = a + b
+        v[:, :, 1, :] = a - b
+        h *= 2
+    return y
+
+
+def rotate_fwht(x: np.ndarray, signs: np.ndarray | None) -> np.ndarray:
+    """The same map as ``rotate`` computed with the fast transform (the oracle's
+    O(d log d) mode, for timing on the host): signs, then the FWHT of each
+    2^n block, then (for d = 12 * 2^n) the dense H12 across the 12 blocks,
+    x~[a 2^n + b] = sum_c y[c 2^n + b] H12[c, a], scaled by 1/sqrt(d); float64,
+    returned as fp32."""
+    x = np.asarray(x)
+    d = x.shape[-1]
+    xs = x.reshape(-1, d).astype(np.float64)
+    if signs is not None:
+        xs = xs * np.asarray(signs, dtype=np.float64)[None, :]
+    if d >= 1 and d & (d - 1) == 0:
+        r = fwht_rows(xs)
+    elif d % 12 == 0 and (d // 12) & (d // 12 - 1) == 0:
+        p = d // 12
+        y = fwht_rows(xs.reshape(-1, p)).reshape(xs.shape[0], 12, p)
+        r = np.einsum("mcb,ca->mab", y, paley12().astype(np.float64)).reshape(xs.shape[0], d)
+    else:
+        raise ValueError(f"no Hadamard construction for d = {d} (need 2^n or 12*2^n)")
+    return (r / math.sqrt(d)).astype(np.float32).reshape(x.shape)
 
 
 # ---------------------------------------------------------------------------

@@ -749,3 +749,31 @@ def test_decode_unrotated_close_to_float_attention():
         p /= p.sum()
         ref[0, h] = p @ v[0, :, g].astype(np.float64)
     assert O.rel_fro(out, ref) < 0.25
+
+
+@pytest.mark.parametrize("d", [1, 2, 16, 256, 4096, 24, 96, 3072, 12288])
+def test_fwht_mode_equals_dense_rotation(d):
+    """The oracle's fast mode computes the dense definition: equal in float64
+    to the dense product up to rounding (the two orders of the same sums), and
+    bit-identical in fp32 except where the double rounding straddles a tie."""
+    rng = np.random.default_rng(d)
+    x = rng.standard_normal((5, d)).astype(np.float16)
+    x[0, :] = 0
+    x[0, d // 3] = 1.0  # one-hot: +-1/sqrt(d) everywhere
+    s = W.random_signs(d, d + 1)
+    dense = O.rotate_f64(x, s)
+    fast = O.rotate_fwht(x, s).astype(np.float64)
+    scale = np.abs(dense).max(axis=1, keepdims=True)
+    assert np.all(np.abs(fast - dense) <= 2 ** -22 * scale)
+    assert np.allclose(np.abs(fast[0]), 1 / np.sqrt(d), rtol=0, atol=1e-7)
+    assert np.mean(fast.astype(np.float32) == O.rotate(x, s)) > 0.99
+
+
+def test_fwht_rows_is_the_sylvester_product():
+    """fwht_rows(x) = x @ H (unnormalized) for the Sylvester matrix, brute force."""
+    rng = np.random.default_rng(3)
+    for d in (1, 2, 4, 8, 64):
+        x = rng.standard_normal((3, d))
+        assert np.allclose(O.fwht_rows(x), x @ O.sylvester(d).astype(np.float64), atol=1e-12)
+    with pytest.raises(ValueError):
+        O.fwht_rows(np.ones((1, 12)))

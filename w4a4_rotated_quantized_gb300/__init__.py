@@ -48,6 +48,7 @@ _SIGS = {
                                           ctypes.c_float, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
     "quarot_decode_attn_static": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                                  ctypes.c_float, ctypes.c_int, _P, _P]),
+    "quarot_legacy_imma_probe": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P, ctypes.POINTER(ctypes.c_int64), _P]),
     "quarot_prefill_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                            ctypes.c_float, ctypes.c_int, _P, _P]),
     "quarot_kv_write_asym": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P,
@@ -239,6 +240,16 @@ def quarot_w4a4_gemm_plan(M: int, N: int, K: int, sms: int) -> tuple[int, int]:
     form, bn = ctypes.c_int(0), ctypes.c_int(0)
     _check(load().quarot_w4a4_gemm_plan(M, N, K, sms, ctypes.byref(form), ctypes.byref(bn)), "quarot_w4a4_gemm_plan")
     return form.value, bn.value
+
+
+def quarot_legacy_imma_probe(bits: int, iters: int, sink, stream=None) -> int:
+    """Launches the mma.sync integer-rate probe on `stream`; returns the integer
+    operations the launch performs.  `sink` is an int32 CUDA tensor."""
+    _need(sink, torch.int32, "sink")
+    ops = ctypes.c_int64(0)
+    _check(load().quarot_legacy_imma_probe(int(bits), int(iters), _ptr(sink), ctypes.byref(ops),
+                                           _stream(stream, sink.device)), "quarot_legacy_imma_probe")
+    return ops.value
 
 
 def quarot_kv_write(k, v, t_start, k_q, k_s, v_q, v_s, stream=None):
