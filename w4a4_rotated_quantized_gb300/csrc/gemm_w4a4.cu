@@ -94,6 +94,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             uint64_t* bar) {
   asm volatile(
@@ -236,6 +240,8 @@ w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   const int b_bytes = BN * BKB;
 
   if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
     for (int s = 0; s < SP; ++s) {
       mbar_init(&pk_full[s], 1);
       mbar_init(&pk_empty[s], NCONV_WARPS);
@@ -704,6 +710,8 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   const uint32_t idesc = IDESC_BASE | (uint32_t(BN >> 3) << 17);
 
   if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
     for (int s = 0; s < SP; ++s) {
       mbar_init(&pk_full[s], 1);
       mbar_init(&pk_empty[s], NCW);
@@ -743,16 +751,22 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs) {
       const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
       const int n0 = (tile % n_tiles_n) * BN + int(rank) * BNH;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      // k-blocks in pairs: the converters release packed stages in pairs (the
+      // second stage's phase completes after the first's), so one wait per
+      // pair and both k-blocks' loads issued back to back
+      for (int kb = 0; kb < nkb; kb += 2, it += 2) {
         const int s = int(it % SP);
-        if (!warp_wait(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
+        if (!warp_wait(&pk_empty[s + 1], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&pk_full[s], A_PK + b_bytes);
-          tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
-          tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            mbar_arrive_expect_tx(&pk_full[s + u], A_PK + b_bytes);
+            tma_load_2d(smem_u32(sm + OFF_AP + (s + u) * A_PK), &tmA, (kb + u) * BKB, m0, &pk_full[s + u]);
+            tma_load_2d(smem_u32(sm + OFF_BP + (s + u) * B_PK), &tmB, (kb + u) * BKB, n0, &pk_full[s + u]);
+          }
         }
         __syncwarp();
-        issued = it + 1;
+        issued = it + 2;
       }
     }
     if (warp_flag(abort_flag) && lane == 0) {
