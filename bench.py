@@ -8,6 +8,13 @@ One step = one pass of every hot-path stage on synthetic, seeded inputs:
 The headline value is W4A4 layer tokens/s: 2048 tokens per step divided by
 the device time of the step, inputs resident in HBM.
 
+The step is a mixed batch: a 2048-token chunk through the down_proj layer
+(1, 2) and a decode step of 16 other sequences (3, 4).  The two share no
+data, so each step is one CUDA graph with two branches, rotate -> GEMM on the
+launching stream and append -> decode on a forked stream, joined at the end.
+The same step with the four kernels in one chain is timed beside it
+("ms_per_step_serial"), and the bench checks that both give identical bytes.
+
 Cold-L2 protocol.  Every device time is measured with CUDA events on the
 launching stream over back-to-back launches that cycle through distinct sets
 of input and output buffers, at least 4x the L2 size in all, so that no launch
@@ -448,8 +455,25 @@ def run_ours(args):
         ]
 
     LAUNCHES_PER_STEP = 1 + 1 + 1 + 2
+    side = torch.cuda.Stream(dev)
 
     def step_fn(sd):
+        """The step's two independent branches: rotate -> GEMM on the current
+        stream, KV append -> decode on `side`, joined before the step ends."""
+        rot, gemm, kvw, dec = stages_of(sd)
+
+        def f():
+            cur = torch.cuda.current_stream(dev)
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                kvw()
+                dec()
+            rot()
+            gemm()
+            cur.wait_stream(side)
+        return f
+
+    def serial_fn(sd):
         fns = stages_of(sd)
 
         def f():
@@ -461,12 +485,13 @@ def run_ours(args):
         for _ in range(max(1, args.warmup // len(SETS) + 1)):
             step_fn(sd)()
     q.quarot_check_error(stream)
-    g_steps = []
+    g_steps, g_serial = [], []
     for sd in SETS:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step_fn(sd)()
-        g_steps.append(g)
+        for fn, lst in ((step_fn, g_steps), (serial_fn, g_serial)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(sd)()
+            lst.append(g)
     for i in range(args.warmup):
         g_steps[i % n_sets].replay()
     torch.cuda.synchronize()
@@ -507,6 +532,29 @@ def run_ours(args):
     torch.cuda.synchronize()
     step_ms_flush = float(np.mean([a.elapsed_time(b) for a, b in evs]))
 
+    # the same steps with the four kernels in one chain, cycled the same way
+    for i in range(args.warmup):
+        g_serial[i % n_sets].replay()
+    e0.record(stream)
+    for i in range(args.steps):
+        g_serial[i % n_sets].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step_ms_serial = float(e0.elapsed_time(e1)) / args.steps
+    # both forms of the step leave identical bytes in Y and the decode output
+    s0 = SETS[0]
+    g_serial[0].replay()
+    torch.cuda.synchronize()
+    y_ser, o_ser = s0["y"].clone(), s0["out"].clone()
+    s0["y"].zero_()
+    s0["out"].zero_()
+    g_steps[0].replay()
+    torch.cuda.synchronize()
+    q.quarot_check_error(stream)
+    if not (torch.equal(y_ser, s0["y"]) and torch.equal(o_ser, s0["out"])):
+        raise RuntimeError("the two-branch step differs from the serial step")
+    del y_ser, o_ser
+
     # ---------------- per-stage device times: back-to-back over the step's buffer sets
     stage_names = ["rotate_quant", "w4a4_gemm", "kv_write_append", "decode_attn"]
     per_set = [stages_of(sd) for sd in SETS]
@@ -537,6 +585,7 @@ def run_ours(args):
     y_h = [torch.empty_like(s0["y"], device="cpu").pin_memory() for _ in range(2)]
     o_h = [torch.empty_like(s0["out"], device="cpu").pin_memory() for _ in range(2)]
     h2d_st, d2h_st = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dec_st = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of the slot copied
     ev_comp = [torch.cuda.Event() for _ in range(2)]  # kernels of the slot done
     ev_out = [torch.cuda.Event() for _ in range(2)]   # results of the slot copied out
@@ -555,10 +604,12 @@ def run_ours(args):
             stream.wait_event(ev_in[sl])
             if i >= 2:
                 stream.wait_event(ev_out[sl])  # slot's results already read back
+            dec_st.wait_stream(stream)  # the decode branch, forked as in the timed step
+            q.quarot_kv_write(kd[sl], vd[sl], T - 1, *s0["cache"], stream=dec_st)
+            q.quarot_decode_attn(qd[sl], *s0["cache"], T=T, out=od[sl], workspace=s0["wsp"], stream=dec_st)
             q.quarot_rotate_quant(xd[sl], st, q_out=aqd[sl], scale_out=asd[sl], stream=stream)
             q.quarot_w4a4_gemm(aqd[sl], asd[sl], s0["wq"], s0["wsc"], y=yd[sl], stream=stream)
-            q.quarot_kv_write(kd[sl], vd[sl], T - 1, *s0["cache"], stream=stream)
-            q.quarot_decode_attn(qd[sl], *s0["cache"], T=T, out=od[sl], workspace=s0["wsp"], stream=stream)
+            stream.wait_stream(dec_st)
             ev_comp[sl].record(stream)
             d2h_st.wait_event(ev_comp[sl])
             with torch.cuda.stream(d2h_st):
@@ -605,19 +656,23 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "ms_per_step_flush": step_ms_flush,
+        "ms_per_step_serial": step_ms_serial,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4+f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens_per_step": M_TOK,
                    "l2": (f"inputs larger than L2: steps cycle through {n_sets} distinct buffer sets "
                           f"({n_sets * set_bytes(SETS[0]) / 1e6:.0f} MB >= {L2_CYCLE}x L2 {l2 / 1e6:.0f} MB), "
                           f"back-to-back; ms_per_step_flush: one set, 2x L2 write before each step"),
-                   "parallelism": f"replicas x{ws}", "launch": "CUDA graph per step"},
+                   "parallelism": f"replicas x{ws}",
+                   "launch": ("CUDA graph per step, two branches joined: rotate+quant -> GEMM | "
+                              "KV append -> decode (a mixed batch: the layer's 2048-token chunk and "
+                              "16 decoding sequences share no data); ms_per_step_serial: one chain")},
         "roofline": {"bound": "tensor", "kernel": "w4a4_gemm", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": GEMM_TRAFFIC_BYTES,
                      "peak_source": f"{peaks['source']} bf16 burst x 2 (fp8/bf16 nominal ratio)"},
         "stages": stages,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipeline": "per-step H2D, kernels and D2H on three streams, double-buffered; no L2 flush "
-                            "(per-step traffic > L2)"},
+                "pipeline": "per-step H2D, kernels (two branches, as in the timed step) and D2H on "
+                            "four streams, double-buffered; no L2 flush (per-step traffic > L2)"},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": dict(clocks.summary(), samples_in_timed_region=timed_samples),
     }
