@@ -51,9 +51,9 @@ import workloads as W  # noqa: E402
 
 M_TOK, K_DIM, N_OUT = 2048, 12288, 4096
 # DRAM bytes (read + write) of one launch of the down_proj GEMM, from one ncu
-# capture of this kernel (37.808384 MB read + 0.553728 MB written); None
-# whenever the kernel has changed since that capture.
-GEMM_TRAFFIC_BYTES = 38_362_112
+# capture of this kernel; None whenever the kernel has changed since that
+# capture.
+GEMM_TRAFFIC_BYTES = None
 KV = W.CONFIGS["kv4"]
 METRIC = "W4A4 layer tokens/s"
 WORKLOAD = ("down_proj W4A4 layer 2048x12288->4096 (H12(x)H1024 rotate+quant, INT4 GEMM, fp16 out) "
@@ -690,6 +690,24 @@ def run_ours(args):
     return 0
 
 
+def _gemm_a8_case(q, tm, dev, g, M, N, K, wq_, ws_, fp8_peak, rot_ms):
+    """quarot_w4a4_gemm_a8 (activations as operand bytes, seeded uniform codes)
+    under the cycled protocol; the layer rate uses quarot_rotate_quant_a8."""
+    import torch
+
+    a8 = torch.randint(0, 16, (M, K), dtype=torch.uint8, generator=g).to(dev)
+    rs = torch.randint(-8 * K // 16, 8 * K // 16, (M,), dtype=torch.int32, generator=g).to(dev)
+    as_ = (torch.rand(M, generator=g) * 0.1 + 0.01).half().to(dev)
+    nbytes = M * K + N * K // 2 + M * N * 2
+    n = tm.sets_for(nbytes, cap=32)
+    sets = [(a8.clone(), wq_.clone(), torch.empty((M, N), dtype=torch.float16, device=dev)) for _ in range(n)]
+    fns = [(lambda a=a, w=w, y=y: q.quarot_w4a4_gemm_a8(a, rs, as_, w, ws_, y=y)) for a, w, y in sets]
+    ms = tm.cycled(fns)
+    tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+    return {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak, "buffer_sets": n,
+            "layer_tokens_per_s": M / ((ms + rot_ms) / 1e3)}
+
+
 def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
     """The other measured workloads (rank 0), each under the cycled cold-L2
     protocol unless labelled warm: the HBM-roof rotate+quant of 2048 x 4096 and
@@ -705,13 +723,17 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
     def rot_case(name, fn_kind, x, s_t, extra=None):
         M, dd = x.shape
         xt = torch.from_numpy(x).to(dev)
-        nbytes = M * dd * 2 + M * dd // 2 + M * 2
+        a8 = fn_kind == "a8"  # codes as operand bytes (d per row) plus int32 row sums
+        nbytes = M * dd * 2 + (M * dd + M * 6 if a8 else M * dd // 2 + M * 2)
         n = tm.sets_for(nbytes)
-        bufs = [(xt if i == 0 else xt.clone(), torch.empty((M, dd // 2), dtype=torch.uint8, device=dev),
+        bufs = [(xt if i == 0 else xt.clone(), torch.empty((M, dd if a8 else dd // 2), dtype=torch.uint8, device=dev),
                  torch.empty((M,), dtype=torch.float16, device=dev)) for i in range(n)]
+        rsb = torch.empty((M,), dtype=torch.int32, device=dev)
 
         def mk(b):
             xi, qo, so = b
+            if a8:
+                return lambda: q.quarot_rotate_quant_a8(xi, s_t, a8_out=qo, scale_out=so, rowsum_out=rsb)
             if fn_kind == "rotate":
                 return lambda: q.quarot_rotate_quant(xi, s_t, q_out=qo, scale_out=so)
             if fn_kind == "rmsnorm":
@@ -740,6 +762,10 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
     sst = torch.from_numpy(ss).to(dev)
     rot_ms = {M: rot_case(f"rotate_quant_{M}x4096", "rotate", np.ascontiguousarray(xs[:M]), sst)
               for M in (512, 2048, 8192)}
+    # the tensor-core operand form (one byte per code, row sums) for the A8 GEMM
+    rot8_ms = {M: rot_case(f"rotate_quant_a8_{M}x4096", "a8", np.ascontiguousarray(xs[:M]), sst)
+               for M in (512, 2048, 8192)}
+    rot8_dp = rot_case("rotate_quant_a8_2048x12288", "a8", x_dp, st)
 
     # ---- KV cache: bulk write of the whole kv4 cache, decode batch sweep
     c = W.CONFIGS["kv4"]
@@ -831,6 +857,9 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
             res[f"w4a4_gemm_{M}x{K}x{N}"] = {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak, "buffer_sets": n,
                                              "layer_tokens_per_s": M / ((ms + rot_ms[M]) / 1e3)}
             del sets, fns
+            res[f"w4a4_gemm_a8_{M}x{K}x{N}"] = _gemm_a8_case(q, tm, dev, g, M, N, K, wq_, ws_, fp8_peak, rot8_ms[M])
+    res["w4a4_gemm_a8_2048x12288x4096"] = _gemm_a8_case(q, tm, dev, g, M_TOK, N_OUT, K_DIM, s0["wq"], s0["wsc"],
+                                                          fp8_peak, rot8_dp)
     # the bench GEMM with its operands warm in L2 (one buffer set, back-to-back)
     ms_w = tm.warm(lambda: q.quarot_w4a4_gemm(s0["aq"], s0["asx"], s0["wq"], s0["wsc"], y=s0["y"]))
     tf = 2.0 * M_TOK * N_OUT * K_DIM / (ms_w / 1e3) / 1e12
@@ -850,6 +879,17 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
         tops = ops / (a.elapsed_time(b) / 1e3) / 1e12
         res[f"int{bits}_tc_legacy_mma_sync"] = {"TOPS": tops, "instruction": f"mma.sync {label}",
                                                 "gemm_2048x12288x4096_frac_of_it": None}
+    # the fp16 form (m16n8k16, fp32 accumulators): the instruction of the
+    # decode and prefill attention kernels, whose tensor share it bounds
+    for _ in range(2):
+        q.quarot_legacy_imma_probe(16, 256, sink)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    ops = q.quarot_legacy_imma_probe(16, 8192, sink)
+    b.record(stream)
+    b.synchronize()
+    res["f16_tc_legacy_mma_sync"] = {"TFLOPS": ops / (a.elapsed_time(b) / 1e3) / 1e12,
+                                     "instruction": "mma.sync f16 m16n8k16, f32 accumulate"}
     gemm_tops = res.get("w4a4_gemm_2048x4096x12288", {}).get("TOPS")
     for bits in (8, 4):
         r = res[f"int{bits}_tc_legacy_mma_sync"]

@@ -187,6 +187,48 @@ int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const uint8_t* w_q
                      const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
                      int32_t* acc_out, void* stream);
 
+/*
+ * quarot_rotate_quant_a8 -- quarot_rotate_quant with the codes written in the
+ * tensor-core operand form that quarot_w4a4_gemm_a8 reads, instead of packed
+ * nibbles.  [S] Stage 2a (online Hadamard, per-token symmetric INT4
+ * quantization): the same codes and scales as quarot_rotate_quant, bit for
+ * bit.  The pages have no such format: sm_103a tensor cores take 8-bit
+ * operands only, so every 4-bit code is widened to a byte before an MMA; this
+ * entry point widens each activation code once, where it is produced, rather
+ * than once per output-column tile inside the GEMM.
+ *
+ *   x, M, d, ld_x, signs, clip_ratio   as quarot_rotate_quant; d = 4096 or
+ *                                      12288 (else QUAROT_ERR_UNSUPPORTED)
+ *   a8_out      uint8 [M, d], 16-byte aligned: byte 8g + j holds u = v + 8
+ *               (0..15) of code 8g + p(j), p = (0, 2, 4, 6, 1, 3, 5, 7); the
+ *               e4m3 byte with that bit pattern has the value u * 2^-9
+ *   scale_out   fp16 [M], 2-byte aligned
+ *   rowsum_out  int32 [M], 4-byte aligned: sum over the row's codes v
+ * Misaligned pointers return QUAROT_ERR_ALIGNMENT before any launch.
+ */
+int quarot_rotate_quant_a8(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                           float clip_ratio, uint8_t* a8_out, void* scale_out, int32_t* rowsum_out,
+                           void* stream);
+
+/*
+ * quarot_w4a4_gemm_a8 -- quarot_w4a4_gemm with the activations in the form
+ * quarot_rotate_quant_a8 writes: the same exact accumulator and the same fp16
+ * output, bit for bit.  [S] Stage 2b, "Kernel Implementation".  The weights
+ * stay packed INT4 (4 bits per code in memory); only their conversion runs
+ * inside the GEMM.
+ *
+ *   a8        uint8 [M, K] (quarot_rotate_quant_a8 layout), 16-byte aligned
+ *   a_rowsum  int32 [M] code sums of the rows, 4-byte aligned
+ *   a_scale, w_q, w_scale, y, acc_out   as quarot_w4a4_gemm
+ *   M, N      >= 0; K % 256 == 0, 256 <= K <= 65536 (else QUAROT_ERR_UNSUPPORTED)
+ * Runs on CTA pairs (thread-block clusters of two); a GPU with fewer than two
+ * SMs gets QUAROT_ERR_UNSUPPORTED.  Misaligned pointers return
+ * QUAROT_ERR_ALIGNMENT before any launch.
+ */
+int quarot_w4a4_gemm_a8(const uint8_t* a8, const int32_t* a_rowsum, const void* a_scale, const uint8_t* w_q,
+                        const void* w_scale, int64_t M, int64_t N, int64_t K, void* y, int32_t* acc_out,
+                        void* stream);
+
 /* quarot_w4a4_gemm_plan -- which kernel and N-tile width quarot_w4a4_gemm
  * launches for an M x N x K problem on a GPU with `sms` SMs (a host-only
  * query: it touches no device).  *form = 2 for the CTA-pair kernel (M > 128
@@ -315,18 +357,20 @@ int quarot_decode_attn_asym(const void* q, const uint8_t* k_q, const void* k_s, 
                             void* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* quarot_legacy_imma_probe -- a measurement utility: one launch that issues
- * nothing but the legacy warp-level integer tensor-core instruction,
- * mma.sync s8 m16n8k32 (bits = 8) or s4 m16n8k64 (bits = 4), from registers,
- * in eight independent chains per warp on every SM.  [S] "Kernel
+ * nothing but one legacy warp-level tensor-core instruction, mma.sync s8
+ * m16n8k32 (bits = 8), s4 m16n8k64 (bits = 4) or f16 m16n8k16 with fp32
+ * accumulators (bits = 16, the instruction of the decode and prefill
+ * attention kernels), from registers, in eight independent chains per warp
+ * on every SM.  [S] "Kernel
  * Implementation and Hardware Efficiency" runs its 4-bit GEMM on this
  * instruction class (CUTLASS INT4 on Ampere); the probe measures the rate it
  * reaches on this GPU, context for the tcgen05 GEMM's throughput.
  *
- *   bits     8 or 4
+ *   bits     8, 4 or 16
  *   iters    loop trips per warp (> 0); each trip issues 8 instructions
  *   sink     int32 device word, 4-byte aligned (written only in a case that
  *            keeps the compiler from removing the arithmetic)
- *   ops      host int64: receives the integer operations the launch performs
+ *   ops      host int64: receives the operations the launch performs
  *            (2 per multiply-accumulate); time the launch with events on
  *            `stream` and divide
  * Returns QUAROT_ERR_INVALID_ARG for other widths, iters <= 0 or null

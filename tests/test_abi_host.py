@@ -184,3 +184,37 @@ def test_gemm_plan_query(lib):
     assert f(8, 8, 100, 152, ctypes.byref(form), ctypes.byref(bn)) == 2
     assert f(8, 8, 131072, 152, ctypes.byref(form), ctypes.byref(bn)) == 2
     assert f(8, 8, 128, 152, None, ctypes.byref(bn)) == 1
+
+
+def test_legacy_probe_validation(lib):
+    """The mma.sync rate probe accepts widths 8, 4 and 16 only, and rejects
+    bad arguments before touching the device."""
+    ops = ctypes.c_int64(0)
+    f = lib.quarot_legacy_imma_probe
+    for bits in (0, 2, 12, 32):
+        assert f(bits, 8, FAKE, ctypes.byref(ops), None) == 1
+    assert f(16, 0, FAKE, ctypes.byref(ops), None) == 1
+    assert f(16, 8, None, ctypes.byref(ops), None) == 1
+    assert f(16, 8, FAKE, None, None) == 1
+    assert f(16, 8, P(0x10002), ctypes.byref(ops), None) == 3
+
+
+def test_a8_validation(lib):
+    """The tensor-core operand form of the layer rejects bad arguments before
+    any launch: widths other than 4096 / 12288, K not a multiple of 256,
+    null and misaligned pointers."""
+    f = lib.quarot_rotate_quant_a8
+    assert f(FAKE, 0, 4096, 4096, None, 1.0, FAKE, FAKE, FAKE, None) == 0  # M = 0 no-op
+    assert f(FAKE, 4, 2048, 2048, None, 1.0, FAKE, FAKE, FAKE, None) == 2
+    assert f(FAKE, 4, 4096, 4096, None, 0.0, FAKE, FAKE, FAKE, None) == 1
+    assert f(FAKE, 4, 4096, 4096, None, 1.0, FAKE, FAKE, None, None) == 1
+    assert f(FAKE, 4, 4096, 4096, None, 1.0, P(0x10008), FAKE, FAKE, None) == 3
+    assert f(FAKE, 4, 4096, 4096, None, 1.0, FAKE, FAKE, P(0x10002), None) == 3
+    g = lib.quarot_w4a4_gemm_a8
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 256, FAKE, None, None) == 0  # M = 0 no-op
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 8, 128, FAKE, None, None) == 2  # K % 256
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 8, 131072, FAKE, None, None) == 2
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 8, 256, FAKE, None, None) == 1
+    assert g(FAKE, None, FAKE, FAKE, FAKE, 8, 8, 256, FAKE, None, None) == 1
+    assert g(FAKE, P(0x10002), FAKE, FAKE, FAKE, 8, 8, 256, FAKE, None, None) == 3
+    assert g(P(0x10008), FAKE, FAKE, FAKE, FAKE, 8, 8, 256, FAKE, None, None) == 3

@@ -8,7 +8,9 @@ missing the calls raise ``QuarotError``.
 
 Functions (same names as the C entry points):
     quarot_rotate_quant, quarot_w4a4_gemm, quarot_kv_write,
-    quarot_decode_attn, quarot_decode_workspace_bytes, quarot_check_error
+    quarot_decode_attn, quarot_decode_workspace_bytes, quarot_check_error,
+    and the tensor-core operand form of the layer: quarot_rotate_quant_a8,
+    quarot_w4a4_gemm_a8
 """
 from __future__ import annotations
 
@@ -40,6 +42,8 @@ _SIGS = {
                                                    _P, _P]),
     "quarot_crosshead_rotate_quant": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_w4a4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "quarot_rotate_quant_a8": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "quarot_w4a4_gemm_a8": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "quarot_w4a4_gemm_plan": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_int)]),
     "quarot_kv_write": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -231,6 +235,58 @@ def quarot_w4a4_gemm(a_q, a_scale, w_q, w_scale, y=None, acc_out=None, stream=No
     st = load().quarot_w4a4_gemm(_ptr(a_q), _ptr(a_scale), _ptr(w_q), _ptr(w_scale), M, N, 2 * Kh, _ptr(y),
                                  _ptr(acc_out), _stream(stream, dev))
     _check(st, "quarot_w4a4_gemm")
+    return y, acc_out
+
+
+def quarot_rotate_quant_a8(x, signs=None, clip_ratio: float = 1.0, a8_out=None, scale_out=None, rowsum_out=None,
+                           stream=None):
+    """x: fp16 [M, d] (d = 4096 or 12288) -> the codes in tensor-core operand
+    form: (uint8 [M, d] offset codes in the GEMM's K order, scale fp16 [M],
+    row code sums int32 [M])."""
+    _need(x, torch.float16, "x")
+    dev = x.device
+    M, d = x.shape
+    if signs is not None:
+        _need(signs, torch.int8, "signs", dev)
+    if a8_out is None:
+        a8_out = torch.empty((M, d), dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float16, device=dev)
+    if rowsum_out is None:
+        rowsum_out = torch.empty((M,), dtype=torch.int32, device=dev)
+    _need(a8_out, torch.uint8, "a8_out", dev)
+    _need(scale_out, torch.float16, "scale_out", dev)
+    _need(rowsum_out, torch.int32, "rowsum_out", dev)
+    st = load().quarot_rotate_quant_a8(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(a8_out),
+                                       _ptr(scale_out), _ptr(rowsum_out), _stream(stream, dev))
+    _check(st, "quarot_rotate_quant_a8")
+    return a8_out, scale_out, rowsum_out
+
+
+def quarot_w4a4_gemm_a8(a8, a_rowsum, a_scale, w_q, w_scale, y=None, acc_out=None, stream=None,
+                        want_acc: bool = False):
+    """a8 uint8 [M, K] (quarot_rotate_quant_a8 form), w_q uint8 [N, K/2] ->
+    (y fp16 [M, N], acc int32 [M, N] or None)."""
+    _need(a8, torch.uint8, "a8")
+    dev = a8.device
+    _need(a_rowsum, torch.int32, "a_rowsum", dev)
+    _need(w_q, torch.uint8, "w_q", dev)
+    _need(a_scale, torch.float16, "a_scale", dev)
+    _need(w_scale, torch.float16, "w_scale", dev)
+    M, K = a8.shape
+    N, Kh = w_q.shape
+    if K != 2 * Kh:
+        raise QuarotError(1, "a8 and w_q disagree on K")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    if acc_out is None and want_acc:
+        acc_out = torch.empty((M, N), dtype=torch.int32, device=dev)
+    _need(y, torch.float16, "y", dev)
+    if acc_out is not None:
+        _need(acc_out, torch.int32, "acc_out", dev)
+    st = load().quarot_w4a4_gemm_a8(_ptr(a8), _ptr(a_rowsum), _ptr(a_scale), _ptr(w_q), _ptr(w_scale), M, N, K,
+                                    _ptr(y), _ptr(acc_out), _stream(stream, dev))
+    _check(st, "quarot_w4a4_gemm_a8")
     return y, acc_out
 
 

@@ -42,6 +42,11 @@
 // pipe idled between k-blocks.  Every wait is bounded; an expired wait
 // records QUAROT_ERR_TIMEOUT and the CTA drains its copies and MMAs, frees
 // TMEM and returns.
+//
+// The file holds three kernels: the one-SM kernel above (M <= 128 or an odd
+// k-block count), the CTA-pair kernel (namespace pair) and the CTA-pair kernel
+// for activations already widened to operand bytes by quarot_rotate_quant_a8
+// (namespace pair::a8, entry point quarot_w4a4_gemm_a8).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -493,7 +498,12 @@ namespace pair {
 // and four converter warps per scheduler to hide it.
 constexpr int BM = 128;          // rows per CTA (256 per pair)
 constexpr int BNH_MAX = 112;     // weight rows per CTA (BN <= 224)
-constexpr int SP = 6;            // packed ring stages (6 lets the loads run ~1.5 us ahead)
+// Packed ring: SP k-block stages, loaded as SP / 2 double stages.  One TMA box
+// of 128-byte rows (128B swizzle) covers k-blocks kb and kb + 1 of a row, so
+// stage pair (s, s + 1) is one box per operand behind the barriers of stage s
+// (the barriers of odd stages are unused).  Half as many TMA row requests as
+// 64-byte boxes: 86.1 -> 85.0 us at 2048 x 4096 x 12288.
+constexpr int SP = 6;
 constexpr int S = 8;             // converted stages (A in tensor memory, W in shared memory)
 constexpr int NAW = 8, NBW = 8;  // A / W converter warps
 constexpr int NCW = NAW + NBW;
@@ -756,21 +766,18 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       // pair and both k-blocks' loads issued back to back
       for (int kb = 0; kb < nkb; kb += 2, it += 2) {
         const int s = int(it % SP);
-        if (!warp_wait(&pk_empty[s + 1], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
+        if (!warp_wait(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
         if (lane == 0) {
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            mbar_arrive_expect_tx(&pk_full[s + u], A_PK + b_bytes);
-            tma_load_2d(smem_u32(sm + OFF_AP + (s + u) * A_PK), &tmA, (kb + u) * BKB, m0, &pk_full[s + u]);
-            tma_load_2d(smem_u32(sm + OFF_BP + (s + u) * B_PK), &tmB, (kb + u) * BKB, n0, &pk_full[s + u]);
-          }
+          mbar_arrive_expect_tx(&pk_full[s], 2 * (A_PK + b_bytes));
+          tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
+          tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
         }
         __syncwarp();
         issued = it + 2;
       }
     }
     if (warp_flag(abort_flag) && lane == 0) {
-      for (long j = (issued > SP ? issued - SP : 0); j < issued; ++j)
+      for (long j = (issued > SP ? issued - SP : 0); j < issued; j += 2)
         mbar_wait_bounded(&pk_full[j % SP], uint32_t((j / SP) & 1), nullptr);
     }
   } else if (warp == 1) {
@@ -842,9 +849,10 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     // 32-bit shared addresses, swizzled chunk offsets hoisted out of the loop:
     // the packed half row is 16-byte chunks 2 part and 2 part + 1 (64B swizzle),
     // the unpacked half row chunks 4 part .. 4 part + 3 (128B swizzle)
-    const uint32_t swz_src = uint32_t(r >> 1) & 3u, swz_dst = uint32_t(r) & 7u;
-    const uint32_t src_row = smem_u32(sm + (is_a ? OFF_AP : OFF_BP)) + uint32_t(r) * 64u;
-    const uint32_t src0 = src_row + (((2u * part) ^ swz_src) << 4), src1 = src_row + (((2u * part + 1u) ^ swz_src) << 4);
+    const uint32_t swz_dst = uint32_t(r) & 7u;
+    const uint32_t src_row = smem_u32(sm + (is_a ? OFF_AP : OFF_BP)) + uint32_t(r) * 128u;
+    const uint32_t src0 = src_row + (((2u * part) ^ swz_dst) << 4), src1 = src_row + (((2u * part + 1u) ^ swz_dst) << 4);
+    const uint32_t src2 = src_row + (((2u * part + 4u) ^ swz_dst) << 4), src3 = src_row + (((2u * part + 5u) ^ swz_dst) << 4);
     const uint32_t pk_stride = is_a ? uint32_t(A_PK) : uint32_t(B_PK);
     const uint32_t dst_row = smem_u32(sm + OFF_BU) + uint32_t(r) * 128u;
     const uint32_t d0 = ((4u * part) ^ swz_dst) << 4, d1 = ((4u * part + 1u) ^ swz_dst) << 4;
@@ -860,7 +868,6 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       bool ok = true;
       for (int kb = 0; kb < nkb; kb += 2) {
         if (!mbar_wait_bounded(&pk_full[sp], pk_par, abort_flag) ||
-            !mbar_wait_bounded(&pk_full[sp + 1], pk_par, abort_flag) ||
             !mbar_wait_bounded(&empty[ss], s_par ^ 1u, abort_flag) ||
             !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
           ok = false;
@@ -868,8 +875,9 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
         uint32_t o[32];
         if (active) {
-          const uint4 w0 = lds128(src0 + sp * pk_stride), w1 = lds128(src1 + sp * pk_stride);
-          const uint4 w2 = lds128(src0 + (sp + 1) * pk_stride), w3 = lds128(src1 + (sp + 1) * pk_stride);
+          const uint32_t pk = sp * pk_stride;
+          const uint4 w0 = lds128(src0 + pk), w1 = lds128(src1 + pk);
+          const uint4 w2 = lds128(src2 + pk), w3 = lds128(src3 + pk);
           unpack_word(w0.x, o[0], o[1]);
           unpack_word(w0.y, o[2], o[3]);
           unpack_word(w0.z, o[4], o[5]);
@@ -918,7 +926,6 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           mbar_arrive(&full[ss]);
           mbar_arrive(&full[ss + 1]);
           mbar_arrive(&pk_empty[sp]);
-          mbar_arrive(&pk_empty[sp + 1]);
         }
         sp += 2;
         if (sp == uint32_t(SP)) { sp = 0; pk_par ^= 1u; }
@@ -1045,6 +1052,435 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   }
 }
 
+
+// ===================================================================== A8 pair kernel
+// The CTA-pair contraction with the activations already in tensor-core
+// operand form (quarot_rotate_quant_a8): one byte per code, u = v + 8, in the
+// K order the W converters produce, and each row's code sum sum_k v_k.  The A
+// tile of a k-block (128 rows x 128 bytes per CTA) then needs no conversion:
+// TMA writes it straight into a 128B-swizzled K-major stage that the MMA reads
+// through a shared-memory descriptor.  Only the weights are converted (their
+// nibbles stay packed in HBM, 4 bits per code), and tensor memory no longer
+// holds A stages, so it holds two accumulators (columns [0, BN) and
+// [256, 256 + BN)): the epilogue of tile i drains one while the MMAs of tile
+// i + 1 fill the other.
+//
+//   warp 0          TMA producer of the packed W half rows (ring of SPW stages)
+//   warp 1          TMEM allocator; MMA issuer in the leader, relay in the peer
+//   warp 2          TMA producer of the A stages (ring of SA stages)
+//   warps 3-10      W converters (packed -> e4m3 bytes -> shared memory)
+//   warps 11-14     epilogue, one warp per TMEM lane quadrant
+//
+// Exact result: the MMA sums u_a u'_w 2^-18 (u'_w = w + 8, the weights'
+// offset codes), so sum_k a_k w_k = 2^18 D - 8 sum_k u'_w - 8 sum_k a_k, the
+// last term from the A row sums.
+namespace a8 {
+
+constexpr int SA = 6;             // operand stages: A bytes (TMA) + converted W half
+constexpr int SPW = 4;            // packed W stages
+constexpr int NBW8 = 8;           // W converter warps
+constexpr int NEW8 = 4;           // epilogue warps
+constexpr int CONV0 = 3;          // first converter warp
+constexpr int EPI0 = CONV0 + NBW8;  // 11
+constexpr int NT8 = 32 * (EPI0 + NEW8);  // 480
+constexpr int A_UN = BM * BK;            // 16 KB
+constexpr int W_PK = BNH_MAX * BKB;      // 7 KB
+constexpr int W_UN = BNH_MAX * BK;       // 14 KB
+constexpr int OFF_A = 0;
+constexpr int OFF_WU = OFF_A + SA * A_UN;
+constexpr int OFF_WP = OFF_WU + SA * W_UN;
+constexpr int OFF_BAR8 = ((OFF_WP + SPW * W_PK) + 1023) / 1024 * 1024;
+// barriers: pk_full[SPW] pk_empty[SPW] a_full[SA] full[SA] empty[SA]
+//           acc_full[2] acc_empty[2] rs_full[2] rs_empty[2] drain
+constexpr int NBAR8 = 2 * SPW + 3 * SA + 8 + 1;
+constexpr int OFF_MISC8 = OFF_BAR8 + NBAR8 * 8;
+constexpr int OFF_RSB8 = (OFF_MISC8 + 16 + 127) / 128 * 128;  // float [2][BN_MAX]: -8 x the tile's W row sums
+constexpr int OFF_SW8 = OFF_RSB8 + 2 * BN_MAX * 4;            // float [NEW8][BN_MAX]: each epilogue warp's scales
+constexpr int SMEM_BYTES8 = OFF_SW8 + NEW8 * BN_MAX * 4 + 1024;
+constexpr uint32_t ACC_STRIDE = 256;  // tensor-memory columns between the two accumulators
+static_assert(SMEM_BYTES8 <= 227 * 1024, "shared memory");
+static_assert(SA % 2 == 0 && SPW % 2 == 0, "converters take stages in pairs");
+static_assert(OFF_WU % 1024 == 0 && OFF_WP % 1024 == 0 && A_UN % 1024 == 0 && W_UN % 1024 == 0, "stage alignment");
+static_assert(BN_MAX <= int(ACC_STRIDE) && 2 * ACC_STRIDE <= TMEM_COLS, "two accumulators in tensor memory");
+static_assert(EPI0 % 4 == 3, "epilogue warps 11..14 cover the four TMEM lane quadrants");
+
+__device__ __forceinline__ void mma2_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__global__ void __launch_bounds__(NT8, 1)
+w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __half* __restrict__ sx, const int32_t* __restrict__ rsx,
+                         const __half* __restrict__ sw, int M, int N, int K, int BN, __half* __restrict__ y,
+                         int32_t* __restrict__ acc_out) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR8);
+  uint64_t* pk_full = bars;
+  uint64_t* pk_empty = pk_full + SPW;
+  uint64_t* a_full = pk_empty + SPW;
+  uint64_t* full = a_full + SA;
+  uint64_t* empty = full + SA;
+  uint64_t* acc_full = empty + SA;  // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2]
+  uint64_t* rs_full = acc_empty + 2;   // [2]
+  uint64_t* rs_empty = rs_full + 2;    // [2]
+  uint64_t* drain = rs_empty + 2;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC8 + 4);
+  float* rsB = reinterpret_cast<float*>(sm + OFF_RSB8);
+  float* swS = reinterpret_cast<float*>(sm + OFF_SW8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair_id = int(blockIdx.x) >> 1, n_pairs = int(gridDim.x) >> 1;
+  const int BNH = BN / 2;
+  const int nkb = K / BK;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + 2 * BM - 1) / (2 * BM)) * n_tiles_n;
+  const uint32_t idesc = IDESC_BASE | (uint32_t(BN >> 3) << 17);
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    for (int s = 0; s < SPW; ++s) {
+      mbar_init(&pk_full[s], 1);
+      mbar_init(&pk_empty[s], NBW8);
+    }
+    // the leader's full barriers count its own converter warps plus the relay
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&full[s], leader ? NBW8 + 1 : NBW8);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 2 * NEW8);  // every epilogue warp of the pair (used in the leader)
+      mbar_init(&rs_full[s], 2 * NBW8);    // every converter warp of the pair
+      mbar_init(&rs_empty[s], 2 * NEW8);   // every epilogue warp of the pair
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival
+  fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ W producer
+    long issued = 0, it = 0;
+    const int b_bytes = BNH * BKB;
+    for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs) {
+      const int n0 = (tile % n_tiles_n) * BN + int(rank) * BNH;
+      for (int kb = 0; kb < nkb; kb += 2, it += 2) {
+        // one 128-byte box per row covers k-blocks kb and kb + 1 (stages s, s + 1)
+        const int s = int(it % SPW);
+        if (!warp_wait(&pk_empty[s], uint32_t((it / SPW) & 1) ^ 1u, abort_flag)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&pk_full[s], 2 * b_bytes);
+          tma_load_2d(smem_u32(sm + OFF_WP + s * W_PK), &tmB, kb * BKB, n0, &pk_full[s]);
+        }
+        __syncwarp();
+        issued = it + 2;
+      }
+    }
+    if (warp_flag(abort_flag) && lane == 0) {
+      for (long j = (issued > SPW ? issued - SPW : 0); j < issued; j += 2)
+        mbar_wait_bounded(&pk_full[j % SPW], uint32_t((j / SPW) & 1), nullptr);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ A producer
+    long issued = 0, it = 0;
+    for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs) {
+      const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = int(it % SA);
+        if (!warp_wait(&empty[s], uint32_t((it / SA) & 1) ^ 1u, abort_flag)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&a_full[s], A_UN);
+          tma_load_2d(smem_u32(sm + OFF_A + s * A_UN), &tmA, kb * BK, m0, &a_full[s]);
+        }
+        __syncwarp();
+        issued = it + 1;
+      }
+    }
+    if (warp_flag(abort_flag) && lane == 0) {
+      for (long j = (issued > SA ? issued - SA : 0); j < issued; ++j)
+        mbar_wait_bounded(&a_full[j % SA], uint32_t((j / SA) & 1), nullptr);
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      // ---------------------------------------------------------- MMA issuer
+      long it = 0;
+      int ti = 0;
+      for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs, ++ti) {
+        const int a = ti & 1;
+        if (!warp_wait(&acc_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+        fence_after_sync();
+        const uint32_t tmem_d = tmem_base + uint32_t(a) * ACC_STRIDE;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = int(it % SA);
+          const uint32_t par = uint32_t((it / SA) & 1);
+          if (!warp_wait(&a_full[s], par, abort_flag) || !warp_wait(&full[s], par, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          if (lane == 0) {
+            const uint64_t ad = sw128_desc(smem_u32(sm + OFF_A + s * A_UN));
+            const uint64_t bd = sw128_desc(smem_u32(sm + OFF_WU + s * W_UN));
+#pragma unroll
+            for (int kk = 0; kk < BK / 32; ++kk)
+              mma2_ss(tmem_d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc, (kb | kk) != 0);
+            commit2(&empty[s]);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) commit2(&acc_full[a]);
+        __syncwarp();
+      }
+      if (lane == 0) {
+        commit2(drain);
+        mbar_wait_bounded(drain, 0, nullptr);
+      }
+    } else {
+      // ---------------------------------------------------------- relay
+      // forward this CTA's completed stages (A landed, W converted) to the
+      // leader, in the order the MMA issuer consumes them
+      long it = 0;
+      bool ok = true;
+      for (int tile = pair_id; ok && tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = int(it % SA);
+          const uint32_t par = uint32_t((it / SA) & 1);
+          if (!warp_wait(&a_full[s], par, abort_flag) || !warp_wait(&full[s], par, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) handoff_at(&full[s], 0);
+          __syncwarp();
+        }
+      }
+    }
+  } else if (warp < EPI0) {
+    // ------------------------------------------------------------ W converters
+    // row 16 * (warp - CONV0) + lane % 16 of this CTA's half of the weight
+    // rows, half lane / 16 of it
+    const int r = 16 * (warp - CONV0) + (lane & 15);
+    const uint32_t part = uint32_t(lane) >> 4;
+    const bool active = r < BNH;
+    const uint32_t swz_dst = uint32_t(r) & 7u;
+    // packed double stage: row r is 128 bytes (k-blocks kb, kb + 1), 128B swizzle
+    const uint32_t src_row = smem_u32(sm + OFF_WP) + uint32_t(r) * 128u;
+    const uint32_t src0 = src_row + (((2u * part) ^ swz_dst) << 4), src1 = src_row + (((2u * part + 1u) ^ swz_dst) << 4);
+    const uint32_t src2 = src_row + (((2u * part + 4u) ^ swz_dst) << 4), src3 = src_row + (((2u * part + 5u) ^ swz_dst) << 4);
+    const uint32_t dst_row = smem_u32(sm + OFF_WU) + uint32_t(r) * 128u;
+    const uint32_t d0 = ((4u * part) ^ swz_dst) << 4, d1 = ((4u * part + 1u) ^ swz_dst) << 4;
+    const uint32_t d2 = ((4u * part + 2u) ^ swz_dst) << 4, d3 = ((4u * part + 3u) ^ swz_dst) << 4;
+    uint32_t sp = 0, pk_par = 0, ss = 0, s_par = 0;  // ring positions and phase parities
+    int ti = 0;
+    for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
+      uint32_t sum = 0;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; kb += 2) {
+        if (!mbar_wait_bounded(&pk_full[sp], pk_par, abort_flag) ||
+            !mbar_wait_bounded(&empty[ss], s_par ^ 1u, abort_flag) ||
+            !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (active) {
+          uint32_t o[32];
+          const uint32_t pk = sp * uint32_t(W_PK);
+          const uint4 w0 = lds128(src0 + pk), w1 = lds128(src1 + pk);
+          const uint4 w2 = lds128(src2 + pk), w3 = lds128(src3 + pk);
+          unpack_word(w0.x, o[0], o[1]);
+          unpack_word(w0.y, o[2], o[3]);
+          unpack_word(w0.z, o[4], o[5]);
+          unpack_word(w0.w, o[6], o[7]);
+          unpack_word(w1.x, o[8], o[9]);
+          unpack_word(w1.y, o[10], o[11]);
+          unpack_word(w1.z, o[12], o[13]);
+          unpack_word(w1.w, o[14], o[15]);
+          unpack_word(w2.x, o[16], o[17]);
+          unpack_word(w2.y, o[18], o[19]);
+          unpack_word(w2.z, o[20], o[21]);
+          unpack_word(w2.w, o[22], o[23]);
+          unpack_word(w3.x, o[24], o[25]);
+          unpack_word(w3.y, o[26], o[27]);
+          unpack_word(w3.z, o[28], o[29]);
+          unpack_word(w3.w, o[30], o[31]);
+          // byte lanes of each 16-word sum stay below 16 * 15 = 240
+          sum = __dp4a((((o[0] + o[1]) + (o[2] + o[3])) + ((o[4] + o[5]) + (o[6] + o[7]))) +
+                           (((o[8] + o[9]) + (o[10] + o[11])) + ((o[12] + o[13]) + (o[14] + o[15]))),
+                       0x01010101u, sum);
+          sum = __dp4a((((o[16] + o[17]) + (o[18] + o[19])) + ((o[20] + o[21]) + (o[22] + o[23]))) +
+                           (((o[24] + o[25]) + (o[26] + o[27])) + ((o[28] + o[29]) + (o[30] + o[31]))),
+                       0x01010101u, sum);
+          const uint32_t d = dst_row + ss * uint32_t(W_UN), e = d + uint32_t(W_UN);
+          sts128(d + d0, o[0], o[1], o[2], o[3]);
+          sts128(d + d1, o[4], o[5], o[6], o[7]);
+          sts128(d + d2, o[8], o[9], o[10], o[11]);
+          sts128(d + d3, o[12], o[13], o[14], o[15]);
+          sts128(e + d0, o[16], o[17], o[18], o[19]);
+          sts128(e + d1, o[20], o[21], o[22], o[23]);
+          sts128(e + d2, o[24], o[25], o[26], o[27]);
+          sts128(e + d3, o[28], o[29], o[30], o[31]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full[ss]);
+          mbar_arrive(&full[ss + 1]);
+          mbar_arrive(&pk_empty[sp]);
+        }
+        sp += 2;
+        if (sp == uint32_t(SPW)) { sp = 0; pk_par ^= 1u; }
+        ss += 2;
+        if (ss == uint32_t(SA)) { ss = 0; s_par ^= 1u; }
+      }
+      if (!ok) break;
+      const int a = ti & 1;
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);  // the row's other half
+      if (!wait_cluster(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
+      if (part == 0 && active) {
+        float* dst = rsB + a * BN_MAX + int(rank) * BNH + r;
+        const float g = -8.0f * float(int(sum));  // exact: |8 sum| < 2^24
+        *dst = g;
+        st_cluster_s32(mapa(smem_u32(dst), rank ^ 1u), __float_as_int(g));
+      }
+      __syncwarp();
+      if (lane == 0) {
+        arrive_at(&rs_full[a], 0);
+        arrive_at(&rs_full[a], 1);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - EPI0;  // 0..3
+    const int q = warp & 3;     // TMEM lane quadrant of this warp
+    const int r = 32 * q + lane;
+    const int nchunks = BN / 32;
+    const bool vec_ok = (N % 16) == 0 && (reinterpret_cast<uintptr_t>(y) & 31) == 0;
+    int ti = 0;
+    for (int tile = pair_id; tile < n_tiles && !*abort_flag; tile += n_pairs, ++ti) {
+      const int a = ti & 1;
+      const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM, n0 = (tile % n_tiles_n) * BN;
+      const int gm = m0 + r;
+      // this warp's weight scales of the tile (warp-private, loaded before the
+      // accumulator is ready; the warp's reads of the previous tile are done)
+      float* sws_w = swS + e * BN_MAX;
+      for (int c = 0; c < nchunks; ++c)
+        sws_w[32 * c + lane] = n0 + 32 * c + lane < N ? __half2float(sw[n0 + 32 * c + lane]) : 0.f;
+      const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
+      const float bias_r = gm < M ? -8.0f * float(rsx[gm]) : 0.f;  // exact: |8 sum| <= 2^22
+      __syncwarp();
+      if (!mbar_wait_bounded(&acc_full[a], uint32_t((ti >> 1) & 1), abort_flag) ||
+          !wait_cluster(&rs_full[a], uint32_t((ti >> 1) & 1), abort_flag))
+        break;
+      fence_after_sync();
+      const float* rsb = rsB + a * BN_MAX;
+      const uint32_t tmem_row = tmem_base + uint32_t(a) * ACC_STRIDE + (uint32_t(32 * q) << 16);
+#pragma unroll 1
+      for (int c = 0; c < nchunks; ++c) {
+        const int c0 = 32 * c;
+        const float* sws = sws_w + c0;  // sws[j]: scale of column n0 + c0 + j
+        uint32_t v[32];
+        __syncwarp();
+        QUAROT_TMEM_LD32(tmem_row + uint32_t(c0), v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (c == nchunks - 1) {  // this warp no longer needs the accumulator
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(&acc_empty[a]);
+            else handoff_at(&acc_empty[a], 0);
+          }
+        }
+        const int gn = n0 + c0;
+        if (gm < M && gn < N) {
+          // exact integer accumulator, in place: acc = 2^18 D - 8 rowsum_w - 8 rowsum_a
+          const uint32_t rs_addr = smem_u32(rsb + c0), sw_addr = smem_u32(sws);
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const uint4 r4 = lds128(rs_addr + 4u * uint32_t(j));
+            v[j] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j]), 262144.0f, __uint_as_float(r4.x)), bias_r));
+            v[j + 1] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 1]), 262144.0f, __uint_as_float(r4.y)), bias_r));
+            v[j + 2] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 2]), 262144.0f, __uint_as_float(r4.z)), bias_r));
+            v[j + 3] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 3]), 262144.0f, __uint_as_float(r4.w)), bias_r));
+          }
+          __half* yrow = y + size_t(gm) * N + gn;
+          if (vec_ok && gn + 32 <= N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 16) {
+              uint32_t o[8];
+#pragma unroll
+              for (int t = 0; t < 8; t += 2) {
+                const uint4 s4 = lds128(sw_addr + 4u * uint32_t(j + 2 * t));
+                const float sv[4] = {__uint_as_float(s4.x), __uint_as_float(s4.y), __uint_as_float(s4.z),
+                                     __uint_as_float(s4.w)};
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int jj = j + 2 * (t + u);
+                  const __half2 hv = __floats2half2_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), sxr), sv[2 * u]),
+                                                       __fmul_rn(__fmul_rn(__uint_as_float(v[jj + 1]), sxr), sv[2 * u + 1]));
+                  o[t + u] = *reinterpret_cast<const uint32_t*>(&hv);
+                }
+              }
+              st_global_v8(yrow + j, o);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) yrow[j] = __float2half_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[j]), sxr), sws[j]));
+          }
+          if (acc_out != nullptr) {
+            int32_t* arow = acc_out + size_t(gm) * N + gn;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gn + j < N) arow[j] = __float2int_rn(__uint_as_float(v[j]));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        arrive_at(&rs_empty[a], 0);
+        arrive_at(&rs_empty[a], 1);
+      }
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
+  if (warp == 1) {
+    fence_after_sync();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace a8
+
 }  // namespace pair
 
 // ------------------------------------------------------------------ host
@@ -1063,13 +1499,25 @@ static bool get_encoder() {
   return g_encode != nullptr;
 }
 
-static bool make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int box_rows) {
+static bool make_map(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int box_rows, bool two_kb = false) {
   cuuint64_t gdim[2] = {cuuint64_t(K / 2), cuuint64_t(rows)};
   cuuint64_t gstride[1] = {cuuint64_t(K / 2)};
-  cuuint32_t box[2] = {cuuint32_t(BKB), cuuint32_t(box_rows)};
+  cuuint32_t box[2] = {cuuint32_t(two_kb ? 2 * BKB : BKB), cuuint32_t(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, two_kb ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Activations in tensor-core operand form: [rows, K] bytes, 128-byte boxes
+// (one k-block) in the 128B swizzle the MMA descriptor reads.
+static bool make_map_a8(CUtensorMap* tm, const void* base, int64_t rows, int64_t K, int box_rows) {
+  cuuint64_t gdim[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t gstride[1] = {cuuint64_t(K)};
+  cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1157,7 +1605,7 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
     // converters take k-blocks in pairs, so K % 256 == 0)
     const int pairs = sms / 2;
     CUtensorMap ta, tb;
-    if (!make_map(&ta, a_q, M, K, pair::BM) || !make_map(&tb, w_q, N, K, bn / 2)) return QUAROT_ERR_CUDA;
+    if (!make_map(&ta, a_q, M, K, pair::BM, true) || !make_map(&tb, w_q, N, K, bn / 2, true)) return QUAROT_ERR_CUDA;
     static quarot::AttrCache pattr;
     if (!smem_attr_once(pair::w4a4_gemm_pair_kernel, pair::SMEM_BYTES, pattr)) return QUAROT_ERR_LAUNCH;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
@@ -1189,6 +1637,51 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
       ta, tb, static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale), int(M), int(N),
       int(K), bn, static_cast<__half*>(y), acc_out);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+extern "C" int quarot_w4a4_gemm_a8(const uint8_t* a8, const int32_t* a_rowsum, const void* a_scale,
+                                   const uint8_t* w_q, const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
+                                   int32_t* acc_out, void* stream) {
+  using namespace quarot::gemm;
+  if (M < 0 || N < 0 || K <= 0) return QUAROT_ERR_INVALID_ARG;
+  if (K % (2 * BK) != 0 || K > MAX_K) return QUAROT_ERR_UNSUPPORTED;
+  if (M > (int64_t(1) << 31) - 2 * BM || N > (int64_t(1) << 31) - BN_MAX) return QUAROT_ERR_UNSUPPORTED;
+  if (M == 0 || N == 0) return QUAROT_OK;
+  if (!a8 || !a_rowsum || !a_scale || !w_q || !w_scale || !y) return QUAROT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a8) & 15) || (reinterpret_cast<uintptr_t>(w_q) & 15) ||
+      (reinterpret_cast<uintptr_t>(a_rowsum) & 3) || (reinterpret_cast<uintptr_t>(a_scale) & 1) ||
+      (reinterpret_cast<uintptr_t>(w_scale) & 15) || (reinterpret_cast<uintptr_t>(y) & 15) ||
+      (acc_out && (reinterpret_cast<uintptr_t>(acc_out) & 3)))
+    return QUAROT_ERR_ALIGNMENT;
+  if (!get_encoder()) return QUAROT_ERR_CUDA;
+  const int sms = sm_count();
+  if (sms < 2) return sms <= 0 ? QUAROT_ERR_CUDA : QUAROT_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int pairs = sms / 2;
+  const int bn = pick_bn_pair(M, N, pairs);
+  CUtensorMap ta, tb;
+  if (!make_map_a8(&ta, a8, M, K, pair::BM) || !make_map(&tb, w_q, N, K, bn / 2, true)) return QUAROT_ERR_CUDA;
+  static quarot::AttrCache attr8;
+  if (!smem_attr_once(pair::a8::w4a4_gemm_a8_pair_kernel, pair::a8::SMEM_BYTES8, attr8)) return QUAROT_ERR_LAUNCH;
+  const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
+  const int64_t npairs = tiles < pairs ? tiles : pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * npairs));
+  cfg.blockDim = dim3(pair::a8::NT8);
+  cfg.dynamicSmemBytes = pair::a8::SMEM_BYTES8;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::a8::w4a4_gemm_a8_pair_kernel, ta, tb,
+                                           static_cast<const __half*>(a_scale), a_rowsum,
+                                           static_cast<const __half*>(w_scale), int(M), int(N), int(K), bn,
+                                           static_cast<__half*>(y), acc_out);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
 
 extern "C" int quarot_w4a4_gemm_plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn) {

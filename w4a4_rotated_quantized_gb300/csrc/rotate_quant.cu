@@ -352,11 +352,16 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 // and 3, the next row's fp16 data arrives in a staging buffer by a bulk
 // asynchronous copy, so the load latency of one row hides behind the
 // arithmetic of the previous one.
-template <int MSEG, bool STAGED, bool RMS>
+//
+// A8 = true writes the tensor-core operand form of the codes instead of
+// packed nibbles: one byte per code holding u = v + 8 (the e4m3 byte whose
+// value is u * 2^-9), in the order (0, 2, 4, 6, 1, 3, 5, 7) within each group
+// of 8 codes, and the row's code sum sum_k v_k into rowsum_out[row].
+template <int MSEG, bool STAGED, bool RMS, bool A8 = false>
 __global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT)
 rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
                         float clip_ratio, float rms_eps, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
-                        float* __restrict__ rot_out) {
+                        float* __restrict__ rot_out, int32_t* __restrict__ rowsum_out = nullptr) {
   using PL = SegPlan<MSEG, STAGED>;
   constexpr int D = PL::D;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -545,7 +550,37 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   const __half S = quant_scale_fp16(amax * post, clip_ratio);
   const float f = post * (1.0f / __half2float(S));
   if (valid && t == 0) scale_out[row] = S;
-  if (valid) {
+  if constexpr (A8) {
+    const float2 fv = make_float2(f, f);
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    const bool need_clamp = clip_ratio < 1.0f || __half2float(S) >= 65504.0f;
+    int vsum = 0;
+#pragma unroll
+    for (int a = 0; a < MSEG; ++a) {
+      uint32_t ev = 0, od = 0;  // bytes of codes 0, 2, 4, 6 and 1, 3, 5, 7
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        float2 yv = __fmul2_rn(v[a][jj], fv);
+        if (need_clamp) {
+          yv.x = fminf(fmaxf(yv.x, -8.0f), 7.0f);
+          yv.y = fminf(fmaxf(yv.y, -8.0f), 7.0f);
+        }
+        const float2 rr = __fadd2_rn(yv, magic);
+        // the integer sits in the low mantissa bits of 1.5 * 2^23 + v
+        const int vx = __float_as_int(rr.x) - 0x4B400000, vy = __float_as_int(rr.y) - 0x4B400000;
+        vsum += vx + vy;
+        ev |= uint32_t(vx + 8) << (8 * jj);
+        od |= uint32_t(vy + 8) << (8 * jj);
+      }
+      if (valid) __stcs(reinterpret_cast<uint2*>(q_out + row * D + a * 1024 + 8 * t), make_uint2(ev, od));
+    }
+    vsum = __reduce_add_sync(0xffffffffu, vsum);
+    int* isum = reinterpret_cast<int*>(red) + 40;  // [RPC][4]
+    if (lane == 0) isum[r_local * 4 + w] = vsum;
+    __syncthreads();
+    if (valid && t == 0)
+      rowsum_out[row] = (isum[r_local * 4] + isum[r_local * 4 + 1]) + (isum[r_local * 4 + 2] + isum[r_local * 4 + 3]);
+  } else if (valid) {
     uint32_t* qrow = reinterpret_cast<uint32_t*>(q_out + row * (D / 2));
     const float2 fv = make_float2(f, f);
     const float2 magic = make_float2(12582912.0f, 12582912.0f);
@@ -580,11 +615,11 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   }  // row loop
 }
 
-template <int MSEG, bool STAGED, bool RMS>
+template <int MSEG, bool STAGED, bool RMS, bool A8 = false>
 static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps, uint8_t* q,
-                      void* s, float* rot, cudaStream_t st) {
+                      void* s, float* rot, cudaStream_t st, int32_t* rowsum = nullptr) {
   using PL = SegPlan<MSEG, STAGED>;
-  auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS>;
+  auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS, A8>;
   static quarot::AttrCache attr_done;
   static std::atomic<int> per_sm_dev[64];  // resident CTAs per SM on devices 0..63; 0 until measured
   if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
@@ -606,7 +641,7 @@ static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* si
   }
   if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
   kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(static_cast<const __half*>(x), M, ld_x, signs, clip,
-                                                                eps, q, static_cast<__half*>(s), rot);
+                                                                eps, q, static_cast<__half*>(s), rot, rowsum);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
 
@@ -712,6 +747,26 @@ extern "C" int quarot_rotate_quant_fp16(const void* x, int64_t M, int64_t d, int
     case 12288: return launch_rq_t<10, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
     default: return QUAROT_ERR_UNSUPPORTED;
   }
+}
+
+extern "C" int quarot_rotate_quant_a8(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                                      float clip_ratio, uint8_t* a8_out, void* scale_out, int32_t* rowsum_out,
+                                      void* stream) {
+  if (M < 0 || d <= 0 || ld_x < d) return QUAROT_ERR_INVALID_ARG;
+  if (!(clip_ratio > 0.f && clip_ratio <= 1.f)) return QUAROT_ERR_INVALID_ARG;
+  if (d != 4096 && d != 12288) return QUAROT_ERR_UNSUPPORTED;
+  if (M == 0) return QUAROT_OK;
+  if (x == nullptr || a8_out == nullptr || scale_out == nullptr || rowsum_out == nullptr) return QUAROT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (ld_x % 8) || (reinterpret_cast<uintptr_t>(a8_out) & 15) ||
+      (reinterpret_cast<uintptr_t>(scale_out) & 1) || (reinterpret_cast<uintptr_t>(rowsum_out) & 3) ||
+      (signs && (reinterpret_cast<uintptr_t>(signs) & 7)))
+    return QUAROT_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 4096)
+    return launch_seg_t<4, false, false, true>(x, M, ld_x, signs, clip_ratio, -1.f, a8_out, scale_out, nullptr, st,
+                                               rowsum_out);
+  return launch_seg_t<12, true, false, true>(x, M, ld_x, signs, clip_ratio, -1.f, a8_out, scale_out, nullptr, st,
+                                             rowsum_out);
 }
 
 extern "C" int quarot_rmsnorm_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, float eps,
