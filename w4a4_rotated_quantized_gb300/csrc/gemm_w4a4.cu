@@ -1009,13 +1009,20 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (gm < M && gn < N) {
           // exact integer accumulator, in place: acc = 2^18 * D - 8 * rowsum_w + bias_r
           const uint32_t rs_addr = smem_u32(rsb + c0), sw_addr = smem_u32(sws);
+          // packed fp32x2 arithmetic: each lane of a pair rounds exactly as
+          // the scalar fma + add would
+          const float2 k18 = make_float2(262144.0f, 262144.0f), bias2 = make_float2(bias_r, bias_r);
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             const uint4 r4 = lds128(rs_addr + 4u * uint32_t(j));
-            v[j] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j]), 262144.0f, __uint_as_float(r4.x)), bias_r));
-            v[j + 1] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 1]), 262144.0f, __uint_as_float(r4.y)), bias_r));
-            v[j + 2] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 2]), 262144.0f, __uint_as_float(r4.z)), bias_r));
-            v[j + 3] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 3]), 262144.0f, __uint_as_float(r4.w)), bias_r));
+            const float2 a01 = __fadd2_rn(__ffma2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), k18,
+                                                     make_float2(__uint_as_float(r4.x), __uint_as_float(r4.y))), bias2);
+            const float2 a23 = __fadd2_rn(__ffma2_rn(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), k18,
+                                                     make_float2(__uint_as_float(r4.z), __uint_as_float(r4.w))), bias2);
+            v[j] = __float_as_uint(a01.x);
+            v[j + 1] = __float_as_uint(a01.y);
+            v[j + 2] = __float_as_uint(a23.x);
+            v[j + 3] = __float_as_uint(a23.y);
           }
           __half* yrow = y + size_t(gm) * N + gn;
           if (vec_ok && gn + 32 <= N) {
@@ -1030,8 +1037,10 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                   const int jj = j + 2 * (t + u);
-                  const __half2 hv = __floats2half2_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), sxr), sv[2 * u]),
-                                                       __fmul_rn(__fmul_rn(__uint_as_float(v[jj + 1]), sxr), sv[2 * u + 1]));
+                  const float2 yv = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
+                                                          make_float2(sxr, sxr)),
+                                               make_float2(sv[2 * u], sv[2 * u + 1]));
+                  const __half2 hv = __floats2half2_rn(yv.x, yv.y);
                   o[t + u] = *reinterpret_cast<const uint32_t*>(&hv);
                 }
               }
@@ -1446,13 +1455,20 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         if (gm < M && gn < N) {
           // exact integer accumulator, in place: acc = 2^18 D - 8 rowsum_w - 8 rowsum_a
           const uint32_t rs_addr = smem_u32(rsb + c0), sw_addr = smem_u32(sws);
+          // packed fp32x2 arithmetic: each lane of a pair rounds exactly as
+          // the scalar fma + add would
+          const float2 k18 = make_float2(262144.0f, 262144.0f), bias2 = make_float2(bias_r, bias_r);
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             const uint4 r4 = lds128(rs_addr + 4u * uint32_t(j));
-            v[j] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j]), 262144.0f, __uint_as_float(r4.x)), bias_r));
-            v[j + 1] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 1]), 262144.0f, __uint_as_float(r4.y)), bias_r));
-            v[j + 2] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 2]), 262144.0f, __uint_as_float(r4.z)), bias_r));
-            v[j + 3] = __float_as_uint(__fadd_rn(__fmaf_rn(__uint_as_float(v[j + 3]), 262144.0f, __uint_as_float(r4.w)), bias_r));
+            const float2 a01 = __fadd2_rn(__ffma2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), k18,
+                                                     make_float2(__uint_as_float(r4.x), __uint_as_float(r4.y))), bias2);
+            const float2 a23 = __fadd2_rn(__ffma2_rn(make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), k18,
+                                                     make_float2(__uint_as_float(r4.z), __uint_as_float(r4.w))), bias2);
+            v[j] = __float_as_uint(a01.x);
+            v[j + 1] = __float_as_uint(a01.y);
+            v[j + 2] = __float_as_uint(a23.x);
+            v[j + 3] = __float_as_uint(a23.y);
           }
           __half* yrow = y + size_t(gm) * N + gn;
           if (vec_ok && gn + 32 <= N) {
@@ -1467,8 +1483,10 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                   const int jj = j + 2 * (t + u);
-                  const __half2 hv = __floats2half2_rn(__fmul_rn(__fmul_rn(__uint_as_float(v[jj]), sxr), sv[2 * u]),
-                                                       __fmul_rn(__fmul_rn(__uint_as_float(v[jj + 1]), sxr), sv[2 * u + 1]));
+                  const float2 yv = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
+                                                          make_float2(sxr, sxr)),
+                                               make_float2(sv[2 * u], sv[2 * u + 1]));
+                  const __half2 hv = __floats2half2_rn(yv.x, yv.y);
                   o[t + u] = *reinterpret_cast<const uint32_t*>(&hv);
                 }
               }
