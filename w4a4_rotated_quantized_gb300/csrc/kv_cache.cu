@@ -515,12 +515,16 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
                            ? ((((sacc[nt][0][2] + sacc[nt][1][2]) + (sacc[nt][0][3] + sacc[nt][1][3])) - qoff[nt]) +
                               kz1 * qsum[nt]) * ks1
                            : -INFINITY;
+      // raise the running max only when it grows by more than 8 (p <= 2^8).
+      // The head's tile max exceeds m_run + 8 exactly when one of its lanes'
+      // own maxima does, so the lanes test their two scores first and the
+      // head-wide max (over the lanes of column c) is formed only in the
+      // rare rescale branch, off the common dependency chain.
       float mt = fmaxf(s0, s1);
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-      // raise the running max only when it grows by more than 8 (p <= 2^8)
       if (__any_sync(0xffffffffu, mt > m_run[nt] + 8.0f)) {
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
         const float m_new = mt > m_run[nt] + 8.0f ? mt : m_run[nt];
         const float alpha = exp2f(m_run[nt] - m_new);  // 0 when the old max is -inf
         m_run[nt] = m_new;
