@@ -296,6 +296,18 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
   const int nkt = causal ? qt + 1 : (T + BKV - 1) / BKV;
   const int64_t cache_row0 = (int64_t(b) * Hkv + g) * T_max;
 
+  // The softmax threads load their half query row (64 fp16) first, so the
+  // load latency overlaps the barrier and tensor-memory setup below.
+  const bool is_sm = warp >= SM_W0;
+  const int sm_r = 32 * (warp & 3) + lane, sm_hh = (warp - SM_W0) >> 2;
+  const int sm_tok = q0 + sm_r;
+  uint4 qraw[8];
+  if (is_sm) {
+    const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t(b) * T + sm_tok) * Hq + h) * HD + 64 * sm_hh);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) qraw[m] = sm_tok < T ? __ldg(src + m) : make_uint4(0u, 0u, 0u, 0u);
+  }
+
   if (threadIdx.x == 0) {
     // in the pair, the leader's operand barriers also count the peer's relay
     const int relay = (PAIR && leader) ? 1 : 0;
@@ -578,35 +590,39 @@ prefill_attn_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq
     // registers, span 64 with the partner thread (same lane, other half)
     // through the fp32 staging area; a half row sits at [r][64 hh ..] in
     // 16-byte chunks, chunk m at m ^ (lane & 7).
-    const int r = 32 * qd + lane;
-    const int tok = q0 + r;
+    const int r = sm_r;
+    const int tok = sm_tok;
     float* qs = reinterpret_cast<float*>(sm + OFF_QS);
     float x[64];
     {
-      uint4 raw[8];
-      const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t(b) * T + tok) * Hq + h) * HD + 64 * hh);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) raw[m] = tok < T ? __ldg(src + m) : make_uint4(0u, 0u, 0u, 0u);
+      // xp[n] = elements (2n, 2n + 1): span 1 inside a pair, spans 2 .. 32
+      // across pairs with packed fp32x2 add / subtract (same roundings as the
+      // scalar butterflies: lower a + b, upper a - b)
+      float2 xp[32];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const uint32_t w4[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+        const uint32_t w4[4] = {qraw[m].x, qraw[m].y, qraw[m].z, qraw[m].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 f = h2_to_f2(w4[k]);
-          x[8 * m + 2 * k] = f.x;
-          x[8 * m + 2 * k + 1] = f.y;
+          xp[4 * m + k] = make_float2(f.x + f.y, f.x - f.y);
         }
       }
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1)
+#pragma unroll
+        for (int n = 0; n < 32; ++n)
+          if ((n & s) == 0) {
+            const float2 u0 = xp[n], u1 = xp[n + s];
+            xp[n] = __fadd2_rn(u0, u1);
+            xp[n + s] = __fadd2_rn(u0, make_float2(-u1.x, -u1.y));
+          }
+#pragma unroll
+      for (int n = 0; n < 32; ++n) {
+        x[2 * n] = xp[n].x;
+        x[2 * n + 1] = xp[n].y;
+      }
     }
-#pragma unroll
-    for (int s = 1; s < 64; s <<= 1)
-#pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if ((i & s) == 0) {
-          const float u0 = x[i], u1 = x[i + s];
-          x[i] = u0 + u1;
-          x[i + s] = u0 - u1;
-        }
     float* my = qs + r * HD + 64 * hh;
 #pragma unroll
     for (int m = 0; m < 16; ++m)
