@@ -358,7 +358,7 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 // value is u * 2^-9), in the order (0, 2, 4, 6, 1, 3, 5, 7) within each group
 // of 8 codes, and the row's code sum sum_k v_k into rowsum_out[row].
 template <int MSEG, bool STAGED, bool RMS, bool A8 = false>
-__global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT)
+__global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT, STAGED ? 3 : 1)
 rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
                         float clip_ratio, float rms_eps, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
                         float* __restrict__ rot_out, int32_t* __restrict__ rowsum_out = nullptr) {
@@ -398,7 +398,10 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
 
   // ---- pass 1 (and the row's sum of squares for RMSNorm)
   float sq = 0.f;
-#pragma unroll 1
+  // the warp's segments unrolled: their load / butterfly / store chains are
+  // independent and overlap (the persistent 12288 kernel is held at 3 CTAs
+  // per SM by its launch bounds, 170 registers)
+#pragma unroll
   for (int sgi = 0; sgi < PL::SPW; ++sgi) {
     const int a = w * PL::SPW + sgi;
     float2 p[16];  // p[4 i + jj] = elements (2 jj, 2 jj + 1) of chunk lane + 32 i
@@ -453,7 +456,7 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     for (int par = 0; par < 2; ++par)
 #pragma unroll
       for (int kl = 0; kl < 4; ++kl) addr[par][kl] = ((base0 ^ par) + 2 * (kl ^ lh)) * 4 + (lane & 3);
-#pragma unroll 1
+#pragma unroll
     for (int sgi = 0; sgi < PL::SPW; ++sgi) {
       const int a = w * PL::SPW + sgi;
       float* seg = reinterpret_cast<float*>(buf + a * 256);
