@@ -219,11 +219,30 @@ def test_rotate_quant_fp16_no_signs_clip_and_close_to_fp32(q):
     assert np.all(err <= 14 * 2.0 ** -11 * np.linalg.norm(x.astype(np.float64), axis=1))
 
 
-def test_rotate_quant_fp16_down_proj_full(q):
-    """The 2048 x 12288 down_proj activations at full size, rows sampled by the oracle."""
-    x, _, s = W.layer_inputs("down_proj", N=0)
+@pytest.mark.parametrize("d", [4096, 12288])
+def test_rotate_quant_fp16_edge_rows(q, d):
+    """Zero, one-hot (small and near the fp16 maximum), alternating, subnormal
+    and smallest-normal rows through the persistent fp16 kernels."""
+    x = np.zeros((7, d), dtype=np.float16)
+    x[1, 3] = 1.0
+    x[2, d - 1] = 60000.0
+    x[3, ::2] = -1.0
+    x[4] = np.float16(6e-8)
+    x[5, 1::3] = 2.0 ** -14
+    x[6, 5::7] = -3.5
+    _check_fp16_rotation(q, x, W.random_signs(d, 3))
+    gq, gs, _ = q.quarot_rotate_quant_fp16(_t(x), None)
+    assert np.all(gq.cpu().numpy()[0] == 0)
+
+
+@pytest.mark.parametrize("config", ["down_proj", "rotq4096"])
+def test_rotate_quant_fp16_full(q, config):
+    """2048 rows at full size (2048 x 12288 and 2048 x 4096): persistent CTAs
+    take several rows each; rows sampled by the oracle, including rows of a
+    CTA's second and later trips."""
+    x, _, s = W.layer_inputs(config, N=0)
     gq, gs, grot = q.quarot_rotate_quant_fp16(_t(x), _t(s), want_rot=True)
-    rows = [0, 1, 777, 2047]
+    rows = [0, 1, 607, 777, 1216, 1520, 2047]
     r16 = O.rotate_fp16_arith(x[rows], s).astype(np.float32)
     grot = grot.cpu().numpy()[rows]
     assert np.array_equal(grot, r16)

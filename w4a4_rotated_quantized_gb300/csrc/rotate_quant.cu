@@ -618,6 +618,271 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   }  // row loop
 }
 
+// ===================================================================== FP16 arithmetic, d = m x 1024
+// The FP16-arithmetic rotation for d = 4096 (Sylvester, bits 10 and 11 across
+// segments) and 12288 (Paley-12 across segments) on persistent CTAs that
+// stage the next row while the current one is transformed.  Values stay
+// fp16 throughout: every butterfly is one fp16x2 add or subtract, i.e. the
+// correctly rounded fp16(a + b) and fp16(a - b), so the passes follow the
+// Sylvester order h = 1, 2, ..., 512 exactly:
+//   pass 1  lane l of warp w takes elements 32 l .. 32 l + 31 of each of the
+//           warp's segments: sign flip, y = fp16(x c) with c = fp16(1/sqrt d),
+//           bits 0..4 in registers;
+//   pass 2  lane l takes the element pairs with bits 1..4 = l & 15 and
+//           bit 9 = l >> 4: bits 5..8;
+//   pass 3  thread t takes elements 4t .. 4t + 3 and 512 + 4t .. 515 + 4t of
+//           every segment: bit 9, then bits 10 and 11 (4096) or the Paley-12
+//           partial sums acc = fp16(acc +- y_a), a = 0 .. 11 (12288); then the
+//           row abs-max, fp16 scale, round, clamp and pack.
+// The fp16 work row holds 32 rows of 16 words (half2) per segment.  Logical
+// row r (the pass-1 lane) lives at r ^ (r >> 4), its 16-byte slot m at
+// m ^ ((r >> 1) & 3): the 16-byte stores of pass 1, the 32-bit accesses of
+// pass 2 and the 8-byte loads of pass 3 are all free of bank conflicts.
+__device__ __forceinline__ void hbfly(__half2& a, __half2& b) {
+  const __half2 s = __hadd2(a, b);
+  b = __hsub2(a, b);
+  a = s;
+}
+__device__ __forceinline__ __half2 hbfly_in(__half2 p) {  // (a, b) -> (a + b, a - b)
+  return __hfma2(__high2half2(p), __floats2half2_rn(1.f, -1.f), __low2half2(p));
+}
+__device__ __forceinline__ int seg16_word(int r, int w) {
+  return 16 * (r ^ ((r >> 4) & 1)) + 4 * ((w >> 2) ^ ((r >> 1) & 3)) + (w & 3);
+}
+
+template <int MSEG>
+struct Seg16Plan {
+  static constexpr int D = MSEG * 1024;
+  static constexpr int NT = 128;
+  static constexpr int SPW = MSEG / 4;
+  // [red 256 B][fp16 work row][fp16 staging row][mbarrier]
+  static constexpr size_t OFF_BUF = 64 * 4;
+  static constexpr size_t OFF_STAGE = OFF_BUF + size_t(D) * 2;
+  static constexpr size_t OFF_MBAR = OFF_STAGE + size_t(D) * 2;
+  static constexpr size_t SMEM = OFF_MBAR + 16;
+  static constexpr int MIN_CTAS = MSEG == 4 ? 8 : 4;
+};
+
+template <int MSEG>
+__global__ void __launch_bounds__(128, Seg16Plan<MSEG>::MIN_CTAS)
+rotate_quant_seg16_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
+                          float clip_ratio, __half h16_c, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
+                          float* __restrict__ rot_out) {
+  using PL = Seg16Plan<MSEG>;
+  constexpr int D = PL::D;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* red = reinterpret_cast<float*>(smem_raw);
+  const int t = threadIdx.x;
+  const int lane = t & 31, w = t >> 5;
+  uint32_t* buf = reinterpret_cast<uint32_t*>(smem_raw + PL::OFF_BUF);  // half2 words, 512 per segment
+  const __half* stage = reinterpret_cast<const __half*>(smem_raw + PL::OFF_STAGE);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_raw + PL::OFF_MBAR);
+  const __half2 c2 = __half2half2(h16_c);
+  int64_t row = blockIdx.x;
+  if (t == 0) {
+    mbar_init(mbar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (t == 0 && row < M) {
+    mbar_arrive_expect_tx(mbar, uint32_t(D) * 2u);
+    bulk_copy_g2s(smem_u32(stage), x + row * ld_x, uint32_t(D) * 2u, mbar);
+  }
+  for (int it = 0; row < M; ++it, row += gridDim.x) {
+    if (!mbar_wait_bounded(mbar, uint32_t(it & 1), nullptr)) break;
+
+    // ---- pass 1: bits 0..4
+#pragma unroll
+    for (int sgi = 0; sgi < PL::SPW; ++sgi) {
+      const int a = w * PL::SPW + sgi;
+      __half2 p[16];  // p[n] = elements (2n, 2n + 1) of the lane's 32
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 raw = *reinterpret_cast<const uint4*>(stage + a * 1024 + 32 * lane + 8 * i);
+        if (signs != nullptr) {
+          const uint2 sg = __ldg(reinterpret_cast<const uint2*>(signs + a * 1024 + 32 * lane + 8 * i));
+          raw.x ^= __byte_perm(sg.x, 0u, 0x1404) & 0x80008000u;
+          raw.y ^= __byte_perm(sg.x, 0u, 0x3424) & 0x80008000u;
+          raw.z ^= __byte_perm(sg.y, 0u, 0x1404) & 0x80008000u;
+          raw.w ^= __byte_perm(sg.y, 0u, 0x3424) & 0x80008000u;
+        }
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p[4 * i + k] = __hmul2(*reinterpret_cast<const __half2*>(&rw[k]), c2);
+      }
+#pragma unroll
+      for (int n = 0; n < 16; ++n) p[n] = hbfly_in(p[n]);
+#pragma unroll
+      for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+        for (int n = 0; n < 16; ++n)
+          if ((n & h) == 0) hbfly(p[n], p[n + h]);
+      uint4* seg = reinterpret_cast<uint4*>(buf + a * 512);
+      const int prow = lane ^ ((lane >> 4) & 1), sx = (lane >> 1) & 3;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint4 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&p[4 * m]);
+        o.y = *reinterpret_cast<const uint32_t*>(&p[4 * m + 1]);
+        o.z = *reinterpret_cast<const uint32_t*>(&p[4 * m + 2]);
+        o.w = *reinterpret_cast<const uint32_t*>(&p[4 * m + 3]);
+        seg[4 * prow + (m ^ sx)] = o;
+      }
+    }
+    __syncwarp();
+
+    // ---- pass 2: bits 5..8 of the warp's own segments
+    {
+      const int b = lane & 15, hb = lane >> 4;
+      // word of (row k + 16 hb, column b): 16 k + addr[k & 1][(k >> 1) & 3]
+      int addr[2][4];
+#pragma unroll
+      for (int par = 0; par < 2; ++par)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          addr[par][kk] = 256 * hb + (par ? -16 * hb : 16 * hb) + 4 * ((b >> 2) ^ kk) + (b & 3);
+#pragma unroll
+      for (int sgi = 0; sgi < PL::SPW; ++sgi) {
+        uint32_t* seg = buf + (w * PL::SPW + sgi) * 512;
+        __half2 p[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t u = seg[16 * k + addr[k & 1][(k >> 1) & 3]];
+          p[k] = *reinterpret_cast<const __half2*>(&u);
+        }
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if ((k & h) == 0) hbfly(p[k], p[k + h]);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) seg[16 * k + addr[k & 1][(k >> 1) & 3]] = *reinterpret_cast<const uint32_t*>(&p[k]);
+      }
+    }
+    __syncthreads();
+    {
+      // every warp is past pass 1: the staging buffer may take the next row
+      const int64_t next = row + gridDim.x;
+      if (t == 0 && next < M) {
+        mbar_arrive_expect_tx(mbar, uint32_t(D) * 2u);
+        bulk_copy_g2s(smem_u32(stage), x + next * ld_x, uint32_t(D) * 2u, mbar);
+      }
+    }
+
+    // ---- pass 3: bit 9, then across segments
+    __half2 v[MSEG][4];  // [a][0..1]: elements 4t .. 4t+3, [a][2..3]: the same + 512
+    {
+      const int off = 4 * (((t & 7) >> 1) ^ ((t >> 4) & 3)) + 2 * (t & 1);
+      const int w0 = 16 * (t >> 3) + off, w1 = 16 * (((t >> 3) + 16) ^ 1) + off;
+#pragma unroll
+      for (int a = 0; a < MSEG; ++a) {
+        const uint2 lo = *reinterpret_cast<const uint2*>(buf + a * 512 + w0);
+        const uint2 hi = *reinterpret_cast<const uint2*>(buf + a * 512 + w1);
+        v[a][0] = *reinterpret_cast<const __half2*>(&lo.x);
+        v[a][1] = *reinterpret_cast<const __half2*>(&lo.y);
+        v[a][2] = *reinterpret_cast<const __half2*>(&hi.x);
+        v[a][3] = *reinterpret_cast<const __half2*>(&hi.y);
+        hbfly(v[a][0], v[a][2]);
+        hbfly(v[a][1], v[a][3]);
+      }
+    }
+    if constexpr (MSEG == 4) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        hbfly(v[0][j], v[1][j]);
+        hbfly(v[2][j], v[3][j]);
+        hbfly(v[0][j], v[2][j]);
+        hbfly(v[1][j], v[3][j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __half2 in[12];
+#pragma unroll
+        for (int a = 0; a < 12; ++a) in[a] = v[a][j];
+#pragma unroll
+        for (int c = 0; c < 12; ++c) {
+          __half2 acc = in[0];  // row 0 of the Paley matrix is all +1
+#pragma unroll
+          for (int a = 1; a < 12; ++a) acc = paley12_entry(a, c) > 0 ? __hadd2(acc, in[a]) : __hsub2(acc, in[a]);
+          v[c][j] = acc;
+        }
+      }
+    }
+    __half2 am2 = __float2half2_rn(0.f);
+#pragma unroll
+    for (int a = 0; a < MSEG; ++a)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) am2 = __hmax2(am2, __habs2(v[a][j]));
+    float amax = fmaxf(__low2float(am2), __high2float(am2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[w] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    const __half S = quant_scale_fp16(amax, clip_ratio);
+    const float f = 1.0f / __half2float(S);
+    if (t == 0) scale_out[row] = S;
+    const float2 fv = make_float2(f, f);
+    const float2 magic = make_float2(12582912.0f, 12582912.0f);
+    // as in the fp32 kernels: with clip ratio 1 the clamp binds only when the
+    // scale saturated at the fp16 maximum
+    const bool need_clamp = clip_ratio < 1.0f || __half2float(S) >= 65504.0f;
+    uint16_t* qrow = reinterpret_cast<uint16_t*>(q_out + row * (D / 2));
+#pragma unroll
+    for (int a = 0; a < MSEG; ++a) {
+      uint32_t byte[4];
+      float2 fl[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        fl[j] = __half22float2(v[a][j]);
+        float2 yv = __fmul2_rn(fl[j], fv);
+        if (need_clamp) {
+          yv.x = fminf(fmaxf(yv.x, -8.0f), 7.0f);
+          yv.y = fminf(fmaxf(yv.y, -8.0f), 7.0f);
+        }
+        const float2 rr = __fadd2_rn(yv, magic);
+        byte[j] = (uint32_t(__float_as_int(rr.x)) & 0x0Fu) | ((uint32_t(__float_as_int(rr.y)) << 4) & 0xF0u);
+      }
+      // codes 4t .. 4t + 3 of segment a are packed bytes 512 a + 2t, 2t + 1
+      __stcs(qrow + a * 256 + t, uint16_t(byte[0] | (byte[1] << 8)));
+      __stcs(qrow + a * 256 + 128 + t, uint16_t(byte[2] | (byte[3] << 8)));
+      if (rot_out != nullptr) {
+        float* ro = rot_out + row * D + a * 1024 + 4 * t;
+        *reinterpret_cast<float4*>(ro) = make_float4(fl[0].x, fl[0].y, fl[1].x, fl[1].y);
+        *reinterpret_cast<float4*>(ro + 512) = make_float4(fl[2].x, fl[2].y, fl[3].x, fl[3].y);
+      }
+    }
+  }
+}
+
+template <int MSEG>
+static int launch_seg16(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, uint8_t* q, void* s,
+                        float* rot, cudaStream_t st) {
+  using PL = Seg16Plan<MSEG>;
+  auto kern = rotate_quant_seg16_kernel<MSEG>;
+  static quarot::AttrCache attr_done;
+  static std::atomic<int> per_sm_dev[64];
+  if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || ((ld_x * 2) & 15)) return QUAROT_ERR_ALIGNMENT;
+  int dev = 0, sms = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QUAROT_ERR_CUDA;
+  const bool known = dev >= 0 && dev < 64;
+  int per_sm = known ? per_sm_dev[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PL::NT, PL::SMEM) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    if (known) per_sm_dev[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t cap = int64_t(sms) * per_sm;
+  const int64_t blocks = M < cap ? M : cap;
+  const __half c = __double2half(1.0 / sqrt(double(PL::D)));
+  kern<<<dim3(unsigned(blocks)), dim3(PL::NT), PL::SMEM, st>>>(static_cast<const __half*>(x), M, ld_x, signs, clip, c,
+                                                                q, static_cast<__half*>(s), rot);
+  return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
 template <int MSEG, bool STAGED, bool RMS, bool A8 = false>
 static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps, uint8_t* q,
                       void* s, float* rot, cudaStream_t st, int32_t* rowsum = nullptr) {
@@ -743,11 +1008,11 @@ extern "C" int quarot_rotate_quant_fp16(const void* x, int64_t M, int64_t d, int
     case 512: return launch_rq_t<9, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
     case 1024: return launch_rq_t<10, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
     case 2048: return launch_rq_t<11, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
-    case 4096: return launch_rq_t<12, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 4096: return launch_seg16<4>(x, M, ld_x, signs, c, q_out, scale_out, rot_out, st);
     case 8192: return launch_rq_t<13, false, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
     case 3072: return launch_rq_t<8, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
     case 6144: return launch_rq_t<9, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
-    case 12288: return launch_rq_t<10, true, false, true>(x, M, ld_x, signs, c, -1.f, q_out, scale_out, rot_out, st);
+    case 12288: return launch_seg16<12>(x, M, ld_x, signs, c, q_out, scale_out, rot_out, st);
     default: return QUAROT_ERR_UNSUPPORTED;
   }
 }
