@@ -541,6 +541,41 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(SP % 2 == 0 && S % 2 == 0, "converters take stages in pairs");
 static_assert(OFF_RSB % 16 == 0 && OFF_SW % 16 == 0 && (BN_MAX * 4) % 16 == 0, "16-byte shared loads of row sums and scales");
 
+// The two forms of the pair kernel.  DBL = false: eight converted stages, A
+// stages at tensor-memory columns [256, 512), one accumulator at [0, BN) with
+// BN up to 224.  DBL = true, for pairs that run many tiles (each tile's
+// accumulator drain would otherwise idle the tensor pipe): six converted
+// stages, A stages at [320, 512), two accumulators at [0, 160) and
+// [160, 320) -- the epilogue drains tile i's while the MMAs of tile i + 1
+// fill the other -- and BN up to 160.
+template <bool DBL>
+struct Layout {
+  static constexpr int S = DBL ? 6 : pair::S;
+  static constexpr int NACC = DBL ? 2 : 1;
+  static constexpr uint32_t ACC_COLS = DBL ? 160u : 0u;
+  static constexpr uint32_t A_COL = DBL ? 320u : TMEM_A_COL;
+  static constexpr int BN_LIMIT = DBL ? 160 : BN_MAX;
+  static constexpr int OFF_BU = 0;
+  static constexpr int OFF_AP = OFF_BU + S * B_UN;
+  static constexpr int OFF_BP = OFF_AP + SP * A_PK;
+  static constexpr int OFF_BAR = ((OFF_BP + SP * B_PK) + 1023) / 1024 * 1024;
+  // barriers: pk_full[SP] pk_empty[SP] full[S] empty[S] acc_full[NACC]
+  //           acc_empty[NACC] rs_full[2] rs_empty[2] drain
+  static constexpr int NBAR = 2 * SP + 2 * S + 2 * NACC + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_RSA = (OFF_MISC + 16 + 127) / 128 * 128;
+  static constexpr int OFF_RSB = OFF_RSA + 4 * BM * 4;
+  static constexpr int OFF_SW = OFF_RSB + 2 * BN_MAX * 4;
+  static constexpr int SMEM_BYTES = OFF_SW + NEW * BN_MAX * 4 + 1024;
+  static_assert(OFF_AP % 1024 == 0 && OFF_BP % 1024 == 0, "stage alignment");
+  static_assert(A_COL + 32 * S <= TMEM_COLS, "A stages in tensor memory");
+  static_assert(uint32_t(NACC - 1) * ACC_COLS + uint32_t(BN_LIMIT) <= A_COL, "accumulators below the A stages");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(S % 2 == 0, "converters take stages in pairs");
+  static_assert(OFF_RSB % 16 == 0 && OFF_SW % 16 == 0, "16-byte shared loads of row sums and scales");
+};
+static_assert(Layout<false>::SMEM_BYTES == SMEM_BYTES && Layout<false>::OFF_BAR == OFF_BAR, "single form keeps its layout");
+
 #define QUAROT_TMEM_ST16(taddr, r)                                                                 \
   asm volatile(                                                                                    \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
@@ -692,28 +727,30 @@ __device__ __forceinline__ void commit2(uint64_t* bar) {
       : "memory");
 }
 
+template <bool DBL>
 __global__ void __launch_bounds__(NTHREADS, 1)
 w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K, int BN,
                       __half* __restrict__ y, int32_t* __restrict__ acc_out) {
+  using L = Layout<DBL>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
   uint64_t* pk_full = bars;
   uint64_t* pk_empty = pk_full + SP;
   uint64_t* full = pk_empty + SP;
-  uint64_t* empty = full + S;
-  uint64_t* acc_full = empty + S;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* rs_full = acc_empty + 1;
+  uint64_t* empty = full + L::S;
+  uint64_t* acc_full = empty + L::S;
+  uint64_t* acc_empty = acc_full + L::NACC;
+  uint64_t* rs_full = acc_empty + L::NACC;
   uint64_t* rs_empty = rs_full + 2;
   uint64_t* drain = rs_empty + 2;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
-  int* rsA = reinterpret_cast<int*>(sm + OFF_RSA);
-  float* rsB = reinterpret_cast<float*>(sm + OFF_RSB);
-  float* swS = reinterpret_cast<float*>(sm + OFF_SW);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::OFF_MISC + 4);
+  int* rsA = reinterpret_cast<int*>(sm + L::OFF_RSA);
+  float* rsB = reinterpret_cast<float*>(sm + L::OFF_RSB);
+  float* swS = reinterpret_cast<float*>(sm + L::OFF_SW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -733,12 +770,14 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       mbar_init(&pk_empty[s], NCW);
     }
     // the leader's full barriers count its own converter warps plus the relay
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < L::S; ++s) {
       mbar_init(&full[s], leader ? NCW + 1 : NCW);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, leader ? NEW + 1 : NEW);
+    for (int a = 0; a < L::NACC; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], leader ? NEW + 1 : NEW);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&rs_full[s], 2 * NCW);   // every converter warp of the pair
       mbar_init(&rs_empty[s], 2 * NEW);  // every epilogue warp of the pair
@@ -775,8 +814,8 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (!warp_wait(&pk_empty[s], uint32_t((it / SP) & 1) ^ 1u, abort_flag)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&pk_full[s], 2 * (A_PK + b_bytes));
-          tma_load_2d(smem_u32(sm + OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
-          tma_load_2d(smem_u32(sm + OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
+          tma_load_2d(smem_u32(sm + L::OFF_AP + s * A_PK), &tmA, kb * BKB, m0, &pk_full[s]);
+          tma_load_2d(smem_u32(sm + L::OFF_BP + s * B_PK), &tmB, kb * BKB, n0, &pk_full[s]);
         }
         __syncwarp();
         issued = it + 2;
@@ -792,7 +831,11 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       long it = 0;
       int ti = 0;
       for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs, ++ti) {
-        if (!warp_wait(acc_empty, uint32_t(ti & 1) ^ 1u, abort_flag)) break;
+        // accumulator slot of this tile and how often the slot was used before
+        const int sa = DBL ? (ti & 1) : 0;
+        const uint32_t use = DBL ? uint32_t(ti >> 1) : uint32_t(ti);
+        if (!warp_wait(&acc_empty[sa], (use & 1u) ^ 1u, abort_flag)) break;
+        const uint32_t tmem_d = tmem_base + uint32_t(sa) * L::ACC_COLS;
         fence_after_sync();
         bool ok = true;
         // stages in pairs, as the converters complete them: the phase of
@@ -800,8 +843,8 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         // converter warp and the relay arrive on s first), so one wait covers
         // both, and the eight MMAs of the pair issue back to back
         for (int kb = 0; kb < nkb; kb += 2, it += 2) {
-          const int s = int(it % S);
-          if (!warp_wait(&full[s + 1], uint32_t((it / S) & 1), abort_flag)) {
+          const int s = int(it % L::S);
+          if (!warp_wait(&full[s + 1], uint32_t((it / L::S) & 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -809,18 +852,18 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           if (lane == 0) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const uint32_t ta = tmem_base + TMEM_A_COL + uint32_t(32 * (s + u));
-              const uint64_t bd = sw128_desc(smem_u32(sm + OFF_BU + (s + u) * B_UN));
+              const uint32_t ta = tmem_base + L::A_COL + uint32_t(32 * (s + u));
+              const uint64_t bd = sw128_desc(smem_u32(sm + L::OFF_BU + (s + u) * B_UN));
 #pragma unroll
               for (int kk = 0; kk < BK / 32; ++kk)
-                mma2_ts(tmem_base, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, ((kb + u) | kk) != 0);
+                mma2_ts(tmem_d, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, ((kb + u) | kk) != 0);
               commit2(&empty[s + u]);
             }
           }
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) commit2(acc_full);
+        if (lane == 0) commit2(&acc_full[sa]);
         __syncwarp();
       }
       if (lane == 0) {
@@ -836,8 +879,8 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       bool ok = true;
       for (int tile = pair_id; ok && tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs, ++ti) {
         for (int kb = 0; kb < nkb; kb += 2, it += 2) {
-          const int s = int(it % S);
-          if (!warp_wait(&full[s + 1], uint32_t((it / S) & 1), abort_flag)) {
+          const int s = int(it % L::S);
+          if (!warp_wait(&full[s + 1], uint32_t((it / L::S) & 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -847,8 +890,18 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           }
           __syncwarp();
         }
-        if (!ok || !warp_wait(acc_empty, uint32_t(ti & 1), abort_flag)) break;
-        if (lane == 0) handoff_at(acc_empty, 0);
+        if (!ok) break;
+        // forward this CTA's drain of a tile's accumulator to the leader.  With
+        // two accumulators the drain of tile ti - 1 is forwarded after tile
+        // ti's stages, so the relay never holds back the stages of the tile
+        // that overlaps the drain; the leader needs it only before tile ti + 1.
+        if (!DBL || ti >= 1) {
+          const int pt = DBL ? ti - 1 : ti;
+          const int pa = DBL ? (pt & 1) : 0;
+          const uint32_t pu = DBL ? uint32_t(pt >> 1) : uint32_t(pt);
+          if (!warp_wait(&acc_empty[pa], pu & 1u, abort_flag)) break;
+          if (lane == 0) handoff_at(&acc_empty[pa], 0);
+        }
         __syncwarp();
       }
     }
@@ -861,16 +914,16 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const int r = is_a ? 32 * (warp & 3) + lane : 16 * (warp - 2 - NAW) + (lane & 15);
     const uint32_t part = is_a ? uint32_t(warp - 2) >> 2 : uint32_t(lane) >> 4;
     const bool active = is_a || r < BNH;
-    const uint32_t tmem_a_row = tmem_base + TMEM_A_COL + (uint32_t(32 * (warp & 3)) << 16) + 16u * part;
+    const uint32_t tmem_a_row = tmem_base + L::A_COL + (uint32_t(32 * (warp & 3)) << 16) + 16u * part;
     // 32-bit shared addresses, swizzled chunk offsets hoisted out of the loop:
     // the packed half row is 16-byte chunks 2 part and 2 part + 1 (64B swizzle),
     // the unpacked half row chunks 4 part .. 4 part + 3 (128B swizzle)
     const uint32_t swz_dst = uint32_t(r) & 7u;
-    const uint32_t src_row = smem_u32(sm + (is_a ? OFF_AP : OFF_BP)) + uint32_t(r) * 128u;
+    const uint32_t src_row = smem_u32(sm + (is_a ? L::OFF_AP : L::OFF_BP)) + uint32_t(r) * 128u;
     const uint32_t src0 = src_row + (((2u * part) ^ swz_dst) << 4), src1 = src_row + (((2u * part + 1u) ^ swz_dst) << 4);
     const uint32_t src2 = src_row + (((2u * part + 4u) ^ swz_dst) << 4), src3 = src_row + (((2u * part + 5u) ^ swz_dst) << 4);
     const uint32_t pk_stride = is_a ? uint32_t(A_PK) : uint32_t(B_PK);
-    const uint32_t dst_row = smem_u32(sm + OFF_BU) + uint32_t(r) * 128u;
+    const uint32_t dst_row = smem_u32(sm + L::OFF_BU) + uint32_t(r) * 128u;
     const uint32_t d0 = ((4u * part) ^ swz_dst) << 4, d1 = ((4u * part + 1u) ^ swz_dst) << 4;
     const uint32_t d2 = ((4u * part + 2u) ^ swz_dst) << 4, d3 = ((4u * part + 3u) ^ swz_dst) << 4;
     // Each iteration converts two consecutive k-blocks (stages sp, sp + 1 and
@@ -946,7 +999,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         sp += 2;
         if (sp == uint32_t(SP)) { sp = 0; pk_par ^= 1u; }
         ss += 2;
-        if (ss == uint32_t(S)) { ss = 0; s_par ^= 1u; }
+        if (ss == uint32_t(L::S)) { ss = 0; s_par ^= 1u; }
       }
       if (!ok) break;
       const int a = ti & 1;
@@ -985,13 +1038,15 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         sws_w[32 * c + lane] = n0 + 32 * c + lane < N ? __half2float(sw[n0 + 32 * c + lane]) : 0.f;
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
       __syncwarp();
-      if (!mbar_wait_bounded(acc_full, uint32_t(ti & 1), abort_flag) ||
+      const int sa = DBL ? a : 0;
+      const uint32_t use = DBL ? uint32_t(ti >> 1) : uint32_t(ti);
+      if (!mbar_wait_bounded(&acc_full[sa], use & 1u, abort_flag) ||
           !wait_cluster(&rs_full[a], uint32_t((ti >> 1) & 1), abort_flag))
         break;
       fence_after_sync();
       const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[2 * a * BM + r] + rsA[(2 * a + 1) * BM + r]);
       const float* rsb = rsB + a * BN_MAX;
-      const uint32_t tmem_row = tmem_base + (uint32_t(32 * q) << 16);
+      const uint32_t tmem_row = tmem_base + uint32_t(sa) * L::ACC_COLS + (uint32_t(32 * q) << 16);
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
         const int c0 = 32 * c;
@@ -1003,7 +1058,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (c == nchunks - 1) {  // the accumulator is no longer needed by this warp
           fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
+          if (lane == 0) mbar_arrive(&acc_empty[sa]);
         }
         const int gn = n0 + c0;
         if (gm < M && gn < N) {
@@ -1600,13 +1655,20 @@ static int pick_bn_pair(int64_t M, int64_t N, int pairs) {
   return best;
 }
 
-// The launch plan of one GEMM on a GPU with `sms` SMs: the CTA-pair kernel
-// (form 2) for M > 128 with an even k-block count, else the one-SM kernel
-// (form 1), and the N-tile width each would use.
+// The launch plan of one GEMM on a GPU with `sms` SMs: for M > 128 with an
+// even k-block count the CTA-pair kernel, else the one-SM kernel (form 1),
+// and the N-tile width.  The pair kernel keeps two accumulators (form 3)
+// where its width is at most 160 anyway and a pair runs three or more tiles,
+// so the drains between them can hide; otherwise one (form 2).  Narrowing a
+// tile to reach two accumulators does not pay: the converters' time per
+// k-block hardly depends on the width (measured: 2048 x 4096 x 12288 takes
+// 117.7 us at BN 160 with two accumulators against 92.2 us at 224 with one).
 static void plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn) {
   if (M > BM && sms >= 2 && (K / BK) % 2 == 0) {
-    *form = 2;
-    *bn = pick_bn_pair(M, N, sms / 2);
+    const int pairs = sms / 2;
+    *bn = pick_bn_pair(M, N, pairs);
+    const int64_t tiles = ((M + 255) / 256) * ((N + *bn - 1) / *bn);
+    *form = (*bn <= pair::Layout<true>::BN_LIMIT && (tiles + pairs - 1) / pairs >= 3) ? 3 : 2;
   } else {
     *form = 1;
     *bn = pick_bn(M, N, sms);
@@ -1644,20 +1706,24 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int form = 0, bn = 0;
   plan(M, N, K, sms, &form, &bn);
-  if (form == 2) {
+  if (form == 2 || form == 3) {
     // 2-SM path: clusters of two CTAs, one 256 x BN tile per pair (its
-    // converters take k-blocks in pairs, so K % 256 == 0)
+    // converters take k-blocks in pairs, so K % 256 == 0); form 3 keeps two
+    // accumulators in tensor memory
     const int pairs = sms / 2;
     CUtensorMap ta, tb;
     if (!make_map(&ta, a_q, M, K, pair::BM, true) || !make_map(&tb, w_q, N, K, bn / 2, true)) return QUAROT_ERR_CUDA;
-    static quarot::AttrCache pattr;
-    if (!smem_attr_once(pair::w4a4_gemm_pair_kernel, pair::SMEM_BYTES, pattr)) return QUAROT_ERR_LAUNCH;
+    const bool dbl = form == 3;
+    auto kern = dbl ? pair::w4a4_gemm_pair_kernel<true> : pair::w4a4_gemm_pair_kernel<false>;
+    const int smem = dbl ? pair::Layout<true>::SMEM_BYTES : pair::Layout<false>::SMEM_BYTES;
+    static quarot::AttrCache pattr1, pattr2;
+    if (!smem_attr_once(kern, smem, dbl ? pattr2 : pattr1)) return QUAROT_ERR_LAUNCH;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
     const int64_t npairs = tiles < pairs ? tiles : pairs;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(2 * npairs));
     cfg.blockDim = dim3(pair::NTHREADS);
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1666,7 +1732,7 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, pair::w4a4_gemm_pair_kernel, ta, tb,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb,
                                              static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale),
                                              int(M), int(N), int(K), bn, static_cast<__half*>(y), acc_out);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
