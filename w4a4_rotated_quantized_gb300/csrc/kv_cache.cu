@@ -54,21 +54,44 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
   uint8_t* __restrict__ cq = blockIdx.y == 0 ? k_q : v_q;
   __half* __restrict__ cs = blockIdx.y == 0 ? k_s : v_s;
   int16_t* __restrict__ cz = blockIdx.y == 0 ? k_z : v_z;
-  const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  // Resident CTAs walk the (vector, part) items with a grid stride, and every
+  // thread loads its next item's 64 bytes before it transforms the current
+  // one, so the loads stay in flight across the whole launch.  The stride is
+  // block-uniform and a multiple of the warp size, so the threads of one
+  // vector share every iteration (and the warp its shuffles).
   const int64_t nvec = B * Hkv * T_new;
+  const int64_t total = nvec * TPV;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  auto src_of = [&](int64_t g) {
+    const int64_t vv = g / TPV, tt = vv % T_new, bb = vv / T_new;
+    return reinterpret_cast<const uint4*>(src + ((bb / Hkv * T_new + tt) * Hkv + bb % Hkv) * D + (g % TPV) * 32);
+  };
+  uint4 nx[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if (gt < total) {
+    const uint4* p0 = src_of(gt);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nx[i] = __ldcs(p0 + i);
+  }
+  for (int64_t base = int64_t(blockIdx.x) * blockDim.x; base < total; base += stride, gt += stride) {
   const int64_t vi = gt / TPV;
   const int part = int(gt % TPV);
-  const bool valid = vi < nvec;
+  const bool valid = gt < total;
   const int64_t t = valid ? vi % T_new : 0;
   const int64_t bh = valid ? vi / T_new : 0;
   const int64_t h = bh % Hkv, b = bh / Hkv;
+  const uint4 cur[4] = {nx[0], nx[1], nx[2], nx[3]};
+  if (gt + stride < total) {
+    const uint4* pn = src_of(gt + stride);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nx[i] = __ldcs(pn + i);
+  }
 
   float v[32];
   if (valid) {
-    const uint4* p = reinterpret_cast<const uint4*>(src + ((b * T_new + t) * Hkv + h) * D + part * 32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 r = __ldcs(p + i);
+      const uint4 r = cur[i];
       const float2 f0 = h2_to_f2(r.x), f1 = h2_to_f2(r.y), f2 = h2_to_f2(r.z), f3 = h2_to_f2(r.w);
       v[8 * i + 0] = f0.x; v[8 * i + 1] = f0.y; v[8 * i + 2] = f1.x; v[8 * i + 3] = f1.y;
       v[8 * i + 4] = f2.x; v[8 * i + 5] = f2.y; v[8 * i + 6] = f3.x; v[8 * i + 7] = f3.y;
@@ -141,6 +164,7 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
       if constexpr (ASYM) cz[pos] = int16_t(zp);
     }
   }
+  }  // item loop
 }
 
 // ------------------------------------------------------------------ decode
@@ -668,6 +692,20 @@ int decode_ctas_per_sm(int G) {
   return cache[slot];
 }
 
+// Resident CTAs per SM of one KV-write instantiation (256 threads), measured
+// once.
+template <int D, bool ASYM>
+int kv_write_ctas_per_sm() {
+  static std::atomic<int> cache{0};
+  int n = cache.load(std::memory_order_relaxed);
+  if (n < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_write_kernel<D, ASYM>, 256, 0) != cudaSuccess || n < 1)
+      n = 1;
+    cache.store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 }  // namespace kv
 }  // namespace quarot
 
@@ -688,21 +726,28 @@ static int kv_write_impl(bool asym, const void* k, const void* v, int64_t B, int
     return QUAROT_ERR_ALIGNMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t threads = B * Hkv * T_new * (d / 32);
-  const int64_t blocks = (threads + 255) / 256;
-  if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
-  auto go = [&](auto kern) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QUAROT_ERR_CUDA;
+  const int64_t need = (threads + 255) / 256;
+  auto go = [&](auto kern, int per_sm) {
+    // one wave of resident CTAs (keys and values share it), each walking its
+    // items with the grid stride
+    int64_t cap = int64_t(sms) * per_sm / 2;
+    if (cap < 1) cap = 1;
+    const int64_t blocks = need < cap ? need : cap;
     kern<<<dim3(unsigned(blocks), 2), 256, 0, st>>>(static_cast<const __half*>(k), static_cast<const __half*>(v),
                                                     B, T_new, Hkv, t_start, T_max, k_q, static_cast<__half*>(k_s),
                                                     v_q, static_cast<__half*>(v_s), k_z, v_z, clip_ratio);
   };
   if (asym) {
-    if (d == 64) go(kv::kv_write_kernel<64, true>);
-    else if (d == 128) go(kv::kv_write_kernel<128, true>);
-    else go(kv::kv_write_kernel<256, true>);
+    if (d == 64) go(kv::kv_write_kernel<64, true>, kv::kv_write_ctas_per_sm<64, true>());
+    else if (d == 128) go(kv::kv_write_kernel<128, true>, kv::kv_write_ctas_per_sm<128, true>());
+    else go(kv::kv_write_kernel<256, true>, kv::kv_write_ctas_per_sm<256, true>());
   } else {
-    if (d == 64) go(kv::kv_write_kernel<64, false>);
-    else if (d == 128) go(kv::kv_write_kernel<128, false>);
-    else go(kv::kv_write_kernel<256, false>);
+    if (d == 64) go(kv::kv_write_kernel<64, false>, kv::kv_write_ctas_per_sm<64, false>());
+    else if (d == 128) go(kv::kv_write_kernel<128, false>, kv::kv_write_ctas_per_sm<128, false>());
+    else go(kv::kv_write_kernel<256, false>, kv::kv_write_ctas_per_sm<256, false>());
   }
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
