@@ -221,6 +221,15 @@ __device__ __forceinline__ void byte_cross(uint32_t wa, uint32_t wb, int p, uint
   }
 }
 
+// 2^x by the hardware approximation (relative error ~2^-22; -inf -> +0).
+// Arguments are scores minus the running max, so results below 2^-126, which
+// it flushes to zero, weigh nothing in the softmax.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -560,7 +569,7 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
           for (int e = 0; e < 4; ++e) o[nt][ii][e] *= alpha;
       }
       const float m_use = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
-      const float P0 = exp2f(s0 - m_use), P1 = exp2f(s1 - m_use);
+      const float P0 = ex2_approx(s0 - m_use), P1 = ex2_approx(s1 - m_use);
       if constexpr (ASYM) zacc[nt] = fmaf(P0, vzp0, fmaf(P1, vzp1, zacc[nt]));
       l_run[nt] += P0 + P1;
 
