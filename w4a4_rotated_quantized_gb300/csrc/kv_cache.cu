@@ -540,14 +540,14 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       // thread holds head 4 nt + c for tokens tr0 (sacc 0 + 1) and tr1 (sacc 2 + 3)
-      const float s0 = tr0 < tn
-                           ? ((((sacc[nt][0][0] + sacc[nt][1][0]) + (sacc[nt][0][1] + sacc[nt][1][1])) - qoff[nt]) +
-                              kz0 * qsum[nt]) * ks0
-                           : -INFINITY;
-      const float s1 = tr1 < tn
-                           ? ((((sacc[nt][0][2] + sacc[nt][1][2]) + (sacc[nt][0][3] + sacc[nt][1][3])) - qoff[nt]) +
-                              kz1 * qsum[nt]) * ks1
-                           : -INFINITY;
+      float i0 = ((sacc[nt][0][0] + sacc[nt][1][0]) + (sacc[nt][0][1] + sacc[nt][1][1])) - qoff[nt];
+      float i1 = ((sacc[nt][0][2] + sacc[nt][1][2]) + (sacc[nt][0][3] + sacc[nt][1][3])) - qoff[nt];
+      if constexpr (ASYM) {
+        i0 += kz0 * qsum[nt];
+        i1 += kz1 * qsum[nt];
+      }
+      const float s0 = tr0 < tn ? i0 * ks0 : -INFINITY;
+      const float s1 = tr1 < tn ? i1 * ks1 : -INFINITY;
       // raise the running max only when it grows by more than 8 (p <= 2^8).
       // The head's tile max exceeds m_run + 8 exactly when one of its lanes'
       // own maxima does, so the lanes test their two scores first and the
@@ -568,8 +568,9 @@ decode_mma_kernel(const __half* __restrict__ q, const uint8_t* __restrict__ kq, 
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[nt][ii][e] *= alpha;
       }
-      const float m_use = m_run[nt] == -INFINITY ? 0.f : m_run[nt];
-      const float P0 = ex2_approx(s0 - m_use), P1 = ex2_approx(s1 - m_use);
+      // m_run is finite here: a warp's first tile holds at least one valid
+      // token (tt < tn), whose finite score raised it from -inf just above
+      const float P0 = ex2_approx(s0 - m_run[nt]), P1 = ex2_approx(s1 - m_run[nt]);
       if constexpr (ASYM) zacc[nt] = fmaf(P0, vzp0, fmaf(P1, vzp1, zacc[nt]));
       l_run[nt] += P0 + P1;
 
