@@ -42,7 +42,7 @@ __device__ __forceinline__ void fwht32(float* v) {
 // with group = the head vector): a = clip * (min, max), s = fp16(range / 15),
 // integer zero point z = rne(a_min / s) (int16), codes q = clamp(rne(x / s) - z,
 // 0, 15) stored as unsigned nibbles; x^ = s (q + z).
-template <int D, bool ASYM>
+template <int D, bool ASYM, bool STRIDED>
 __global__ void __launch_bounds__(256)
 kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_src, int64_t B, int64_t T_new,
                 int64_t Hkv, int64_t t_start, int64_t T_max, uint8_t* __restrict__ k_q, __half* __restrict__ k_s,
@@ -54,11 +54,13 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
   uint8_t* __restrict__ cq = blockIdx.y == 0 ? k_q : v_q;
   __half* __restrict__ cs = blockIdx.y == 0 ? k_s : v_s;
   int16_t* __restrict__ cz = blockIdx.y == 0 ? k_z : v_z;
-  // Resident CTAs walk the (vector, part) items with a grid stride, and every
-  // thread loads its next item's 64 bytes before it transforms the current
-  // one, so the loads stay in flight across the whole launch.  The stride is
-  // block-uniform and a multiple of the warp size, so the threads of one
-  // vector share every iteration (and the warp its shuffles).
+  // STRIDED: resident CTAs walk the (vector, part) items with a grid stride,
+  // and every thread loads its next item's 64 bytes before it transforms the
+  // current one, so the loads stay in flight across the whole launch.  The
+  // stride is block-uniform and a multiple of the warp size, so the threads
+  // of one vector share every iteration (and the warp its shuffles).  Without
+  // it (launches of at most one wave, such as a one-token append) each thread
+  // takes one item and carries no prefetch state.
   const int64_t nvec = B * Hkv * T_new;
   const int64_t total = nvec * TPV;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -81,10 +83,12 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
   const int64_t bh = valid ? vi / T_new : 0;
   const int64_t h = bh % Hkv, b = bh / Hkv;
   const uint4 cur[4] = {nx[0], nx[1], nx[2], nx[3]};
-  if (gt + stride < total) {
-    const uint4* pn = src_of(gt + stride);
+  if constexpr (STRIDED) {
+    if (gt + stride < total) {
+      const uint4* pn = src_of(gt + stride);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) nx[i] = __ldcs(pn + i);
+      for (int i = 0; i < 4; ++i) nx[i] = __ldcs(pn + i);
+    }
   }
 
   float v[32];
@@ -164,6 +168,7 @@ kv_write_kernel(const __half* __restrict__ k_src, const __half* __restrict__ v_s
       if constexpr (ASYM) cz[pos] = int16_t(zp);
     }
   }
+  if constexpr (!STRIDED) break;
   }  // item loop
 }
 
@@ -702,14 +707,14 @@ int decode_ctas_per_sm(int G) {
   return cache[slot];
 }
 
-// Resident CTAs per SM of one KV-write instantiation (256 threads), measured
-// once.
+// Resident CTAs per SM of the strided KV-write instantiation (256 threads),
+// measured once.
 template <int D, bool ASYM>
 int kv_write_ctas_per_sm() {
   static std::atomic<int> cache{0};
   int n = cache.load(std::memory_order_relaxed);
   if (n < 1) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_write_kernel<D, ASYM>, 256, 0) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kv_write_kernel<D, ASYM, true>, 256, 0) != cudaSuccess || n < 1)
       n = 1;
     cache.store(n, std::memory_order_relaxed);
   }
@@ -740,24 +745,26 @@ static int kv_write_impl(bool asym, const void* k, const void* v, int64_t B, int
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return QUAROT_ERR_CUDA;
   const int64_t need = (threads + 255) / 256;
-  auto go = [&](auto kern, int per_sm) {
-    // one wave of resident CTAs (keys and values share it), each walking its
-    // items with the grid stride
+  auto go = [&](auto kern_one, auto kern_strided, int per_sm) {
+    // more items than one wave of resident CTAs (keys and values share it):
+    // that wave walks them with the grid stride; else one item per thread
     int64_t cap = int64_t(sms) * per_sm / 2;
     if (cap < 1) cap = 1;
-    const int64_t blocks = need < cap ? need : cap;
+    const bool strided = need > cap;
+    const int64_t blocks = strided ? cap : need;
+    auto kern = strided ? kern_strided : kern_one;
     kern<<<dim3(unsigned(blocks), 2), 256, 0, st>>>(static_cast<const __half*>(k), static_cast<const __half*>(v),
                                                     B, T_new, Hkv, t_start, T_max, k_q, static_cast<__half*>(k_s),
                                                     v_q, static_cast<__half*>(v_s), k_z, v_z, clip_ratio);
   };
   if (asym) {
-    if (d == 64) go(kv::kv_write_kernel<64, true>, kv::kv_write_ctas_per_sm<64, true>());
-    else if (d == 128) go(kv::kv_write_kernel<128, true>, kv::kv_write_ctas_per_sm<128, true>());
-    else go(kv::kv_write_kernel<256, true>, kv::kv_write_ctas_per_sm<256, true>());
+    if (d == 64) go(kv::kv_write_kernel<64, true, false>, kv::kv_write_kernel<64, true, true>, kv::kv_write_ctas_per_sm<64, true>());
+    else if (d == 128) go(kv::kv_write_kernel<128, true, false>, kv::kv_write_kernel<128, true, true>, kv::kv_write_ctas_per_sm<128, true>());
+    else go(kv::kv_write_kernel<256, true, false>, kv::kv_write_kernel<256, true, true>, kv::kv_write_ctas_per_sm<256, true>());
   } else {
-    if (d == 64) go(kv::kv_write_kernel<64, false>, kv::kv_write_ctas_per_sm<64, false>());
-    else if (d == 128) go(kv::kv_write_kernel<128, false>, kv::kv_write_ctas_per_sm<128, false>());
-    else go(kv::kv_write_kernel<256, false>, kv::kv_write_ctas_per_sm<256, false>());
+    if (d == 64) go(kv::kv_write_kernel<64, false, false>, kv::kv_write_kernel<64, false, true>, kv::kv_write_ctas_per_sm<64, false>());
+    else if (d == 128) go(kv::kv_write_kernel<128, false, false>, kv::kv_write_kernel<128, false, true>, kv::kv_write_ctas_per_sm<128, false>());
+    else go(kv::kv_write_kernel<256, false, false>, kv::kv_write_kernel<256, false, true>, kv::kv_write_ctas_per_sm<256, false>());
   }
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
