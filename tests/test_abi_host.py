@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import __graft_entry__
 import w4a4_rotated_quantized_gb300 as q
@@ -222,3 +223,20 @@ def test_a8_validation(lib):
     assert g(FAKE, None, FAKE, FAKE, FAKE, 8, 8, 256, FAKE, None, None) == 1
     assert g(FAKE, P(0x10002), FAKE, FAKE, FAKE, 8, 8, 256, FAKE, None, None) == 3
     assert g(P(0x10008), FAKE, FAKE, FAKE, FAKE, 8, 8, 256, FAKE, None, None) == 3
+
+
+def test_row_strided_views_accepted_and_others_rejected():
+    """The binding's row check: a column slice of a wider tensor passes with
+    its row stride; a transposed view (non-contiguous rows) is rejected before
+    any launch (host only: the check runs before the library is called)."""
+    if not torch.cuda.is_available():
+        # the check itself needs CUDA tensors; on a CPU-only host assert the
+        # CPU-tensor rejection path instead
+        with pytest.raises(q.QuarotError):
+            q._need_rows(torch.zeros((4, 16), dtype=torch.float16), torch.float16, "x")
+        return
+    wide = torch.zeros((4, 40), dtype=torch.float16, device="cuda")
+    assert q._need_rows(wide[:, 8:24], torch.float16, "x") == 40
+    assert q._need_rows(wide[:1, 8:24], torch.float16, "x") == 16
+    with pytest.raises(q.QuarotError):
+        q._need_rows(wide.t(), torch.float16, "x")

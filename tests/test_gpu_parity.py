@@ -803,3 +803,38 @@ def test_zz_scale_differences_are_rare(q):
     if t["rows"] == 0:
         pytest.skip("no quantizer checks ran")
     assert t["differ"] < 1e-3 * t["rows"], t
+
+
+# ---------------------------------------------------------------- row-strided inputs (ld_x > d)
+@pytest.mark.parametrize("entry,d", [("rotate", 256), ("rotate", 3072), ("rotate", 4096), ("rotate", 12288),
+                                     ("fp16", 1024), ("fp16", 4096), ("fp16", 12288),
+                                     ("rmsnorm", 4096), ("rmsnorm", 12288),
+                                     ("a8", 4096), ("a8", 12288), ("crosshead", 4096)])
+def test_rotate_family_row_strided(q, entry, d):
+    """A column slice of a wider tensor (row stride d + 72, column offset 8):
+    the entry points read it through their ld argument and return exactly
+    what they return for the same rows made contiguous -- every kernel form
+    (generic, segment, staged persistent with bulk row copies)."""
+    M = 300
+    x = W.activations(M, d, W.outlier_channels(d, 4, 7 + d), 50.0, 13 + d)
+    wide = torch.zeros((M, d + 72), dtype=torch.float16, device=DEV)
+    wide[:, 8:8 + d] = _t(x)
+    xs = wide[:, 8:8 + d]
+    assert xs.stride(0) == d + 72 and not xs.is_contiguous()
+    xc = xs.contiguous()
+    s = _t(W.random_signs(d, 5 + d))
+    if entry == "rotate":
+        got, ref = q.quarot_rotate_quant(xs, s, want_rot=True), q.quarot_rotate_quant(xc, s, want_rot=True)
+    elif entry == "fp16":
+        got, ref = q.quarot_rotate_quant_fp16(xs, s, want_rot=True), q.quarot_rotate_quant_fp16(xc, s, want_rot=True)
+    elif entry == "rmsnorm":
+        got, ref = q.quarot_rmsnorm_rotate_quant(xs, s, want_rot=True), q.quarot_rmsnorm_rotate_quant(xc, s, want_rot=True)
+    elif entry == "a8":
+        got, ref = q.quarot_rotate_quant_a8(xs, s), q.quarot_rotate_quant_a8(xc, s)
+    else:
+        got, ref = q.quarot_crosshead_rotate_quant(xs, 32, want_rot=True), q.quarot_crosshead_rotate_quant(xc, 32, want_rot=True)
+    q.quarot_check_error()
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
+    # the padding columns were not written and the contiguous path agrees with the oracle elsewhere
+    assert torch.count_nonzero(wide[:, :8]) == 0 and torch.count_nonzero(wide[:, 8 + d:]) == 0

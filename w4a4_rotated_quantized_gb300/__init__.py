@@ -114,6 +114,25 @@ def _need(t, dtype, name, dev=None):
         raise QuarotError(1, f"{name} must be contiguous")
 
 
+def _need_rows(t, dtype, name, dev=None) -> int:
+    """A 2-D input read row by row: contiguous rows, any row stride >= the
+    width (a column slice of a wider tensor).  Returns the row stride in
+    elements, the entry points' ld argument."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise QuarotError(1, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise QuarotError(1, f"{name} must be {dtype}, got {t.dtype}")
+    if dev is not None and t.device != dev:
+        raise QuarotError(1, f"{name} is on {t.device}, expected {dev}")
+    if t.dim() != 2:
+        raise QuarotError(1, f"{name} must be 2-D")
+    if t.shape[0] > 1 and (t.stride(1) != 1 or t.stride(0) < t.shape[1]):
+        raise QuarotError(1, f"{name} must have contiguous rows")
+    if t.shape[0] <= 1 and t.shape[1] > 1 and t.stride(1) != 1:
+        raise QuarotError(1, f"{name} must have contiguous rows")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
 def quarot_version() -> int:
     return load().quarot_version()
 
@@ -132,7 +151,7 @@ def quarot_selftest_wait(stream=None, device=None) -> None:
 
 
 def _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot):
-    _need(x, torch.float16, "x")
+    _need_rows(x, torch.float16, "x")
     dev = x.device
     M, d = x.shape
     if signs is not None:
@@ -156,7 +175,7 @@ def quarot_rmsnorm_rotate_quant(x, signs=None, eps: float = 1e-6, clip_ratio: fl
     one kernel: (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d] or None)."""
     q_out, scale_out, rot_out = _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot)
     M, d = x.shape
-    st = load().quarot_rmsnorm_rotate_quant(_ptr(x), M, d, d, float(eps), _ptr(signs), float(clip_ratio),
+    st = load().quarot_rmsnorm_rotate_quant(_ptr(x), M, d, _need_rows(x, torch.float16, "x"), float(eps), _ptr(signs), float(clip_ratio),
                                             _ptr(q_out), _ptr(scale_out), _ptr(rot_out), _stream(stream, x.device))
     _check(st, "quarot_rmsnorm_rotate_quant")
     return q_out, scale_out, rot_out
@@ -172,7 +191,7 @@ def quarot_crosshead_rotate_quant(z, nh: int, clip_ratio: float = 1.0, q_out=Non
     M, d = z.shape
     if d % nh:
         raise QuarotError(1, "row width is not a multiple of nh")
-    st = load().quarot_crosshead_rotate_quant(_ptr(z), M, int(nh), d // int(nh), d, float(clip_ratio), _ptr(q_out),
+    st = load().quarot_crosshead_rotate_quant(_ptr(z), M, int(nh), d // int(nh), _need_rows(z, torch.float16, "z"), float(clip_ratio), _ptr(q_out),
                                               _ptr(scale_out), _ptr(rot_out), _stream(stream, z.device))
     _check(st, "quarot_crosshead_rotate_quant")
     return q_out, scale_out, rot_out
@@ -180,8 +199,9 @@ def quarot_crosshead_rotate_quant(z, nh: int, clip_ratio: float = 1.0, q_out=Non
 
 def quarot_rotate_quant(x, signs=None, clip_ratio: float = 1.0, q_out=None, scale_out=None, rot_out=None,
                         stream=None, want_rot: bool = False):
-    """x: fp16 [M, d] -> (packed uint8 [M, d/2], scale fp16 [M], rotated fp32 [M, d] or None)."""
-    _need(x, torch.float16, "x")
+    """x: fp16 [M, d], rows contiguous (any row stride) -> (packed uint8 [M, d/2],
+    scale fp16 [M], rotated fp32 [M, d] or None)."""
+    ld = _need_rows(x, torch.float16, "x")
     dev = x.device
     M, d = x.shape
     if signs is not None:
@@ -196,7 +216,7 @@ def quarot_rotate_quant(x, signs=None, clip_ratio: float = 1.0, q_out=None, scal
     _need(scale_out, torch.float16, "scale_out", dev)
     if rot_out is not None:
         _need(rot_out, torch.float32, "rot_out", dev)
-    st = load().quarot_rotate_quant(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(q_out),
+    st = load().quarot_rotate_quant(_ptr(x), M, d, ld, _ptr(signs), float(clip_ratio), _ptr(q_out),
                                     _ptr(scale_out), _ptr(rot_out), _stream(stream, dev))
     _check(st, "quarot_rotate_quant")
     return q_out, scale_out, rot_out
@@ -208,7 +228,7 @@ def quarot_rotate_quant_fp16(x, signs=None, clip_ratio: float = 1.0, q_out=None,
     FP16 online-Hadamard variant); rot_out receives the fp16 values as fp32."""
     q_out, scale_out, rot_out = _rotate_quant_outputs(x, signs, q_out, scale_out, rot_out, want_rot)
     M, d = x.shape
-    st = load().quarot_rotate_quant_fp16(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(q_out),
+    st = load().quarot_rotate_quant_fp16(_ptr(x), M, d, _need_rows(x, torch.float16, "x"), _ptr(signs), float(clip_ratio), _ptr(q_out),
                                          _ptr(scale_out), _ptr(rot_out), _stream(stream, x.device))
     _check(st, "quarot_rotate_quant_fp16")
     return q_out, scale_out, rot_out
@@ -243,7 +263,7 @@ def quarot_rotate_quant_a8(x, signs=None, clip_ratio: float = 1.0, a8_out=None, 
     """x: fp16 [M, d] (d = 4096 or 12288) -> the codes in tensor-core operand
     form: (uint8 [M, d] offset codes in the GEMM's K order, scale fp16 [M],
     row code sums int32 [M])."""
-    _need(x, torch.float16, "x")
+    ld = _need_rows(x, torch.float16, "x")
     dev = x.device
     M, d = x.shape
     if signs is not None:
@@ -257,7 +277,7 @@ def quarot_rotate_quant_a8(x, signs=None, clip_ratio: float = 1.0, a8_out=None, 
     _need(a8_out, torch.uint8, "a8_out", dev)
     _need(scale_out, torch.float16, "scale_out", dev)
     _need(rowsum_out, torch.int32, "rowsum_out", dev)
-    st = load().quarot_rotate_quant_a8(_ptr(x), M, d, d, _ptr(signs), float(clip_ratio), _ptr(a8_out),
+    st = load().quarot_rotate_quant_a8(_ptr(x), M, d, ld, _ptr(signs), float(clip_ratio), _ptr(a8_out),
                                        _ptr(scale_out), _ptr(rowsum_out), _stream(stream, dev))
     _check(st, "quarot_rotate_quant_a8")
     return a8_out, scale_out, rowsum_out
