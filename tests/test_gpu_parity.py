@@ -838,3 +838,39 @@ def test_rotate_family_row_strided(q, entry, d):
         assert torch.equal(g, r)
     # the padding columns were not written and the contiguous path agrees with the oracle elsewhere
     assert torch.count_nonzero(wide[:, :8]) == 0 and torch.count_nonzero(wide[:, 8 + d:]) == 0
+
+
+# 1024 CTAs of work each: more than any one wave (at most 8 CTAs of 256
+# threads per SM, keys and values sharing it) on this GPU
+@pytest.mark.parametrize("d,B,H,T", [(64, 4, 8, 4096), (128, 2, 8, 4096), (256, 2, 4, 4096)])
+@pytest.mark.parametrize("asym", [False, True])
+def test_kv_write_grid_stride(q, d, B, H, T, asym):
+    """Appends large enough (more items than one wave of resident CTAs) that
+    the KV write walks them with its grid stride and register prefetch; every
+    vector against the oracle, with an offset and untouched slots around it."""
+    T_max, t0 = T + 24, 16
+    k = W.kv_tensors(B, T, H, d, 2, 20.0, 71 + d)
+    v = W.kv_tensors(B, T, H, d, 2, 20.0, 72 + d)
+    if asym:
+        gc = q.new_kv_cache_asym(B, H, T_max, d, DEV)
+        q.quarot_kv_write_asym(_t(k), _t(v), t0, *gc, clip_ratio=0.95)
+        gk, gks, gkz, gv, gvs, gvz = [t.cpu().numpy() for t in gc]
+        parts = ((k, gk, gks, gkz), (v, gv, gvs, gvz))
+    else:
+        gc = q.new_kv_cache(B, H, T_max, d, DEV)
+        q.quarot_kv_write(_t(k), _t(v), t0, *gc)
+        gk, gks, gv, gvs = [t.cpu().numpy() for t in gc]
+        parts = ((k, gk, gks, None), (v, gv, gvs, None))
+    for src, codes, scales, zeros in parts:
+        r = O.rotate(src, None)  # [B, T, H, d]
+        if asym:
+            _check_asym_vectors(r, 0.95, O.unpack_uint4(codes[:, :, t0:t0 + T].transpose(0, 2, 1, 3)),
+                                scales[:, :, t0:t0 + T].transpose(0, 2, 1), zeros[:, :, t0:t0 + T].transpose(0, 2, 1))
+        else:
+            q_ref, s_ref = O.quantize_rows(r, 1.0)
+            s_gpu = scales[:, :, t0:t0 + T].transpose(0, 2, 1)
+            c_gpu = O.unpack_int4(codes[:, :, t0:t0 + T].transpose(0, 2, 1, 3))
+            assert np.all(np.abs(s_gpu.astype(np.float64) - s_ref.astype(np.float64)) <= _fp16_ulp(s_ref))
+            assert not ((c_gpu != q_ref) & ~O.boundary_mask(r, s_ref)).any()
+        assert np.all(codes[:, :, :t0] == 0) and np.all(codes[:, :, t0 + T:] == 0)
+        assert np.all(scales[:, :, :t0] == 0) and np.all(scales[:, :, t0 + T:] == 0)
