@@ -874,3 +874,27 @@ def test_kv_write_grid_stride(q, d, B, H, T, asym):
             assert not ((c_gpu != q_ref) & ~O.boundary_mask(r, s_ref)).any()
         assert np.all(codes[:, :, :t0] == 0) and np.all(codes[:, :, t0 + T:] == 0)
         assert np.all(scales[:, :, :t0] == 0) and np.all(scales[:, :, t0 + T:] == 0)
+
+
+# ---------------------------------------------------------------- the layer object
+@pytest.mark.parametrize("K,N", [(4096, 1024), (12288, 512), (256, 1000)])
+def test_quarot_linear_layer(q, K, N):
+    """QuarotLinear: the two-call chain (weights prepared once), against the
+    oracle's layer and bit-identical to calling the entry points by hand;
+    leading batch dimensions pass through."""
+    x, w, s = W.layer_inputs("down_proj" if K == 12288 else ("rotq4096" if K == 4096 else "tiny"), M=96, N=N)
+    x = x[:96, :K]
+    w = w[:N, :K]
+    s = s[:K]
+    lin = q.QuarotLinear(_t(w), _t(s))
+    y = lin(_t(x).view(2, 48, K))
+    assert y.shape == (2, 48, N)
+    wq, wsc, _ = q.quarot_rotate_quant(_t(w), _t(s))
+    aq, asc, _ = q.quarot_rotate_quant(_t(x), _t(s))
+    yh, _ = q.quarot_w4a4_gemm(aq, asc, wq, wsc)
+    q.quarot_check_error()
+    assert torch.equal(y.view(96, N), yh)
+    oa, osx, _ = O.rotate_quant(x, s)
+    ow, osw, _ = O.rotate_quant(w, s)
+    _, oy = O.w4a4_gemm(oa, osx, ow, osw)
+    assert O.rel_fro(y.view(96, N).cpu().numpy(), oy) <= OUT_TOL

@@ -11,6 +11,10 @@ Functions (same names as the C entry points):
     quarot_decode_attn, quarot_decode_workspace_bytes, quarot_check_error,
     and the tensor-core operand form of the layer: quarot_rotate_quant_a8,
     quarot_w4a4_gemm_a8
+
+``QuarotLinear`` composes them into the W4A4 linear layer: weight rows
+rotated and quantized once, then per call the tokens rotated and quantized
+and the INT4 GEMM with its dequant epilogue.
 """
 from __future__ import annotations
 
@@ -417,6 +421,36 @@ def quarot_prefill_attn(q, k_q, k_s, v_q, v_s, sm_scale: float = 0.0, causal: bo
                                     float(sm_scale), int(bool(causal)), _ptr(out), _stream(stream, dev))
     _check(st, "quarot_prefill_attn")
     return out
+
+
+class QuarotLinear:
+    """The QuaRot W4A4 linear layer, y = x W^T in the rotated INT4 domain
+    ([G] "End-to-End Implementation", [S] Stages 1a, 2a, 2b): at
+    construction the weight rows are rotated by diag(s) H / sqrt(K) and
+    quantized per output channel (quarot_rotate_quant on the rows); each call
+    rotates and quantizes the tokens the same way (per token) and runs
+    quarot_w4a4_gemm.  weight: fp16 [N, K] on the GPU, K a supported rotation
+    width; signs: int8 [K] of +-1 or None; x: fp16 [..., K] -> fp16 [..., N].
+    No bias: the layer is the hot path's two kernels and nothing else."""
+
+    def __init__(self, weight, signs=None, clip_ratio: float = 1.0, weight_clip_ratio: float = 1.0, stream=None):
+        ld = _need_rows(weight, torch.float16, "weight")
+        del ld
+        self.out_features, self.in_features = weight.shape
+        self.signs = signs
+        self.clip_ratio = float(clip_ratio)
+        self.w_q, self.w_scale, _ = quarot_rotate_quant(weight, signs, clip_ratio=weight_clip_ratio, stream=stream)
+
+    def __call__(self, x, y=None, stream=None):
+        if x.shape[-1] != self.in_features:
+            raise QuarotError(1, f"x has {x.shape[-1]} features, the layer {self.in_features}")
+        lead = x.shape[:-1]
+        x2 = x.reshape(-1, self.in_features)
+        a_q, a_scale, _ = quarot_rotate_quant(x2, self.signs, clip_ratio=self.clip_ratio, stream=stream)
+        if y is not None:
+            y = y.view(-1, self.out_features)
+        y, _ = quarot_w4a4_gemm(a_q, a_scale, self.w_q, self.w_scale, y=y, stream=stream)
+        return y.view(*lead, self.out_features)
 
 
 def new_kv_cache(B: int, Hkv: int, T_max: int, d: int, device):
