@@ -898,3 +898,40 @@ def test_quarot_linear_layer(q, K, N):
     ow, osw, _ = O.rotate_quant(w, s)
     _, oy = O.w4a4_gemm(oa, osx, ow, osw)
     assert O.rel_fro(y.view(96, N).cpu().numpy(), oy) <= OUT_TOL
+
+
+@pytest.mark.parametrize("asym", [False, True])
+def test_quarot_kv_cache_object(q, asym):
+    """QuarotKVCache: a 300-token prompt appended in two chunks, its prompt
+    attention (symmetric cache), then three one-token decode steps, each
+    against the oracle's cache and attention at the same length."""
+    B, Hkv, G, d, T_max = 2, 2, 4, 128, 512
+    cache = q.QuarotKVCache(B, Hkv, T_max, d, DEV, asym=asym)
+    oc = _caches_asym((B, 0, Hkv, d), T_max) if asym else _caches((B, 0, Hkv, d), T_max)
+    owrite = (lambda k, v, t: O.kv_write_asym(k, v, t, *oc)) if asym else (lambda k, v, t: O.kv_write(k, v, t, *oc))
+    k = W.kv_tensors(B, 300, Hkv, d, 2, 20.0, 91)
+    v = W.kv_tensors(B, 300, Hkv, d, 2, 20.0, 92)
+    for lo, hi in ((0, 180), (180, 300)):
+        cache.append(_t(k[:, lo:hi]), _t(v[:, lo:hi]))
+        owrite(k[:, lo:hi], v[:, lo:hi], lo)
+    assert cache.length == 300
+    if not asym:
+        qp = W.prefill_query(B, 300, Hkv * G, d, 93)
+        out = cache.prefill(_t(qp))
+        assert O.rel_fro(out.cpu().numpy(), O.prefill_attn(qp, *oc, T=300)) <= OUT_TOL
+    else:
+        with pytest.raises(q.QuarotError):
+            cache.prefill(_t(W.prefill_query(B, 300, Hkv * G, d, 93)))
+    for step in range(3):
+        kn = W.kv_tensors(B, 1, Hkv, d, 2, 20.0, 100 + step)
+        vn = W.kv_tensors(B, 1, Hkv, d, 2, 20.0, 200 + step)
+        cache.append(_t(kn), _t(vn))
+        owrite(kn, vn, 300 + step)
+        qq = W.query(B, Hkv * G, d, 300 + step)
+        out = cache.decode(_t(qq))
+        T = 301 + step
+        ref = O.decode_attn_asym(qq, *oc, T=T) if asym else O.decode_attn(qq, *oc, T=T)
+        assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+    q.quarot_check_error()
+    with pytest.raises(q.QuarotError):
+        cache.append(_t(W.kv_tensors(B, 300, Hkv, d, 2, 20.0, 5)), _t(W.kv_tensors(B, 300, Hkv, d, 2, 20.0, 6)))

@@ -14,7 +14,8 @@ Functions (same names as the C entry points):
 
 ``QuarotLinear`` composes them into the W4A4 linear layer: weight rows
 rotated and quantized once, then per call the tokens rotated and quantized
-and the INT4 GEMM with its dequant epilogue.
+and the INT4 GEMM with its dequant epilogue.  ``QuarotKVCache`` holds the
+rotated INT4 KV cache with its append, decode and prompt-attention calls.
 """
 from __future__ import annotations
 
@@ -451,6 +452,57 @@ class QuarotLinear:
             y = y.view(-1, self.out_features)
         y, _ = quarot_w4a4_gemm(a_q, a_scale, self.w_q, self.w_scale, y=y, stream=stream)
         return y.view(*lead, self.out_features)
+
+
+class QuarotKVCache:
+    """The rotated INT4 KV cache of B sequences, Hkv heads of width d, room
+    for T_max tokens ([S] Stage 2c, Append / Decode / Init routines):
+    ``append`` quantizes new tokens into positions length .. length + T_new - 1
+    (quarot_kv_write, or quarot_kv_write_asym for the asymmetric cache);
+    ``decode`` attends one query token per sequence over the cached tokens
+    (quarot_decode_attn / _asym, with a workspace sized once for T_max);
+    ``prefill`` runs the prompt attention of length query tokens over them
+    (quarot_prefill_attn, symmetric cache).  Queries and outputs stay in the
+    rotated head basis unless unrotate_out is set."""
+
+    def __init__(self, B: int, Hkv: int, T_max: int, d: int = 128, device=None, asym: bool = False,
+                 clip_ratio: float = 0.95):
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.B, self.Hkv, self.T_max, self.d = int(B), int(Hkv), int(T_max), int(d)
+        self.asym, self.clip_ratio = bool(asym), float(clip_ratio)
+        self.tensors = (new_kv_cache_asym if self.asym else new_kv_cache)(self.B, self.Hkv, self.T_max, self.d, device)
+        self.length = 0
+        self._ws = {}
+
+    def append(self, k, v, stream=None) -> None:
+        """k, v fp16 [B, T_new, Hkv, d]."""
+        T_new = int(k.shape[1])
+        if self.length + T_new > self.T_max:
+            raise QuarotError(1, f"cache holds {self.T_max} tokens; {self.length} + {T_new} do not fit")
+        if self.asym:
+            quarot_kv_write_asym(k, v, self.length, *self.tensors, clip_ratio=self.clip_ratio, stream=stream)
+        else:
+            quarot_kv_write(k, v, self.length, *self.tensors, stream=stream)
+        self.length += T_new
+
+    def decode(self, q, sm_scale: float = 0.0, unrotate_out: bool = False, out=None, stream=None):
+        """q fp16 [B, Hq, d] -> fp16 [B, Hq, d] over the length cached tokens."""
+        Hq = int(q.shape[1])
+        ws = self._ws.get(Hq)
+        if ws is None:
+            need = quarot_decode_workspace_bytes(self.B, Hq, self.d, self.T_max)
+            ws = self._ws[Hq] = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+        fn = quarot_decode_attn_asym if self.asym else quarot_decode_attn
+        return fn(q, *self.tensors, T=self.length, sm_scale=sm_scale, unrotate_out=unrotate_out, out=out,
+                  workspace=ws, stream=stream)
+
+    def prefill(self, q, sm_scale: float = 0.0, causal: bool = True, out=None, stream=None):
+        """q fp16 [B, length, Hq, d] -> fp16 [B, length, Hq, d]."""
+        if self.asym:
+            raise QuarotError(2, "prompt attention reads the symmetric cache only")
+        if int(q.shape[1]) != self.length:
+            raise QuarotError(1, f"{q.shape[1]} query tokens for {self.length} cached tokens")
+        return quarot_prefill_attn(q, *self.tensors, sm_scale=sm_scale, causal=causal, out=out, stream=stream)
 
 
 def new_kv_cache(B: int, Hkv: int, T_max: int, d: int, device):
