@@ -1,8 +1,10 @@
 """Benchmark of the QuaRot W4A4 hot path on GB300.
 
 One step = one pass of every hot-path stage on synthetic, seeded inputs:
-  1. quarot_rotate_quant  X [2048, 12288] fp16 (H12 (x) H1024, random signs)
-  2. quarot_w4a4_gemm     -> Y [2048, 4096] fp16 against W~ [4096, 12288] INT4
+  1. quarot_rotate_quant_rowsum  X [2048, 12288] fp16 (H12 (x) H1024, random
+                                 signs) -> packed INT4, fp16 scales, row code sums
+  2. quarot_w4a4_gemm_rowsums    -> Y [2048, 4096] fp16 against W~ [4096, 12288]
+                                 INT4 (its row code sums prepared with it)
   3. quarot_kv_write      append one token for 16 sequences (8 KV heads x 128)
   4. quarot_decode_attn   16 sequences x 32 query heads over 4096 cached tokens
 The headline value is W4A4 layer tokens/s: 2048 tokens per step divided by
@@ -50,10 +52,11 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 M_TOK, K_DIM, N_OUT = 2048, 12288, 4096
-# DRAM bytes (read + write) of one launch of the down_proj GEMM, from one ncu
-# capture of this kernel (37.807360 MB read + 0.321280 MB written); None
-# whenever the kernel has changed since that capture.
-GEMM_TRAFFIC_BYTES = 38_128_640
+# DRAM bytes (read + write) of one launch of the down_proj GEMM (the row-sum
+# form the step runs), from one ncu capture of this kernel (37.832192 MB read
+# + 0.547840 MB written); None whenever the kernel has changed since that
+# capture.
+GEMM_TRAFFIC_BYTES = 38_380_032
 KV = W.CONFIGS["kv4"]
 METRIC = "W4A4 layer tokens/s"
 WORKLOAD = ("down_proj W4A4 layer 2048x12288->4096 (H12(x)H1024 rotate+quant, INT4 GEMM, fp16 out) "
@@ -412,6 +415,7 @@ def run_ours(args):
     xt = torch.from_numpy(x).to(dev)
     st = torch.from_numpy(s).to(dev)
     wq, wsc, _ = q.quarot_rotate_quant(torch.from_numpy(w).to(dev), st)
+    wrs = q.quarot_int4_rowsum(wq)  # the weight rows' code sums, prepared with the weights
     del w
     cache = q.new_kv_cache(B, Hkv, T, d, dev)
     q.quarot_kv_write(torch.from_numpy(k[:, :T - 1]).to(dev), torch.from_numpy(v[:, :T - 1]).to(dev), 0, *cache)
@@ -427,7 +431,8 @@ def run_ours(args):
     def new_set(i):
         if i == 0:
             return dict(x=xt, aq=torch.empty((M_TOK, K_DIM // 2), dtype=torch.uint8, device=dev),
-                        asx=torch.empty((M_TOK,), dtype=torch.float16, device=dev), wq=wq, wsc=wsc,
+                        asx=torch.empty((M_TOK,), dtype=torch.float16, device=dev),
+                        ars=torch.empty((M_TOK,), dtype=torch.int32, device=dev), wq=wq, wsc=wsc, wrs=wrs,
                         y=torch.empty((M_TOK, N_OUT), dtype=torch.float16, device=dev), cache=cache,
                         k_new=k_new, v_new=v_new, q=q_dec,
                         out=torch.empty((B, Hq, d), dtype=torch.float16, device=dev),
@@ -448,8 +453,9 @@ def run_ours(args):
 
     def stages_of(sd):
         return [
-            lambda: q.quarot_rotate_quant(sd["x"], st, q_out=sd["aq"], scale_out=sd["asx"]),
-            lambda: q.quarot_w4a4_gemm(sd["aq"], sd["asx"], sd["wq"], sd["wsc"], y=sd["y"]),
+            lambda: q.quarot_rotate_quant_rowsum(sd["x"], st, q_out=sd["aq"], scale_out=sd["asx"], rowsum_out=sd["ars"]),
+            lambda: q.quarot_w4a4_gemm_rowsums(sd["aq"], sd["asx"], sd["ars"], sd["wq"], sd["wsc"], sd["wrs"],
+                                               y=sd["y"]),
             lambda: q.quarot_kv_write(sd["k_new"], sd["v_new"], T - 1, *sd["cache"]),
             lambda: q.quarot_decode_attn(sd["q"], *sd["cache"], T=T, out=sd["out"], workspace=sd["wsp"]),
         ]
@@ -553,7 +559,13 @@ def run_ours(args):
     q.quarot_check_error(stream)
     if not (torch.equal(y_ser, s0["y"]) and torch.equal(o_ser, s0["out"])):
         raise RuntimeError("the two-branch step differs from the serial step")
-    del y_ser, o_ser
+    # the row-sum path against the plain entry points on the same input
+    aq_p, as_p, _ = q.quarot_rotate_quant(s0["x"], st)
+    y_p, _ = q.quarot_w4a4_gemm(aq_p, as_p, s0["wq"], s0["wsc"])
+    torch.cuda.synchronize()
+    if not (torch.equal(aq_p, s0["aq"]) and torch.equal(y_p, s0["y"])):
+        raise RuntimeError("the row-sum step differs from quarot_rotate_quant + quarot_w4a4_gemm")
+    del y_ser, o_ser, aq_p, as_p, y_p
 
     # ---------------- per-stage device times: back-to-back over the step's buffer sets
     stage_names = ["rotate_quant", "w4a4_gemm", "kv_write_append", "decode_attn"]
@@ -580,6 +592,7 @@ def run_ours(args):
     qd = [torch.empty_like(q_dec) for _ in range(2)]
     aqd = [torch.empty_like(s0["aq"]) for _ in range(2)]
     asd = [torch.empty_like(s0["asx"]) for _ in range(2)]
+    ard = [torch.empty_like(s0["ars"]) for _ in range(2)]
     yd = [torch.empty_like(s0["y"]) for _ in range(2)]
     od = [torch.empty_like(s0["out"]) for _ in range(2)]
     y_h = [torch.empty_like(s0["y"], device="cpu").pin_memory() for _ in range(2)]
@@ -607,8 +620,10 @@ def run_ours(args):
             dec_st.wait_stream(stream)  # the decode branch, forked as in the timed step
             q.quarot_kv_write(kd[sl], vd[sl], T - 1, *s0["cache"], stream=dec_st)
             q.quarot_decode_attn(qd[sl], *s0["cache"], T=T, out=od[sl], workspace=s0["wsp"], stream=dec_st)
-            q.quarot_rotate_quant(xd[sl], st, q_out=aqd[sl], scale_out=asd[sl], stream=stream)
-            q.quarot_w4a4_gemm(aqd[sl], asd[sl], s0["wq"], s0["wsc"], y=yd[sl], stream=stream)
+            q.quarot_rotate_quant_rowsum(xd[sl], st, q_out=aqd[sl], scale_out=asd[sl], rowsum_out=ard[sl],
+                                         stream=stream)
+            q.quarot_w4a4_gemm_rowsums(aqd[sl], asd[sl], ard[sl], s0["wq"], s0["wsc"], s0["wrs"], y=yd[sl],
+                                       stream=stream)
             stream.wait_stream(dec_st)
             ev_comp[sl].record(stream)
             d2h_st.wait_event(ev_comp[sl])
@@ -724,7 +739,7 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
         M, dd = x.shape
         xt = torch.from_numpy(x).to(dev)
         a8 = fn_kind == "a8"  # codes as operand bytes (d per row) plus int32 row sums
-        nbytes = M * dd * 2 + (M * dd + M * 6 if a8 else M * dd // 2 + M * 2)
+        nbytes = M * dd * 2 + (M * dd + M * 6 if a8 else M * dd // 2 + M * 2) + (M * 4 if fn_kind == "rs" else 0)
         n = tm.sets_for(nbytes)
         bufs = [(xt if i == 0 else xt.clone(), torch.empty((M, dd if a8 else dd // 2), dtype=torch.uint8, device=dev),
                  torch.empty((M,), dtype=torch.float16, device=dev)) for i in range(n)]
@@ -736,6 +751,8 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
                 return lambda: q.quarot_rotate_quant_a8(xi, s_t, a8_out=qo, scale_out=so, rowsum_out=rsb)
             if fn_kind == "rotate":
                 return lambda: q.quarot_rotate_quant(xi, s_t, q_out=qo, scale_out=so)
+            if fn_kind == "rs":
+                return lambda: q.quarot_rotate_quant_rowsum(xi, s_t, q_out=qo, scale_out=so, rowsum_out=rsb)
             if fn_kind == "rmsnorm":
                 return lambda: q.quarot_rmsnorm_rotate_quant(xi, s_t, eps=1e-6, q_out=qo, scale_out=so)
             if fn_kind == "fp16":
@@ -766,6 +783,9 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
     rot8_ms = {M: rot_case(f"rotate_quant_a8_{M}x4096", "a8", np.ascontiguousarray(xs[:M]), sst)
                for M in (512, 2048, 8192)}
     rot8_dp = rot_case("rotate_quant_a8_2048x12288", "a8", x_dp, st)
+    # packed codes plus int32 row code sums for the row-sum GEMM
+    rotrs_ms = {M: rot_case(f"rotate_quant_rowsum_{M}x4096", "rs", np.ascontiguousarray(xs[:M]), sst)
+                for M in (512, 2048, 8192)}
 
     # ---- KV cache: bulk write of the whole kv4 cache, decode batch sweep
     c = W.CONFIGS["kv4"]
@@ -856,12 +876,23 @@ def _other_configs(q, dev, stream, tm, hbm_peak, fp8_peak, s0, st, x_dp, qq_kv):
             tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
             res[f"w4a4_gemm_{M}x{K}x{N}"] = {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak, "buffer_sets": n,
                                              "layer_tokens_per_s": M / ((ms + rot_ms[M]) / 1e3)}
+            # both operands' row code sums given (quarot_rotate_quant_rowsum and
+            # the weights' quarot_int4_rowsum, prepared outside the timing)
+            ars_, wrs_ = q.quarot_int4_rowsum(aq_), q.quarot_int4_rowsum(wq_)
+            fns = [(lambda a=a, b=b, c_=c_, e=e, y=y: q.quarot_w4a4_gemm_rowsums(a, b, ars_, c_, e, wrs_, y=y))
+                   for a, b, c_, e, y in sets]
+            ms = tm.cycled(fns)
+            tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+            res[f"w4a4_gemm_rowsums_{M}x{K}x{N}"] = {"ms": ms, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak,
+                                                     "buffer_sets": n,
+                                                     "layer_tokens_per_s": M / ((ms + rotrs_ms[M]) / 1e3)}
             del sets, fns
             res[f"w4a4_gemm_a8_{M}x{K}x{N}"] = _gemm_a8_case(q, tm, dev, g, M, N, K, wq_, ws_, fp8_peak, rot8_ms[M])
     res["w4a4_gemm_a8_2048x12288x4096"] = _gemm_a8_case(q, tm, dev, g, M_TOK, N_OUT, K_DIM, s0["wq"], s0["wsc"],
                                                           fp8_peak, rot8_dp)
     # the bench GEMM with its operands warm in L2 (one buffer set, back-to-back)
-    ms_w = tm.warm(lambda: q.quarot_w4a4_gemm(s0["aq"], s0["asx"], s0["wq"], s0["wsc"], y=s0["y"]))
+    ms_w = tm.warm(lambda: q.quarot_w4a4_gemm_rowsums(s0["aq"], s0["asx"], s0["ars"], s0["wq"], s0["wsc"], s0["wrs"],
+                                                      y=s0["y"]))
     tf = 2.0 * M_TOK * N_OUT * K_DIM / (ms_w / 1e3) / 1e12
     res["w4a4_gemm_2048x12288x4096_warm_l2"] = {"ms": ms_w, "TOPS": tf, "frac_fp8_peak": tf / fp8_peak}
 

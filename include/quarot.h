@@ -229,6 +229,40 @@ int quarot_w4a4_gemm_a8(const uint8_t* a8, const int32_t* a_rowsum, const void* 
                         const void* w_scale, int64_t M, int64_t N, int64_t K, void* y, int32_t* acc_out,
                         void* stream);
 
+/*
+ * quarot_rotate_quant_rowsum -- quarot_rotate_quant (same codes, scales and
+ * errors) that also writes each row's code sum rowsum_out[i] = sum_k q[i, k]
+ * (int32 [M], 4-byte aligned), the per-token offset correction of
+ * quarot_w4a4_gemm_rowsums.  Supported widths: d = 4096 and 12288
+ * (QUAROT_ERR_UNSUPPORTED otherwise; quarot_int4_rowsum serves any width).
+ */
+int quarot_rotate_quant_rowsum(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                               float clip_ratio, uint8_t* q_out, void* scale_out, int32_t* rowsum_out,
+                               void* stream);
+
+/*
+ * quarot_int4_rowsum -- code sums of the rows of a packed INT4 matrix q
+ * (uint8 [M, K/2] in the quarot_rotate_quant format, 16-byte aligned):
+ * rowsum_out[i] = sum_k q[i, k] (int32 [M], 4-byte aligned).  K % 32 == 0,
+ * K <= 2^24.  For the weight rows this runs once, at weight preparation.
+ */
+int quarot_int4_rowsum(const uint8_t* q, int64_t M, int64_t K, int32_t* rowsum_out, void* stream);
+
+/*
+ * quarot_w4a4_gemm_rowsums -- quarot_w4a4_gemm with the row code sums of
+ * both operands given: a_rowsum[i] = sum_k a[i, k] (int32 [M]) and
+ * w_rowsum[j] = sum_k w[j, k] (int32 [N]), both 4-byte aligned, from
+ * quarot_rotate_quant_rowsum / quarot_int4_rowsum.  The result is the same,
+ * bit for bit (the exact accumulator and its dequantization); the CTA-pair
+ * kernel then leaves the sums of its offset encoding to these inputs instead
+ * of summing the codes it unpacks.  Sums that are not the codes' sums give
+ * wrong results.  Other arguments and errors as quarot_w4a4_gemm; null sums
+ * (M, N > 0) are QUAROT_ERR_INVALID_ARG.
+ */
+int quarot_w4a4_gemm_rowsums(const uint8_t* a_q, const void* a_scale, const int32_t* a_rowsum,
+                             const uint8_t* w_q, const void* w_scale, const int32_t* w_rowsum, int64_t M, int64_t N,
+                             int64_t K, void* y, int32_t* acc_out, void* stream);
+
 /* quarot_w4a4_gemm_plan -- which kernel and N-tile width quarot_w4a4_gemm
  * launches for an M x N x K problem on a GPU with `sms` SMs (a host-only
  * query: it touches no device).  *form = 2 for the CTA-pair kernel (M > 128

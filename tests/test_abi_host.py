@@ -240,3 +240,24 @@ def test_row_strided_views_accepted_and_others_rejected():
     assert q._need_rows(wide[:1, 8:24], torch.float16, "x") == 16
     with pytest.raises(q.QuarotError):
         q._need_rows(wide.t(), torch.float16, "x")
+
+
+def test_rowsum_entry_points_validate_on_host(lib):
+    """The row-sum entry points reject bad arguments before any launch."""
+    P = ctypes.c_void_p(16)
+    f = lib.quarot_int4_rowsum
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(P, -1, 128, P, None) == 1
+    assert f(P, 4, 100, P, None) == 1          # K % 32
+    assert f(None, 4, 128, P, None) == 1
+    assert f(ctypes.c_void_p(8), 4, 128, P, None) == 3
+    assert f(P, 0, 128, P, None) == 0
+    g = lib.quarot_rotate_quant_rowsum
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert g(P, 4, 256, 256, None, 1.0, P, P, P, None) == 2   # width without the sum form
+    assert g(P, 4, 4096, 4096, None, 1.0, P, P, None, None) == 1
+    h = lib.quarot_w4a4_gemm_rowsums
+    h.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 3
+    assert h(P, P, None, P, P, P, 256, 256, 256, P, None, None) == 1
+    assert h(P, P, P, P, P, ctypes.c_void_p(18), 256, 256, 256, P, None, None) == 3

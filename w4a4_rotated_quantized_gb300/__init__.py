@@ -49,6 +49,9 @@ _SIGS = {
     "quarot_w4a4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "quarot_rotate_quant_a8": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "quarot_w4a4_gemm_a8": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "quarot_rotate_quant_rowsum": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "quarot_int4_rowsum": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+    "quarot_w4a4_gemm_rowsums": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "quarot_w4a4_gemm_plan": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_int)]),
     "quarot_kv_write": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -315,6 +318,72 @@ def quarot_w4a4_gemm_a8(a8, a_rowsum, a_scale, w_q, w_scale, y=None, acc_out=Non
     return y, acc_out
 
 
+def quarot_rotate_quant_rowsum(x, signs=None, clip_ratio: float = 1.0, q_out=None, scale_out=None, rowsum_out=None,
+                               stream=None):
+    """x: fp16 [M, d] (d = 4096 or 12288), rows contiguous -> (packed uint8
+    [M, d/2], scale fp16 [M], row code sums int32 [M])."""
+    ld = _need_rows(x, torch.float16, "x")
+    dev = x.device
+    M, d = x.shape
+    if signs is not None:
+        _need(signs, torch.int8, "signs", dev)
+    if q_out is None:
+        q_out = torch.empty((M, d // 2), dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float16, device=dev)
+    if rowsum_out is None:
+        rowsum_out = torch.empty((M,), dtype=torch.int32, device=dev)
+    _need(q_out, torch.uint8, "q_out", dev)
+    _need(scale_out, torch.float16, "scale_out", dev)
+    _need(rowsum_out, torch.int32, "rowsum_out", dev)
+    st = load().quarot_rotate_quant_rowsum(_ptr(x), M, d, ld, _ptr(signs), float(clip_ratio), _ptr(q_out),
+                                           _ptr(scale_out), _ptr(rowsum_out), _stream(stream, dev))
+    _check(st, "quarot_rotate_quant_rowsum")
+    return q_out, scale_out, rowsum_out
+
+
+def quarot_int4_rowsum(q, rowsum_out=None, stream=None):
+    """q: packed uint8 [M, K/2] -> row code sums int32 [M]."""
+    _need(q, torch.uint8, "q")
+    M, Kh = q.shape
+    if rowsum_out is None:
+        rowsum_out = torch.empty((M,), dtype=torch.int32, device=q.device)
+    _need(rowsum_out, torch.int32, "rowsum_out", q.device)
+    st = load().quarot_int4_rowsum(_ptr(q), M, 2 * Kh, _ptr(rowsum_out), _stream(stream, q.device))
+    _check(st, "quarot_int4_rowsum")
+    return rowsum_out
+
+
+def quarot_w4a4_gemm_rowsums(a_q, a_scale, a_rowsum, w_q, w_scale, w_rowsum, y=None, acc_out=None, stream=None,
+                             want_acc: bool = False):
+    """quarot_w4a4_gemm with both operands' row code sums given (int32 [M]
+    and [N]) -> (y fp16 [M, N], acc int32 [M, N] or None)."""
+    _need(a_q, torch.uint8, "a_q")
+    dev = a_q.device
+    _need(w_q, torch.uint8, "w_q", dev)
+    _need(a_scale, torch.float16, "a_scale", dev)
+    _need(w_scale, torch.float16, "w_scale", dev)
+    _need(a_rowsum, torch.int32, "a_rowsum", dev)
+    _need(w_rowsum, torch.int32, "w_rowsum", dev)
+    M, Kh = a_q.shape
+    N, Kh2 = w_q.shape
+    if Kh != Kh2:
+        raise QuarotError(1, "a_q and w_q disagree on K")
+    if a_rowsum.numel() != M or w_rowsum.numel() != N:
+        raise QuarotError(1, "row sums must have M and N entries")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    if acc_out is None and want_acc:
+        acc_out = torch.empty((M, N), dtype=torch.int32, device=dev)
+    _need(y, torch.float16, "y", dev)
+    if acc_out is not None:
+        _need(acc_out, torch.int32, "acc_out", dev)
+    st = load().quarot_w4a4_gemm_rowsums(_ptr(a_q), _ptr(a_scale), _ptr(a_rowsum), _ptr(w_q), _ptr(w_scale),
+                                         _ptr(w_rowsum), M, N, 2 * Kh, _ptr(y), _ptr(acc_out), _stream(stream, dev))
+    _check(st, "quarot_w4a4_gemm_rowsums")
+    return y, acc_out
+
+
 def quarot_w4a4_gemm_plan(M: int, N: int, K: int, sms: int) -> tuple[int, int]:
     """(form, bn): the kernel quarot_w4a4_gemm launches for M x N x K on a GPU
     with `sms` SMs (2 = CTA pair, 1 = one SM) and its N-tile width."""
@@ -441,16 +510,25 @@ class QuarotLinear:
         self.signs = signs
         self.clip_ratio = float(clip_ratio)
         self.w_q, self.w_scale, _ = quarot_rotate_quant(weight, signs, clip_ratio=weight_clip_ratio, stream=stream)
+        # widths whose quantizer also writes the row code sums: the GEMM then
+        # takes both operands' sums instead of forming them while unpacking
+        self.rowsums = self.in_features in (4096, 12288)
+        self.w_rowsum = quarot_int4_rowsum(self.w_q, stream=stream) if self.rowsums else None
 
     def __call__(self, x, y=None, stream=None):
         if x.shape[-1] != self.in_features:
             raise QuarotError(1, f"x has {x.shape[-1]} features, the layer {self.in_features}")
         lead = x.shape[:-1]
         x2 = x.reshape(-1, self.in_features)
-        a_q, a_scale, _ = quarot_rotate_quant(x2, self.signs, clip_ratio=self.clip_ratio, stream=stream)
         if y is not None:
             y = y.view(-1, self.out_features)
-        y, _ = quarot_w4a4_gemm(a_q, a_scale, self.w_q, self.w_scale, y=y, stream=stream)
+        if self.rowsums:
+            a_q, a_scale, a_rs = quarot_rotate_quant_rowsum(x2, self.signs, clip_ratio=self.clip_ratio, stream=stream)
+            y, _ = quarot_w4a4_gemm_rowsums(a_q, a_scale, a_rs, self.w_q, self.w_scale, self.w_rowsum, y=y,
+                                            stream=stream)
+        else:
+            a_q, a_scale, _ = quarot_rotate_quant(x2, self.signs, clip_ratio=self.clip_ratio, stream=stream)
+            y, _ = quarot_w4a4_gemm(a_q, a_scale, self.w_q, self.w_scale, y=y, stream=stream)
         return y.view(*lead, self.out_features)
 
 

@@ -566,7 +566,10 @@ struct Layout {
   static constexpr int OFF_RSA = (OFF_MISC + 16 + 127) / 128 * 128;
   static constexpr int OFF_RSB = OFF_RSA + 4 * BM * 4;
   static constexpr int OFF_SW = OFF_RSB + 2 * BN_MAX * 4;
-  static constexpr int SMEM_BYTES = OFF_SW + NEW * BN_MAX * 4 + 1024;
+  // each epilogue warp's column corrections of the tile when the weight row
+  // sums are given (float [NEW][BN_MAX])
+  static constexpr int OFF_RW = OFF_SW + NEW * BN_MAX * 4;
+  static constexpr int SMEM_BYTES = OFF_RW + NEW * BN_MAX * 4 + 1024;
   static_assert(OFF_AP % 1024 == 0 && OFF_BP % 1024 == 0, "stage alignment");
   static_assert(A_COL + 32 * S <= TMEM_COLS, "A stages in tensor memory");
   static_assert(uint32_t(NACC - 1) * ACC_COLS + uint32_t(BN_LIMIT) <= A_COL, "accumulators below the A stages");
@@ -574,7 +577,7 @@ struct Layout {
   static_assert(S % 2 == 0, "converters take stages in pairs");
   static_assert(OFF_RSB % 16 == 0 && OFF_SW % 16 == 0, "16-byte shared loads of row sums and scales");
 };
-static_assert(Layout<false>::SMEM_BYTES == SMEM_BYTES && Layout<false>::OFF_BAR == OFF_BAR, "single form keeps its layout");
+static_assert(Layout<false>::OFF_BAR == OFF_BAR && Layout<false>::OFF_SW == OFF_SW, "single form keeps its layout");
 
 #define QUAROT_TMEM_ST16(taddr, r)                                                                 \
   asm volatile(                                                                                    \
@@ -727,11 +730,17 @@ __device__ __forceinline__ void commit2(uint64_t* bar) {
       : "memory");
 }
 
-template <bool DBL>
+// PRE: the code sums of the activation rows (sum_k a) and of the weight rows
+// (sum_k w) are given, so the converters only unpack and the epilogue forms
+// the offset corrections from them: -8 sum_k a for the row and
+// -8 (sum_k w + 8 K) for the column (both exact in fp32), the same values the
+// converters' sums give.
+template <bool DBL, bool PRE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K, int BN,
-                      __half* __restrict__ y, int32_t* __restrict__ acc_out) {
+                      __half* __restrict__ y, int32_t* __restrict__ acc_out, const int32_t* __restrict__ a_rowsum,
+                      const int32_t* __restrict__ w_rowsum) {
   using L = Layout<DBL>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -751,6 +760,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   int* rsA = reinterpret_cast<int*>(sm + L::OFF_RSA);
   float* rsB = reinterpret_cast<float*>(sm + L::OFF_RSB);
   float* swS = reinterpret_cast<float*>(sm + L::OFF_SW);
+  float* rwS = reinterpret_cast<float*>(sm + L::OFF_RW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -964,12 +974,14 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
           unpack_word(w3.z, o[28], o[29]);
           unpack_word(w3.w, o[30], o[31]);
           // byte lanes of each 16-word sum stay below 16 * 15 = 240
-          sum = __dp4a((((o[0] + o[1]) + (o[2] + o[3])) + ((o[4] + o[5]) + (o[6] + o[7]))) +
-                           (((o[8] + o[9]) + (o[10] + o[11])) + ((o[12] + o[13]) + (o[14] + o[15]))),
-                       0x01010101u, sum);
-          sum = __dp4a((((o[16] + o[17]) + (o[18] + o[19])) + ((o[20] + o[21]) + (o[22] + o[23]))) +
-                           (((o[24] + o[25]) + (o[26] + o[27])) + ((o[28] + o[29]) + (o[30] + o[31]))),
-                       0x01010101u, sum);
+          if constexpr (!PRE) {
+            sum = __dp4a((((o[0] + o[1]) + (o[2] + o[3])) + ((o[4] + o[5]) + (o[6] + o[7]))) +
+                             (((o[8] + o[9]) + (o[10] + o[11])) + ((o[12] + o[13]) + (o[14] + o[15]))),
+                         0x01010101u, sum);
+            sum = __dp4a((((o[16] + o[17]) + (o[18] + o[19])) + ((o[20] + o[21]) + (o[22] + o[23]))) +
+                             (((o[24] + o[25]) + (o[26] + o[27])) + ((o[28] + o[29]) + (o[30] + o[31]))),
+                         0x01010101u, sum);
+          }
           if (!is_a) {
             const uint32_t d = dst_row + ss * uint32_t(B_UN), e = d + uint32_t(B_UN);
             sts128(d + d0, o[0], o[1], o[2], o[3]);
@@ -1002,6 +1014,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (ss == uint32_t(L::S)) { ss = 0; s_par ^= 1u; }
       }
       if (!ok) break;
+      if constexpr (PRE) continue;  // the row sums are given
       const int a = ti & 1;
       if (!is_a) sum += __shfl_xor_sync(0xffffffffu, sum, 16);  // the row's other half
       if (!wait_cluster(&rs_empty[a], uint32_t((ti >> 1) & 1) ^ 1u, abort_flag)) break;
@@ -1037,15 +1050,24 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       for (int c = 0; c < nchunks; ++c)
         sws_w[32 * c + lane] = n0 + 32 * c + lane < N ? __half2float(sw[n0 + 32 * c + lane]) : 0.f;
       const float sxr = gm < M ? __half2float(sx[gm]) : 0.f;
+      float* rws_w = rwS + e * BN_MAX;  // PRE: -8 (sum_k w + 8 K) of the tile's columns
+      float bias_r = 0.f;
+      if constexpr (PRE) {
+        for (int c = 0; c < nchunks; ++c) {
+          const int n = n0 + 32 * c + lane;
+          rws_w[32 * c + lane] = n < N ? -8.0f * float(w_rowsum[n] + 8 * K) : 0.f;
+        }
+        bias_r = gm < M ? -8.0f * float(a_rowsum[gm]) : 0.f;
+      }
       __syncwarp();
       const int sa = DBL ? a : 0;
       const uint32_t use = DBL ? uint32_t(ti >> 1) : uint32_t(ti);
       if (!mbar_wait_bounded(&acc_full[sa], use & 1u, abort_flag) ||
-          !wait_cluster(&rs_full[a], uint32_t((ti >> 1) & 1), abort_flag))
+          (!PRE && !wait_cluster(&rs_full[a], uint32_t((ti >> 1) & 1), abort_flag)))
         break;
       fence_after_sync();
-      const float bias_r = 64.0f * float(K) - 8.0f * float(rsA[2 * a * BM + r] + rsA[(2 * a + 1) * BM + r]);
-      const float* rsb = rsB + a * BN_MAX;
+      if constexpr (!PRE) bias_r = 64.0f * float(K) - 8.0f * float(rsA[2 * a * BM + r] + rsA[(2 * a + 1) * BM + r]);
+      const float* rsb = PRE ? rws_w : rsB + a * BN_MAX;
       const uint32_t tmem_row = tmem_base + uint32_t(sa) * L::ACC_COLS + (uint32_t(32 * q) << 16);
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
@@ -1115,7 +1137,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
       }
       __syncwarp();
-      if (lane == 0) {
+      if (!PRE && lane == 0) {
         arrive_at(&rs_empty[a], 0);
         arrive_at(&rs_empty[a], 1);
       }
@@ -1687,18 +1709,22 @@ static int sm_count() {
 
 using namespace quarot;
 
-extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const uint8_t* w_q,
-                                const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
-                                int32_t* acc_out, void* stream) {
+// Shared by quarot_w4a4_gemm (no row sums) and quarot_w4a4_gemm_rowsums
+// (both code-sum vectors given: the CTA-pair forms skip the converters' sums).
+static int w4a4_gemm_impl(const uint8_t* a_q, const void* a_scale, const int32_t* a_rowsum, const uint8_t* w_q,
+                          const void* w_scale, const int32_t* w_rowsum, int64_t M, int64_t N, int64_t K, void* y,
+                          int32_t* acc_out, void* stream) {
   using namespace quarot::gemm;
   if (M < 0 || N < 0 || K <= 0) return QUAROT_ERR_INVALID_ARG;
   if (K % BK != 0 || K > MAX_K) return QUAROT_ERR_UNSUPPORTED;
   if (M > (int64_t(1) << 31) - BM || N > (int64_t(1) << 31) - BN_MAX) return QUAROT_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return QUAROT_OK;
   if (!a_q || !a_scale || !w_q || !w_scale || !y) return QUAROT_ERR_INVALID_ARG;
+  const bool pre = a_rowsum != nullptr && w_rowsum != nullptr;
   if ((reinterpret_cast<uintptr_t>(a_q) & 15) || (reinterpret_cast<uintptr_t>(w_q) & 15) ||
       (reinterpret_cast<uintptr_t>(a_scale) & 1) || (reinterpret_cast<uintptr_t>(w_scale) & 15) ||
-      (reinterpret_cast<uintptr_t>(y) & 15) || (acc_out && (reinterpret_cast<uintptr_t>(acc_out) & 3)))
+      (reinterpret_cast<uintptr_t>(y) & 15) || (acc_out && (reinterpret_cast<uintptr_t>(acc_out) & 3)) ||
+      (pre && ((reinterpret_cast<uintptr_t>(a_rowsum) & 3) || (reinterpret_cast<uintptr_t>(w_rowsum) & 3))))
     return QUAROT_ERR_ALIGNMENT;
   if (!get_encoder()) return QUAROT_ERR_CUDA;
   const int sms = sm_count();
@@ -1714,10 +1740,11 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
     CUtensorMap ta, tb;
     if (!make_map(&ta, a_q, M, K, pair::BM, true) || !make_map(&tb, w_q, N, K, bn / 2, true)) return QUAROT_ERR_CUDA;
     const bool dbl = form == 3;
-    auto kern = dbl ? pair::w4a4_gemm_pair_kernel<true> : pair::w4a4_gemm_pair_kernel<false>;
+    auto kern = dbl ? (pre ? pair::w4a4_gemm_pair_kernel<true, true> : pair::w4a4_gemm_pair_kernel<true, false>)
+                    : (pre ? pair::w4a4_gemm_pair_kernel<false, true> : pair::w4a4_gemm_pair_kernel<false, false>);
     const int smem = dbl ? pair::Layout<true>::SMEM_BYTES : pair::Layout<false>::SMEM_BYTES;
-    static quarot::AttrCache pattr1, pattr2;
-    if (!smem_attr_once(kern, smem, dbl ? pattr2 : pattr1)) return QUAROT_ERR_LAUNCH;
+    static quarot::AttrCache pattr[4];
+    if (!smem_attr_once(kern, smem, pattr[(dbl ? 2 : 0) + (pre ? 1 : 0)])) return QUAROT_ERR_LAUNCH;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
     const int64_t npairs = tiles < pairs ? tiles : pairs;
     cudaLaunchConfig_t cfg = {};
@@ -1734,7 +1761,8 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb,
                                              static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale),
-                                             int(M), int(N), int(K), bn, static_cast<__half*>(y), acc_out);
+                                             int(M), int(N), int(K), bn, static_cast<__half*>(y), acc_out,
+                                             pre ? a_rowsum : nullptr, pre ? w_rowsum : nullptr);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QUAROT_OK : QUAROT_ERR_LAUNCH;
   }
   CUtensorMap ta, tb;
@@ -1747,6 +1775,60 @@ extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const u
       ta, tb, static_cast<const __half*>(a_scale), static_cast<const __half*>(w_scale), int(M), int(N),
       int(K), bn, static_cast<__half*>(y), acc_out);
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+extern "C" int quarot_w4a4_gemm(const uint8_t* a_q, const void* a_scale, const uint8_t* w_q,
+                                const void* w_scale, int64_t M, int64_t N, int64_t K, void* y,
+                                int32_t* acc_out, void* stream) {
+  return w4a4_gemm_impl(a_q, a_scale, nullptr, w_q, w_scale, nullptr, M, N, K, y, acc_out, stream);
+}
+
+namespace quarot {
+namespace gemm {
+// Row code sums of a packed INT4 matrix (two's complement nibbles): one warp
+// per row, 16 bytes (32 codes) per lane and step.  With u = v + 8 (the
+// nibble with its sign bit flipped) the byte-wise sums of the low and high
+// nibbles stay below 256, dp4a adds them, and sum v = sum u - 8 K.
+__global__ void __launch_bounds__(256) int4_rowsum_kernel(const uint8_t* __restrict__ q, int64_t M, int64_t K,
+                                                          int32_t* __restrict__ out) {
+  const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const uint4* src = reinterpret_cast<const uint4*>(q + row * (K / 2));
+  uint32_t acc = 0;
+  for (int64_t c = lane; c < K / 32; c += 32) {
+    const uint4 w = __ldg(src + c);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t x = ws[i] ^ 0x88888888u;
+      acc = __dp4a((x & 0x0F0F0F0Fu) + ((x >> 4) & 0x0F0F0F0Fu), 0x01010101u, acc);
+    }
+  }
+  acc = __reduce_add_sync(0xffffffffu, acc);
+  if (lane == 0) out[row] = int32_t(int64_t(acc) - 8 * K);
+}
+}  // namespace gemm
+}  // namespace quarot
+
+extern "C" int quarot_int4_rowsum(const uint8_t* q, int64_t M, int64_t K, int32_t* rowsum_out, void* stream) {
+  if (M < 0 || K <= 0 || K % 32 != 0 || K > (int64_t(1) << 24)) return QUAROT_ERR_INVALID_ARG;
+  if (M == 0) return QUAROT_OK;
+  if (q == nullptr || rowsum_out == nullptr) return QUAROT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(rowsum_out) & 3))
+    return QUAROT_ERR_ALIGNMENT;
+  const int64_t blocks = (M + 7) / 8;
+  if (blocks > 0x7fffffff) return QUAROT_ERR_UNSUPPORTED;
+  quarot::gemm::int4_rowsum_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(q, M, K,
+                                                                                                   rowsum_out);
+  return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
+}
+
+extern "C" int quarot_w4a4_gemm_rowsums(const uint8_t* a_q, const void* a_scale, const int32_t* a_rowsum,
+                                        const uint8_t* w_q, const void* w_scale, const int32_t* w_rowsum, int64_t M,
+                                        int64_t N, int64_t K, void* y, int32_t* acc_out, void* stream) {
+  if (M > 0 && N > 0 && (a_rowsum == nullptr || w_rowsum == nullptr)) return QUAROT_ERR_INVALID_ARG;
+  return w4a4_gemm_impl(a_q, a_scale, a_rowsum, w_q, w_scale, w_rowsum, M, N, K, y, acc_out, stream);
 }
 
 extern "C" int quarot_w4a4_gemm_a8(const uint8_t* a8, const int32_t* a_rowsum, const void* a_scale,

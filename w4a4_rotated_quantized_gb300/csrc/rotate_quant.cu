@@ -357,8 +357,8 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 // packed nibbles: one byte per code holding u = v + 8 (the e4m3 byte whose
 // value is u * 2^-9), in the order (0, 2, 4, 6, 1, 3, 5, 7) within each group
 // of 8 codes, and the row's code sum sum_k v_k into rowsum_out[row].
-template <int MSEG, bool STAGED, bool RMS, bool A8 = false>
-__global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT, STAGED ? 3 : 1)
+template <int MSEG, bool STAGED, bool RMS, bool A8 = false, bool RS = false>
+__global__ void __launch_bounds__(SegPlan<MSEG, STAGED>::NT, STAGED ? 3 : (RS ? 4 : 1))
 rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, const int8_t* __restrict__ signs,
                         float clip_ratio, float rms_eps, uint8_t* __restrict__ q_out, __half* __restrict__ scale_out,
                         float* __restrict__ rot_out, int32_t* __restrict__ rowsum_out = nullptr) {
@@ -399,8 +399,9 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
   // ---- pass 1 (and the row's sum of squares for RMSNorm)
   float sq = 0.f;
   // the warp's segments unrolled: their load / butterfly / store chains are
-  // independent and overlap (the persistent 12288 kernel is held at 3 CTAs
-  // per SM by its launch bounds, 170 registers)
+  // independent and overlap (launch bounds hold the persistent 12288 kernel
+  // at 3 CTAs per SM, and the two-row 4096 kernel with row sums at 4, i.e. 64
+  // registers: without them it took 72 and ran 3 CTAs per SM)
 #pragma unroll
   for (int sgi = 0; sgi < PL::SPW; ++sgi) {
     const int a = w * PL::SPW + sgi;
@@ -583,7 +584,12 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
     __syncthreads();
     if (valid && t == 0)
       rowsum_out[row] = (isum[r_local * 4] + isum[r_local * 4 + 1]) + (isum[r_local * 4 + 2] + isum[r_local * 4 + 3]);
-  } else if (valid) {
+  } else {
+    // RS: also the row's code sum sum_k v_k into rowsum_out[row].  The
+    // rounded values' bit patterns are 0x4B400000 + v; their sum is kept
+    // modulo 2^32 and the offsets come off once per thread.
+    uint32_t vsum_u = 0;
+    if (valid) {
     uint32_t* qrow = reinterpret_cast<uint32_t*>(q_out + row * (D / 2));
     const float2 fv = make_float2(f, f);
     const float2 magic = make_float2(12582912.0f, 12582912.0f);
@@ -604,6 +610,7 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
         const float2 rr = __fadd2_rn(yv, magic);
         // low nibble of each: the round-half-even integer in two's complement
         byte[jj] = (uint32_t(__float_as_int(rr.x)) & 0x0Fu) | ((uint32_t(__float_as_int(rr.y)) << 4) & 0xF0u);
+        if constexpr (RS) vsum_u += uint32_t(__float_as_int(rr.x)) + uint32_t(__float_as_int(rr.y));
       }
       const uint32_t word = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040),
                                         0x5410);
@@ -613,6 +620,16 @@ rotate_quant_seg_kernel(const __half* __restrict__ x, int64_t M, int64_t ld_x, c
         ro[0] = make_float4(v[a][0].x * post, v[a][0].y * post, v[a][1].x * post, v[a][1].y * post);
         ro[1] = make_float4(v[a][2].x * post, v[a][2].y * post, v[a][3].x * post, v[a][3].y * post);
       }
+    }
+    }  // valid
+    if constexpr (RS) {
+      // valid rows: 8 MSEG values per thread
+      const int vsum = __reduce_add_sync(0xffffffffu, valid ? int(vsum_u - uint32_t(8 * MSEG) * 0x4B400000u) : 0);
+      int* isum = reinterpret_cast<int*>(red) + 40;  // [RPC][4]
+      if (lane == 0) isum[r_local * 4 + w] = vsum;
+      __syncthreads();
+      if (valid && t == 0)
+        rowsum_out[row] = (isum[r_local * 4] + isum[r_local * 4 + 1]) + (isum[r_local * 4 + 2] + isum[r_local * 4 + 3]);
     }
   }
   }  // row loop
@@ -883,11 +900,11 @@ static int launch_seg16(const void* x, int64_t M, int64_t ld_x, const int8_t* si
   return cudaGetLastError() == cudaSuccess ? QUAROT_OK : QUAROT_ERR_LAUNCH;
 }
 
-template <int MSEG, bool STAGED, bool RMS, bool A8 = false>
+template <int MSEG, bool STAGED, bool RMS, bool A8 = false, bool RS = false>
 static int launch_seg_t(const void* x, int64_t M, int64_t ld_x, const int8_t* signs, float clip, float eps, uint8_t* q,
                       void* s, float* rot, cudaStream_t st, int32_t* rowsum = nullptr) {
   using PL = SegPlan<MSEG, STAGED>;
-  auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS, A8>;
+  auto kern = rotate_quant_seg_kernel<MSEG, STAGED, RMS, A8, RS>;
   static quarot::AttrCache attr_done;
   static std::atomic<int> per_sm_dev[64];  // resident CTAs per SM on devices 0..63; 0 until measured
   if (!smem_attr_once(kern, int(PL::SMEM), attr_done)) return QUAROT_ERR_LAUNCH;
@@ -1035,6 +1052,26 @@ extern "C" int quarot_rotate_quant_a8(const void* x, int64_t M, int64_t d, int64
                                                rowsum_out);
   return launch_seg_t<12, true, false, true>(x, M, ld_x, signs, clip_ratio, -1.f, a8_out, scale_out, nullptr, st,
                                              rowsum_out);
+}
+
+extern "C" int quarot_rotate_quant_rowsum(const void* x, int64_t M, int64_t d, int64_t ld_x, const int8_t* signs,
+                                          float clip_ratio, uint8_t* q_out, void* scale_out, int32_t* rowsum_out,
+                                          void* stream) {
+  if (M < 0 || d <= 0 || ld_x < d) return QUAROT_ERR_INVALID_ARG;
+  if (!(clip_ratio > 0.f && clip_ratio <= 1.f)) return QUAROT_ERR_INVALID_ARG;
+  if (d != 4096 && d != 12288) return QUAROT_ERR_UNSUPPORTED;
+  if (M == 0) return QUAROT_OK;
+  if (x == nullptr || q_out == nullptr || scale_out == nullptr || rowsum_out == nullptr) return QUAROT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || (ld_x % 8) || (reinterpret_cast<uintptr_t>(q_out) & 15) ||
+      (reinterpret_cast<uintptr_t>(scale_out) & 1) || (reinterpret_cast<uintptr_t>(rowsum_out) & 3) ||
+      (signs && (reinterpret_cast<uintptr_t>(signs) & 7)))
+    return QUAROT_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 4096)
+    return launch_seg_t<4, false, false, false, true>(x, M, ld_x, signs, clip_ratio, -1.f, q_out, scale_out, nullptr,
+                                                      st, rowsum_out);
+  return launch_seg_t<12, true, false, false, true>(x, M, ld_x, signs, clip_ratio, -1.f, q_out, scale_out, nullptr, st,
+                                                    rowsum_out);
 }
 
 extern "C" int quarot_rmsnorm_rotate_quant(const void* x, int64_t M, int64_t d, int64_t ld_x, float eps,
