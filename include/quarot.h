@@ -52,7 +52,10 @@ enum {
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* quarot_status_string(int status);
 
-/* ABI version: (major << 16) | minor. */
+/* ABI version: (major << 16) | minor.  1.1 adds, with every 1.0 entry point
+ * unchanged: quarot_w4a4_gemm_plan, quarot_legacy_imma_probe,
+ * quarot_rotate_quant_a8, quarot_w4a4_gemm_a8, quarot_rotate_quant_rowsum,
+ * quarot_int4_rowsum and quarot_w4a4_gemm_rowsums. */
 int quarot_version(void);
 
 /* Synchronizes `stream`, then returns and clears the device error word of the

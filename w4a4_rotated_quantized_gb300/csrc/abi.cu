@@ -61,7 +61,7 @@ extern "C" const char* quarot_status_string(int status) {
   }
 }
 
-extern "C" int quarot_version(void) { return (1 << 16) | 0; }
+extern "C" int quarot_version(void) { return (1 << 16) | 1; }
 
 extern "C" int quarot_check_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QUAROT_ERR_CUDA;
