@@ -271,7 +271,7 @@ int quarot_w4a4_gemm_rowsums(const uint8_t* a_q, const void* a_scale, const int3
  * query: it touches no device).  *form = 2 for the CTA-pair kernel (M > 128
  * and an even number of 128-wide k-blocks) with one tensor-memory
  * accumulator, 3 for the same kernel with two (when its tile width is at most
- * 160 and a pair runs three or more tiles, so one tile's drain overlaps the
+ * 192 and a pair runs three or more tiles, so one tile's drain overlaps the
  * next tile's MMAs), 1 for the one-SM kernel; *bn is the N-tile width, one of
  * 128, 160, 192, 224.  Returns QUAROT_ERR_INVALID_ARG
  * for non-positive sizes or null outputs and QUAROT_ERR_UNSUPPORTED for a K

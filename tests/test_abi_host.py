@@ -178,7 +178,8 @@ def test_gemm_plan_query(lib):
     assert q.quarot_w4a4_gemm_plan(8192, 4096, 4096, 152) == (3, 160)  # 11 tiles per pair: two accumulators
     assert q.quarot_w4a4_gemm_plan(1137, 7330, 512, 152) == (3, 128)
     assert q.quarot_w4a4_gemm_plan(2048, 2560, 1024, 152) == (2, 160)
-    assert q.quarot_w4a4_gemm_plan(8192, 12288, 4096, 152) == (2, 192)  # wider than 160: one accumulator
+    assert q.quarot_w4a4_gemm_plan(8192, 12288, 4096, 152) == (3, 192)  # 27 tiles per pair at 192
+    assert q.quarot_w4a4_gemm_plan(2048, 12288, 4096, 152) == (2, 224)  # 6 tiles per pair, wider than 192
     assert q.quarot_w4a4_gemm_plan(512, 12288, 4096, 152) == (2, 192)
     assert q.quarot_w4a4_gemm_plan(16, 256, 256, 152) == (1, 128)
     assert q.quarot_w4a4_gemm_plan(1156, 2888, 128, 152) == (1, 224)

@@ -414,8 +414,9 @@ def test_gemm_sweep_shapes(q, M, N):
 ONE_SM_WIDE = [(1156, 2888, 128), (1030, 2568, 384), (771, 2696, 128)]
 
 # CTA-pair plans the sweep does not reach: one accumulator at BN 160, and two
-# accumulators with ragged M and N tails, from one stage pair per tile to six
-PAIR_FORMS = [(2048, 2560, 1024), (4000, 3000, 256), (1137, 7330, 512), (3100, 7000, 768)]
+# accumulators with ragged M and N tails at BN 128, 160 (six-stage ring) and
+# 192 (four-stage ring), from one stage pair per tile to four
+PAIR_FORMS = [(2048, 2560, 1024), (4000, 3000, 256), (1137, 7330, 512), (3100, 7000, 768), (1548, 5648, 768)]
 
 
 @pytest.mark.parametrize("M,N,K", PAIR_FORMS)
@@ -431,12 +432,12 @@ def test_gemm_one_sm_wide_tiles(q, M, N, K):
 def test_gemm_parity_covers_every_tile_width(q):
     """The GEMM shapes of this module reach N-tile widths 128, 160, 192 and
     224 in both the one-SM and the single-accumulator CTA-pair kernel, and
-    128 and 160 in the two-accumulator CTA-pair kernel, on this GPU."""
+    128, 160 and 192 in the two-accumulator CTA-pair kernel, on this GPU."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shapes = list(GEMM_SHAPES) + [(2048, 4096, 12288)] + [(M, N, 4096) for M in (512, 2048, 8192)
                                                          for N in (4096, 12288)] + ONE_SM_WIDE + PAIR_FORMS
     seen = {q.quarot_w4a4_gemm_plan(M, N, K, sms) for M, N, K in shapes}
-    want = [(f, bn) for f in (1, 2) for bn in (128, 160, 192, 224)] + [(3, 128), (3, 160)]
+    want = [(f, bn) for f in (1, 2) for bn in (128, 160, 192, 224)] + [(3, 128), (3, 160), (3, 192)]
     for p in want:
         assert p in seen, (p, sms)
 

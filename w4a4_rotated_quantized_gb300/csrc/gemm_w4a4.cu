@@ -541,20 +541,22 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 static_assert(SP % 2 == 0 && S % 2 == 0, "converters take stages in pairs");
 static_assert(OFF_RSB % 16 == 0 && OFF_SW % 16 == 0 && (BN_MAX * 4) % 16 == 0, "16-byte shared loads of row sums and scales");
 
-// The two forms of the pair kernel.  DBL = false: eight converted stages, A
+// The three forms of the pair kernel.  V = 0: eight converted stages, A
 // stages at tensor-memory columns [256, 512), one accumulator at [0, BN) with
-// BN up to 224.  DBL = true, for pairs that run many tiles (each tile's
-// accumulator drain would otherwise idle the tensor pipe): six converted
-// stages, A stages at [320, 512), two accumulators at [0, 160) and
-// [160, 320) -- the epilogue drains tile i's while the MMAs of tile i + 1
-// fill the other -- and BN up to 160.
-template <bool DBL>
+// BN up to 224.  V = 1 and 2, for pairs that run many tiles (each tile's
+// accumulator drain would otherwise idle the tensor pipe): two accumulators
+// -- the epilogue drains tile i's while the MMAs of tile i + 1 fill the
+// other -- at [0, 160) and [160, 320) with six converted stages at
+// [320, 512) and BN up to 160 (V = 1), or at [0, 192) and [192, 384) with
+// four converted stages at [384, 512) and BN up to 192 (V = 2).
+template <int V>
 struct Layout {
-  static constexpr int S = DBL ? 6 : pair::S;
+  static constexpr bool DBL = V != 0;
+  static constexpr int S = V == 0 ? pair::S : (V == 1 ? 6 : 4);
   static constexpr int NACC = DBL ? 2 : 1;
-  static constexpr uint32_t ACC_COLS = DBL ? 160u : 0u;
-  static constexpr uint32_t A_COL = DBL ? 320u : TMEM_A_COL;
-  static constexpr int BN_LIMIT = DBL ? 160 : BN_MAX;
+  static constexpr uint32_t ACC_COLS = V == 0 ? 0u : (V == 1 ? 160u : 192u);
+  static constexpr uint32_t A_COL = V == 0 ? TMEM_A_COL : (V == 1 ? 320u : 384u);
+  static constexpr int BN_LIMIT = V == 0 ? BN_MAX : int(ACC_COLS);
   static constexpr int OFF_BU = 0;
   static constexpr int OFF_AP = OFF_BU + S * B_UN;
   static constexpr int OFF_BP = OFF_AP + SP * A_PK;
@@ -577,7 +579,7 @@ struct Layout {
   static_assert(S % 2 == 0, "converters take stages in pairs");
   static_assert(OFF_RSB % 16 == 0 && OFF_SW % 16 == 0, "16-byte shared loads of row sums and scales");
 };
-static_assert(Layout<false>::OFF_BAR == OFF_BAR && Layout<false>::OFF_SW == OFF_SW, "single form keeps its layout");
+static_assert(Layout<0>::OFF_BAR == OFF_BAR && Layout<0>::OFF_SW == OFF_SW, "single form keeps its layout");
 
 #define QUAROT_TMEM_ST16(taddr, r)                                                                 \
   asm volatile(                                                                                    \
@@ -735,13 +737,14 @@ __device__ __forceinline__ void commit2(uint64_t* bar) {
 // the offset corrections from them: -8 sum_k a for the row and
 // -8 (sum_k w + 8 K) for the column (both exact in fp32), the same values the
 // converters' sums give.
-template <bool DBL, bool PRE>
+template <int V, bool PRE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __half* __restrict__ sx, const __half* __restrict__ sw, int M, int N, int K, int BN,
                       __half* __restrict__ y, int32_t* __restrict__ acc_out, const int32_t* __restrict__ a_rowsum,
                       const int32_t* __restrict__ w_rowsum) {
-  using L = Layout<DBL>;
+  using L = Layout<V>;
+  constexpr bool DBL = L::DBL;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1680,17 +1683,18 @@ static int pick_bn_pair(int64_t M, int64_t N, int pairs) {
 // The launch plan of one GEMM on a GPU with `sms` SMs: for M > 128 with an
 // even k-block count the CTA-pair kernel, else the one-SM kernel (form 1),
 // and the N-tile width.  The pair kernel keeps two accumulators (form 3)
-// where its width is at most 160 anyway and a pair runs three or more tiles,
+// where its width is at most 192 anyway and a pair runs three or more tiles,
 // so the drains between them can hide; otherwise one (form 2).  Narrowing a
 // tile to reach two accumulators does not pay: the converters' time per
 // k-block hardly depends on the width (measured: 2048 x 4096 x 12288 takes
-// 117.7 us at BN 160 with two accumulators against 92.2 us at 224 with one).
+// 117.7 us at BN 160 with two accumulators against 92.2 us at 224 with one,
+// and 2048 x 12288 x 4096 88.2 us at 192 with two against 85.3 at 224).
 static void plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn) {
   if (M > BM && sms >= 2 && (K / BK) % 2 == 0) {
     const int pairs = sms / 2;
     *bn = pick_bn_pair(M, N, pairs);
     const int64_t tiles = ((M + 255) / 256) * ((N + *bn - 1) / *bn);
-    *form = (*bn <= pair::Layout<true>::BN_LIMIT && (tiles + pairs - 1) / pairs >= 3) ? 3 : 2;
+    *form = (*bn <= pair::Layout<2>::BN_LIMIT && (tiles + pairs - 1) / pairs >= 3) ? 3 : 2;
   } else {
     *form = 1;
     *bn = pick_bn(M, N, sms);
@@ -1739,12 +1743,17 @@ static int w4a4_gemm_impl(const uint8_t* a_q, const void* a_scale, const int32_t
     const int pairs = sms / 2;
     CUtensorMap ta, tb;
     if (!make_map(&ta, a_q, M, K, pair::BM, true) || !make_map(&tb, w_q, N, K, bn / 2, true)) return QUAROT_ERR_CUDA;
-    const bool dbl = form == 3;
-    auto kern = dbl ? (pre ? pair::w4a4_gemm_pair_kernel<true, true> : pair::w4a4_gemm_pair_kernel<true, false>)
-                    : (pre ? pair::w4a4_gemm_pair_kernel<false, true> : pair::w4a4_gemm_pair_kernel<false, false>);
-    const int smem = dbl ? pair::Layout<true>::SMEM_BYTES : pair::Layout<false>::SMEM_BYTES;
-    static quarot::AttrCache pattr[4];
-    if (!smem_attr_once(kern, smem, pattr[(dbl ? 2 : 0) + (pre ? 1 : 0)])) return QUAROT_ERR_LAUNCH;
+    // form 2: one accumulator; form 3: two, the width deciding the layout
+    const int v = form == 2 ? 0 : (bn <= pair::Layout<1>::BN_LIMIT ? 1 : 2);
+    using KernT = decltype(&pair::w4a4_gemm_pair_kernel<0, false>);
+    const KernT kerns[3][2] = {{pair::w4a4_gemm_pair_kernel<0, false>, pair::w4a4_gemm_pair_kernel<0, true>},
+                               {pair::w4a4_gemm_pair_kernel<1, false>, pair::w4a4_gemm_pair_kernel<1, true>},
+                               {pair::w4a4_gemm_pair_kernel<2, false>, pair::w4a4_gemm_pair_kernel<2, true>}};
+    const int smems[3] = {pair::Layout<0>::SMEM_BYTES, pair::Layout<1>::SMEM_BYTES, pair::Layout<2>::SMEM_BYTES};
+    auto kern = kerns[v][pre ? 1 : 0];
+    const int smem = smems[v];
+    static quarot::AttrCache pattr[6];
+    if (!smem_attr_once(kern, smem, pattr[2 * v + (pre ? 1 : 0)])) return QUAROT_ERR_LAUNCH;
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn);
     const int64_t npairs = tiles < pairs ? tiles : pairs;
     cudaLaunchConfig_t cfg = {};
