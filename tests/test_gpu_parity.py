@@ -544,6 +544,25 @@ def test_decode_single_sequence_long(q):
         _check_per_head(out, ref)
 
 
+@pytest.mark.parametrize("G", [1, 8])
+@pytest.mark.parametrize("T", [2048, 2304])
+def test_decode_split_counts(q, G, T):
+    """One sequence, two KV heads: T 2048 runs 8 splits of 256 tokens per row
+    and T 2304 runs 9, so the combine merges 8 and 9 partial states per head,
+    for one query head per KV head and for eight."""
+    B, Hkv, d = 1, 2, 128
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 61 + T + G)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 62 + T + G)
+    qq = W.query(B, Hkv * G, d, 63 + T + G)
+    oc = _caches(k.shape, T)
+    O.kv_write(k, v, 0, *oc)
+    for unrot in (False, True):
+        out = q.quarot_decode_attn(_t(qq), *[_t(c) for c in oc], T=T, unrotate_out=unrot).cpu().numpy()
+        ref = O.decode_attn(qq, *oc, T=T, unrotate=unrot)
+        assert O.rel_fro(out, ref) <= OUT_TOL
+        _check_per_head(out, ref)
+
+
 def test_decode_custom_scale_and_zero_T(q):
     B, Hkv, G, d, T = 1, 2, 4, 128, 77
     k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 5)
