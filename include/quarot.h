@@ -270,10 +270,12 @@ int quarot_w4a4_gemm_rowsums(const uint8_t* a_q, const void* a_scale, const int3
  * launches for an M x N x K problem on a GPU with `sms` SMs (a host-only
  * query: it touches no device).  *form = 2 for the CTA-pair kernel (M > 128
  * and an even number of 128-wide k-blocks) with one tensor-memory
- * accumulator, 3 for the same kernel with two (when its tile width is at most
- * 192 and a pair runs three or more tiles, so one tile's drain overlaps the
- * next tile's MMAs), 1 for the one-SM kernel; *bn is the N-tile width, one of
- * 128, 160, 192, 224.  Returns QUAROT_ERR_INVALID_ARG
+ * accumulator, 3 for the same kernel with two (possible at tile widths up to
+ * 192 from three tiles per pair: one tile's drain overlaps the next tile's
+ * MMAs), 1 for the one-SM kernel; *bn is the N-tile width, one of 128, 160,
+ * 192, 224.  The pair kernel's width and form minimise a time model per pair
+ * (a tile costs its k-block count, each drain that one accumulator exposes
+ * about 5 k-blocks more, ties going to the narrower width).  Returns QUAROT_ERR_INVALID_ARG
  * for non-positive sizes or null outputs and QUAROT_ERR_UNSUPPORTED for a K
  * the GEMM rejects.  The pages have no counterpart: it lets tests and tools
  * see which tile configuration a shape exercises. */

@@ -170,16 +170,19 @@ def test_missing_library_fails_loudly(monkeypatch):
 
 def test_gemm_plan_query(lib):
     """The launch plan (kernel form, N-tile width) as the host computes it for
-    a 152-SM GB300: the bench shape takes the CTA pair at BN 224, the sweep
-    reaches 160 and 192, many tiles per pair at BN <= 160 the pair kernel with
-    two accumulators, small M the one-SM kernel, an odd k-block count the
-    one-SM kernel at any M; bad sizes are rejected."""
+    a 152-SM GB300: the pair kernel's width and accumulator count minimise
+    its modelled time per pair (a tile costs its k-blocks, a drain exposed by
+    the one-accumulator form about 5 more; ties go to the narrower width),
+    small M takes the one-SM kernel, an odd k-block count the one-SM kernel at
+    any M; bad sizes are rejected."""
     assert q.quarot_w4a4_gemm_plan(2048, 4096, 12288, 152) == (2, 224)
-    assert q.quarot_w4a4_gemm_plan(8192, 4096, 4096, 152) == (3, 160)  # 11 tiles per pair: two accumulators
-    assert q.quarot_w4a4_gemm_plan(1137, 7330, 512, 152) == (3, 128)
+    assert q.quarot_w4a4_gemm_plan(8192, 4096, 4096, 152) == (2, 224)  # 8 tiles at 224 beat 10 and 11 narrower
+    assert q.quarot_w4a4_gemm_plan(4000, 3000, 256, 152) == (3, 160)  # tied with 192: the narrower
+    assert q.quarot_w4a4_gemm_plan(7000, 1000, 256, 152) == (3, 128)  # tied with 160 and 192
+    assert q.quarot_w4a4_gemm_plan(1137, 7330, 512, 152) == (3, 192)
     assert q.quarot_w4a4_gemm_plan(2048, 2560, 1024, 152) == (2, 160)
     assert q.quarot_w4a4_gemm_plan(8192, 12288, 4096, 152) == (3, 192)  # 27 tiles per pair at 192
-    assert q.quarot_w4a4_gemm_plan(2048, 12288, 4096, 152) == (2, 224)  # 6 tiles per pair, wider than 192
+    assert q.quarot_w4a4_gemm_plan(2048, 12288, 4096, 152) == (2, 224)  # 6 x 32 + 5 drains < 7 x 32
     assert q.quarot_w4a4_gemm_plan(512, 12288, 4096, 152) == (2, 192)
     assert q.quarot_w4a4_gemm_plan(16, 256, 256, 152) == (1, 128)
     assert q.quarot_w4a4_gemm_plan(1156, 2888, 128, 152) == (1, 224)

@@ -416,7 +416,8 @@ ONE_SM_WIDE = [(1156, 2888, 128), (1030, 2568, 384), (771, 2696, 128)]
 # CTA-pair plans the sweep does not reach: one accumulator at BN 160, and two
 # accumulators with ragged M and N tails at BN 128, 160 (six-stage ring) and
 # 192 (four-stage ring), from one stage pair per tile to four
-PAIR_FORMS = [(2048, 2560, 1024), (4000, 3000, 256), (1137, 7330, 512), (3100, 7000, 768), (1548, 5648, 768)]
+PAIR_FORMS = [(2048, 2560, 1024), (4000, 3000, 256), (1137, 7330, 512), (3100, 7000, 768), (1548, 5648, 768),
+              (7000, 1000, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", PAIR_FORMS)

@@ -1663,38 +1663,42 @@ static int pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-// Pair kernel: the N-tile width minimising the per-pair makespan.
-static int pick_bn_pair(int64_t M, int64_t N, int pairs) {
-  const int cands[4] = {224, 192, 160, 128};
-  int best = 224;
+// Pair kernel: the N-tile width and form with the smallest modelled time per
+// pair.  The converters bound the pair and take about the same time per
+// k-block at every width (~0.37-0.39 us on 152 SMs), so a tile costs its
+// k-block count whatever its width.  With one accumulator every tile but the
+// last also exposes its drain, which the next tile's MMAs must wait out
+// (~2 us, about 5 k-blocks); two accumulators (widths up to 192, from three
+// tiles per pair) hide it.  Ties go to the narrower tile, which gives each
+// pair less work.  Fitted to the K = 4096 sweep and the 12288-deep shape:
+// e.g. 8192 x 4096 x 4096 runs 112.3 us at 224 (8 tiles per pair, one
+// accumulator), 122.3 at 192 and 130.4 at 160 (10 and 11 tiles, two).
+// allow_dbl = false: a kernel with one accumulator only.
+static void pick_pair_plan(int64_t M, int64_t N, int64_t K, int pairs, int* form, int* bn, bool allow_dbl = true) {
+  constexpr int64_t kDrainKBlocks = 5;
+  const int cands[4] = {128, 160, 192, 224};
+  const int64_t mt = (M + 255) / 256, kb = K / BK;
   int64_t best_cost = -1;
-  const int64_t mt = (M + 255) / 256;
-  for (int bn : cands) {
-    const int64_t tiles = mt * ((N + bn - 1) / bn);
-    const int64_t cost = ((tiles + pairs - 1) / pairs) * bn;
+  for (int w : cands) {
+    const int64_t tiles = mt * ((N + w - 1) / w);
+    const int64_t tpp = (tiles + pairs - 1) / pairs;
+    const bool dbl = allow_dbl && w <= pair::Layout<2>::BN_LIMIT && tpp >= 3;
+    const int64_t cost = tpp * kb + (dbl ? 0 : (tpp - 1) * kDrainKBlocks);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      best = bn;
+      *bn = w;
+      *form = dbl ? 3 : 2;
     }
   }
-  return best;
 }
 
 // The launch plan of one GEMM on a GPU with `sms` SMs: for M > 128 with an
 // even k-block count the CTA-pair kernel, else the one-SM kernel (form 1),
-// and the N-tile width.  The pair kernel keeps two accumulators (form 3)
-// where its width is at most 192 anyway and a pair runs three or more tiles,
-// so the drains between them can hide; otherwise one (form 2).  Narrowing a
-// tile to reach two accumulators does not pay: the converters' time per
-// k-block hardly depends on the width (measured: 2048 x 4096 x 12288 takes
-// 117.7 us at BN 160 with two accumulators against 92.2 us at 224 with one,
-// and 2048 x 12288 x 4096 88.2 us at 192 with two against 85.3 at 224).
+// and the N-tile width.  The pair kernel keeps one accumulator (form 2) or
+// two (form 3), as pick_pair_plan models.
 static void plan(int64_t M, int64_t N, int64_t K, int sms, int* form, int* bn) {
   if (M > BM && sms >= 2 && (K / BK) % 2 == 0) {
-    const int pairs = sms / 2;
-    *bn = pick_bn_pair(M, N, pairs);
-    const int64_t tiles = ((M + 255) / 256) * ((N + *bn - 1) / *bn);
-    *form = (*bn <= pair::Layout<2>::BN_LIMIT && (tiles + pairs - 1) / pairs >= 3) ? 3 : 2;
+    pick_pair_plan(M, N, K, sms / 2, form, bn);
   } else {
     *form = 1;
     *bn = pick_bn(M, N, sms);
@@ -1859,7 +1863,8 @@ extern "C" int quarot_w4a4_gemm_a8(const uint8_t* a8, const int32_t* a_rowsum, c
   if (sms < 2) return sms <= 0 ? QUAROT_ERR_CUDA : QUAROT_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int pairs = sms / 2;
-  const int bn = pick_bn_pair(M, N, pairs);
+  int form_a8 = 0, bn = 0;
+  pick_pair_plan(M, N, K, pairs, &form_a8, &bn, false);
   CUtensorMap ta, tb;
   if (!make_map_a8(&ta, a8, M, K, pair::BM) || !make_map(&tb, w_q, N, K, bn / 2, true)) return QUAROT_ERR_CUDA;
   static quarot::AttrCache attr8;
