@@ -576,8 +576,9 @@ def run_ours(args):
         stage_ms_flush.append(tm.flushed(per_set[0][j], reps=max(10, min(args.steps, 50))))
 
     # ---------------- e2e: host buffers through the C ABI, copies inside the timed region
-    # Every step copies its inputs (X, the new K/V token, q) from pinned host
-    # memory and reads its results (Y, the decode output) back.  The steps are
+    # Every step copies its inputs (X, and the new K/V token with q as one
+    # packed copy) from pinned host memory and reads its results (Y, the decode
+    # output) back.  The steps are
     # pipelined the way a serving loop would run them: host-to-device copies on
     # one stream, the four kernels on the compute stream, device-to-host copies
     # on a third, with double-buffered device tensors, so step i+1's input copy
@@ -585,11 +586,29 @@ def run_ours(args):
     # KV cache 69 MB) exceeds L2, so no flush is needed between steps.
     s0 = SETS[0]
     x_h = torch.from_numpy(x).pin_memory()
-    kn_h, vn_h, q_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q_dec.cpu().pin_memory()
+    # the decode branch's three small inputs travel as one copy: a pinned host
+    # buffer [k_new | v_new | q] and, per slot, a device buffer viewed as the
+    # three tensors (each piece starts on a 256-byte boundary)
+    small = [k_new, v_new, q_dec]
+    offs, tot = [], 0
+    for t_ in small:
+        offs.append(tot)
+        tot += (t_.numel() * t_.element_size() + 255) // 256 * 256
+    small_h = torch.zeros(tot, dtype=torch.uint8).pin_memory()
+    for t_, o_ in zip(small, offs):
+        nb_ = t_.numel() * t_.element_size()
+        small_h[o_:o_ + nb_].copy_(t_.cpu().contiguous().view(-1).view(torch.uint8))
+    small_d = [torch.empty(tot, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def piece(buf, i):
+        t_ = small[i]
+        nb_ = t_.numel() * t_.element_size()
+        return buf[offs[i]:offs[i] + nb_].view(t_.dtype).view(t_.shape)
+
     xd = [torch.empty_like(xt) for _ in range(2)]
-    kd = [torch.empty_like(k_new) for _ in range(2)]
-    vd = [torch.empty_like(v_new) for _ in range(2)]
-    qd = [torch.empty_like(q_dec) for _ in range(2)]
+    kd = [piece(small_d[i], 0) for i in range(2)]
+    vd = [piece(small_d[i], 1) for i in range(2)]
+    qd = [piece(small_d[i], 2) for i in range(2)]
     aqd = [torch.empty_like(s0["aq"]) for _ in range(2)]
     asd = [torch.empty_like(s0["asx"]) for _ in range(2)]
     ard = [torch.empty_like(s0["ars"]) for _ in range(2)]
@@ -609,10 +628,8 @@ def run_ours(args):
             if i >= 2:
                 h2d_st.wait_event(ev_comp[sl])  # slot's inputs no longer read
             with torch.cuda.stream(h2d_st):
+                small_d[sl].copy_(small_h, non_blocking=True)
                 xd[sl].copy_(x_h, non_blocking=True)
-                kd[sl].copy_(kn_h, non_blocking=True)
-                vd[sl].copy_(vn_h, non_blocking=True)
-                qd[sl].copy_(q_h, non_blocking=True)
             ev_in[sl].record(h2d_st)
             stream.wait_event(ev_in[sl])
             if i >= 2:
@@ -644,7 +661,7 @@ def run_ours(args):
     q.quarot_check_error(stream)
     e2e_total = _job_time_ms(float(e_start.elapsed_time(e_end)), ws, dev)
     e2e_val = _job_rate(M_TOK, args.steps, ws, e2e_total)
-    h2d = (xd[0].numel() * 2 + kd[0].numel() * 2 + vd[0].numel() * 2 + qd[0].numel() * 2)
+    h2d = xd[0].numel() * xd[0].element_size() + small_h.numel()
     d2h = s0["y"].numel() * 2 + s0["out"].numel() * 2
     # the results of the last step match the device-resident step's
     torch.cuda.synchronize()
