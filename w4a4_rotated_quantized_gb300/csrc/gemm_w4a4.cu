@@ -745,6 +745,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                       const int32_t* __restrict__ w_rowsum) {
   using L = Layout<V>;
   constexpr bool DBL = L::DBL;
+  constexpr bool EARLY_PK = V != 2;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -985,6 +986,16 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                              (((o[24] + o[25]) + (o[26] + o[27])) + ((o[28] + o[29]) + (o[30] + o[31]))),
                          0x01010101u, sum);
           }
+        }
+        // the packed stage pair is in registers: hand it back to the producer
+        // before the stores (not in the four-stage layout, whose converters
+        // already run at most two pairs ahead; measured there 316.3 -> 318.8 us
+        // at 8192 x 4096 x 12288, elsewhere 0.2-1.0 us faster)
+        if constexpr (EARLY_PK) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pk_empty[sp]);
+        }
+        if (active) {
           if (!is_a) {
             const uint32_t d = dst_row + ss * uint32_t(B_UN), e = d + uint32_t(B_UN);
             sts128(d + d0, o[0], o[1], o[2], o[3]);
@@ -1009,7 +1020,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if (lane == 0) {
           mbar_arrive(&full[ss]);
           mbar_arrive(&full[ss + 1]);
-          mbar_arrive(&pk_empty[sp]);
+          if constexpr (!EARLY_PK) mbar_arrive(&pk_empty[sp]);
         }
         sp += 2;
         if (sp == uint32_t(SP)) { sp = 0; pk_par ^= 1u; }
