@@ -871,8 +871,10 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 #pragma unroll
               for (int kk = 0; kk < BK / 32; ++kk)
                 mma2_ts(tmem_d, ta + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc, ((kb + u) | kk) != 0);
-              commit2(&empty[s + u]);
             }
+            // one commit frees the pair: it tracks every earlier MMA of this
+            // thread, those of stage s included
+            commit2(&empty[s + 1]);
           }
           __syncwarp();
         }
@@ -950,8 +952,8 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       uint32_t sum = 0;
       bool ok = true;
       for (int kb = 0; kb < nkb; kb += 2) {
+        // empty[ss + 1] completes once the MMAs of both stages are done
         if (!mbar_wait_bounded(&pk_full[sp], pk_par, abort_flag) ||
-            !mbar_wait_bounded(&empty[ss], s_par ^ 1u, abort_flag) ||
             !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -1328,7 +1330,8 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = int(it % SA);
-        if (!warp_wait(&empty[s], uint32_t((it / SA) & 1) ^ 1u, abort_flag)) break;
+        // stages are freed in pairs, by the commit on the odd one (same lap)
+        if (!warp_wait(&empty[s | 1], uint32_t((it / SA) & 1) ^ 1u, abort_flag)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&a_full[s], A_UN);
           tma_load_2d(smem_u32(sm + OFF_A + s * A_UN), &tmA, kb * BK, m0, &a_full[s]);
@@ -1371,8 +1374,10 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 #pragma unroll
               for (int kk = 0; kk < BK / 32; ++kk)
                 mma2_ss(tmem_d, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc, ((kb + u) | kk) != 0);
-              commit2(&empty[s + u]);
             }
+            // one commit frees the pair: it tracks every earlier MMA of this
+            // thread, those of stage s included
+            commit2(&empty[s + 1]);
           }
           __syncwarp();
         }
@@ -1428,8 +1433,8 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       uint32_t sum = 0;
       bool ok = true;
       for (int kb = 0; kb < nkb; kb += 2) {
+        // empty[ss + 1] completes once the MMAs of both stages are done
         if (!mbar_wait_bounded(&pk_full[sp], pk_par, abort_flag) ||
-            !mbar_wait_bounded(&empty[ss], s_par ^ 1u, abort_flag) ||
             !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
           ok = false;
           break;
