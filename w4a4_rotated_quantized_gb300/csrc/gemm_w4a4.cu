@@ -852,10 +852,10 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         const uint32_t tmem_d = tmem_base + uint32_t(sa) * L::ACC_COLS;
         fence_after_sync();
         bool ok = true;
-        // stages in pairs, as the converters complete them: the phase of
-        // stage s + 1 completes only after every arrival on stage s (each
-        // converter warp and the relay arrive on s first), so one wait covers
-        // both, and the eight MMAs of the pair issue back to back
+        // stages in pairs, as the converters complete them: each converter
+        // warp and the relay arrive once per pair, on its second stage, after
+        // their writes of both stages, so one wait covers both, and the eight
+        // MMAs of the pair issue back to back
         for (int kb = 0; kb < nkb; kb += 2, it += 2) {
           const int s = int(it % L::S);
           if (!warp_wait(&full[s + 1], uint32_t((it / L::S) & 1), abort_flag)) {
@@ -901,8 +901,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             break;
           }
           if (lane == 0) {
-            handoff_at(&full[s], 0);
-            handoff_at(&full[s + 1], 0);
+            handoff_at(&full[s + 1], 0);  // the issuer waits on the pair's second stage only
           }
           __syncwarp();
         }
@@ -1020,8 +1019,7 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&full[ss]);
-          mbar_arrive(&full[ss + 1]);
+          mbar_arrive(&full[ss + 1]);  // after the writes of both stages: covers the pair
           if constexpr (!EARLY_PK) mbar_arrive(&pk_empty[sp]);
         }
         sp += 2;
@@ -1405,8 +1403,7 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             break;
           }
           if (lane == 0) {
-            handoff_at(&full[s], 0);
-            handoff_at(&full[s + 1], 0);
+            handoff_at(&full[s + 1], 0);  // the issuer waits on the pair's second stage only
           }
           __syncwarp();
         }
@@ -1480,8 +1477,7 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&full[ss]);
-          mbar_arrive(&full[ss + 1]);
+          mbar_arrive(&full[ss + 1]);  // after the writes of both stages: covers the pair
           mbar_arrive(&pk_empty[sp]);
         }
         sp += 2;
