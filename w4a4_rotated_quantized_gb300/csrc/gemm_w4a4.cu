@@ -1326,21 +1326,23 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     long issued = 0, it = 0;
     for (int tile = pair_id; tile < n_tiles && !warp_flag(abort_flag); tile += n_pairs) {
       const int m0 = (tile / n_tiles_n) * 2 * BM + int(rank) * BM;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+      // stage pairs, as the MMAs free them (the commit on the odd stage) and
+      // behind one barrier (the odd stage's) for both k-blocks' loads
+      for (int kb = 0; kb < nkb; kb += 2, it += 2) {
         const int s = int(it % SA);
-        // stages are freed in pairs, by the commit on the odd one (same lap)
-        if (!warp_wait(&empty[s | 1], uint32_t((it / SA) & 1) ^ 1u, abort_flag)) break;
+        if (!warp_wait(&empty[s + 1], uint32_t((it / SA) & 1) ^ 1u, abort_flag)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&a_full[s], A_UN);
-          tma_load_2d(smem_u32(sm + OFF_A + s * A_UN), &tmA, kb * BK, m0, &a_full[s]);
+          mbar_arrive_expect_tx(&a_full[s + 1], 2 * A_UN);
+          tma_load_2d(smem_u32(sm + OFF_A + s * A_UN), &tmA, kb * BK, m0, &a_full[s + 1]);
+          tma_load_2d(smem_u32(sm + OFF_A + (s + 1) * A_UN), &tmA, (kb + 1) * BK, m0, &a_full[s + 1]);
         }
         __syncwarp();
-        issued = it + 1;
+        issued = it + 2;
       }
     }
     if (warp_flag(abort_flag) && lane == 0) {
-      for (long j = (issued > SA ? issued - SA : 0); j < issued; ++j)
-        mbar_wait_bounded(&a_full[j % SA], uint32_t((j / SA) & 1), nullptr);
+      for (long j = (issued > SA ? issued - SA : 0); j < issued; j += 2)
+        mbar_wait_bounded(&a_full[j % SA + 1], uint32_t((j / SA) & 1), nullptr);
     }
   } else if (warp == 1) {
     if (leader) {
@@ -1353,13 +1355,12 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         fence_after_sync();
         const uint32_t tmem_d = tmem_base + uint32_t(a) * ACC_STRIDE;
         bool ok = true;
-        // stages in pairs (the converters complete them in pairs; the two A
-        // loads are separate transactions, so both are waited for)
+        // stages in pairs (the converters complete them in pairs; the pair's
+        // two A loads complete one barrier)
         for (int kb = 0; kb < nkb; kb += 2, it += 2) {
           const int s = int(it % SA);
           const uint32_t par = uint32_t((it / SA) & 1);
-          if (!warp_wait(&a_full[s], par, abort_flag) || !warp_wait(&a_full[s + 1], par, abort_flag) ||
-              !warp_wait(&full[s + 1], par, abort_flag)) {
+          if (!warp_wait(&a_full[s + 1], par, abort_flag) || !warp_wait(&full[s + 1], par, abort_flag)) {
             ok = false;
             break;
           }
@@ -1397,8 +1398,7 @@ w4a4_gemm_a8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         for (int kb = 0; kb < nkb; kb += 2, it += 2) {
           const int s = int(it % SA);
           const uint32_t par = uint32_t((it / SA) & 1);
-          if (!warp_wait(&a_full[s], par, abort_flag) || !warp_wait(&a_full[s + 1], par, abort_flag) ||
-              !warp_wait(&full[s + 1], par, abort_flag)) {
+          if (!warp_wait(&a_full[s + 1], par, abort_flag) || !warp_wait(&full[s + 1], par, abort_flag)) {
             ok = false;
             break;
           }
