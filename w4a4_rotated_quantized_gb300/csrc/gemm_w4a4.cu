@@ -746,6 +746,13 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
   using L = Layout<V>;
   constexpr bool DBL = L::DBL;
   constexpr bool EARLY_PK = V != 2;
+  // Converters wait for a free converted stage pair after loading and
+  // unpacking the packed one, not before, where that was measured to pay:
+  // with the row sums given (2048 x 4096 x 12288 70.5 -> 68.2 us,
+  // 8192 x 4096 x 12288 306 -> 285 us) and in the four-stage layout (the
+  // latter shape without row sums 347 -> 330 us); without the row sums the
+  // one-accumulator and 160-wide forms ran ~5 % slower with it.
+  constexpr bool LATE_EMPTY = PRE || V == 2;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -951,9 +958,8 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
       uint32_t sum = 0;
       bool ok = true;
       for (int kb = 0; kb < nkb; kb += 2) {
-        // empty[ss + 1] completes once the MMAs of both stages are done
         if (!mbar_wait_bounded(&pk_full[sp], pk_par, abort_flag) ||
-            !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
+            (!LATE_EMPTY && !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
@@ -995,6 +1001,13 @@ w4a4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         if constexpr (EARLY_PK) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&pk_empty[sp]);
+        }
+        // the converted stage pair is written once the MMAs have freed it
+        // (empty[ss + 1] completes once the MMAs of both stages are done);
+        // with LATE_EMPTY the loads and unpacking above overlap that wait
+        if (LATE_EMPTY && !mbar_wait_bounded(&empty[ss + 1], s_par ^ 1u, abort_flag)) {
+          ok = false;
+          break;
         }
         if (active) {
           if (!is_a) {
