@@ -264,7 +264,7 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 //   output  O^T[128 x 2G] += Vcodes^T[128 x 16 tok] . P'^T, with P' = p * v_scale
 //           in fp16 (even columns; odd columns zero); output dims are permuted
 //           so each thread's value bytes are one 8-byte load per token.
-constexpr int NS = 4;                 // tiles in flight per warp
+constexpr int NS = 3;                 // tiles in flight per warp
 constexpr int TILE_BYTES = 2 * 16 * (HD / 2) + 2 * 32;  // K, V codes + scales = 2112
 constexpr int TILE_STRIDE = 2176;     // rounded to 128 bytes
 constexpr int QS = HD + 16;           // padded q~ row: dim d at d + 4 (d >> 5)
