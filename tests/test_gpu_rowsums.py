@@ -91,6 +91,34 @@ def test_gemm_rowsums_full_size(q, M, N, K):
     _gemm_both(q, M, N, K, 800 + M + N)
 
 
+@pytest.mark.parametrize("M,N,K,reps", [(2048, 4096, 12288, 100), (8192, 12288, 4096, 20), (4000, 3000, 256, 100)])
+def test_gemm_repeatable(q, M, N, K, reps):
+    """Back-to-back launches of both GEMM entry points on one set of codes give
+    the same bits every time: the bench shape (one accumulator), a shape with
+    two 192-wide accumulators and the four-stage ring, and one with two
+    160-wide accumulators and one stage pair per tile.  A rare ordering slip
+    between the converters, the relay, the MMA issuer and the epilogue would
+    show as a launch that differs."""
+    g = torch.Generator(device="cpu").manual_seed(M + N + K)
+    aq = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, generator=g).to(DEV)
+    wq = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g).to(DEV)
+    sx = (torch.rand(M, generator=g) * 0.1 + 0.01).half().to(DEV)
+    sw = (torch.rand(N, generator=g) * 0.01 + 0.001).half().to(DEV)
+    ars, wrs = q.quarot_int4_rowsum(aq), q.quarot_int4_rowsum(wq)
+    y0, acc0 = q.quarot_w4a4_gemm_rowsums(aq, sx, ars, wq, sw, wrs, want_acc=True)
+    yp, accp = q.quarot_w4a4_gemm(aq, sx, wq, sw, want_acc=True)
+    assert torch.equal(acc0, accp) and torch.equal(y0, yp)
+    y = torch.empty_like(y0)
+    acc = torch.empty_like(acc0)
+    for i in range(reps):
+        if i % 2 == 0:
+            q.quarot_w4a4_gemm_rowsums(aq, sx, ars, wq, sw, wrs, y=y, acc_out=acc)
+        else:
+            q.quarot_w4a4_gemm(aq, sx, wq, sw, y=y, acc_out=acc)
+        assert torch.equal(acc, acc0) and torch.equal(y, y0), i
+    q.quarot_check_error()
+
+
 def test_gemm_rowsums_extremes_large_k(q):
     M, N, K = 200, 136, 65536
     a = np.full((M, K), 7, dtype=np.int8)
