@@ -780,6 +780,34 @@ def test_kv_write_asym_parity(q, d):
         assert np.all(zeros[:, :, :t0] == 0) and np.all(zeros[:, :, t0 + T:] == 0)
 
 
+@pytest.mark.parametrize("asym", [False, True])
+@pytest.mark.parametrize("T", [997, 1003])
+def test_decode_unaligned_cache_rows(q, asym, T):
+    """A cache capacity that is not a multiple of 8 tokens: the scale rows (and
+    zero-point rows) of the (sequence, KV head) rows start off 16-byte
+    boundaries, so bulk copies cannot fetch them and every tile takes the
+    plain-load path; T 997 also ends on a ragged tile, T 1003 fills the cache."""
+    B, Hkv, G, d, T_max = 2, 2, 4, 128, 1003
+    k = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 71 + T)
+    v = W.kv_tensors(B, T, Hkv, d, 2, 20.0, 72 + T)
+    qq = W.query(B, Hkv * G, d, 73 + T)
+    if asym:
+        oc = _caches_asym(k.shape, T_max)
+        O.kv_write_asym(k, v, 0, *oc, clip_ratio=0.95)
+    else:
+        oc = _caches(k.shape, T_max)
+        O.kv_write(k, v, 0, *oc)
+    for unrot in (False, True):
+        if asym:
+            out = q.quarot_decode_attn_asym(_t(qq), *[_t(c) for c in oc], T=T, unrotate_out=unrot)
+            ref = O.decode_attn_asym(qq, *oc, T=T, unrotate=unrot)
+        else:
+            out = q.quarot_decode_attn(_t(qq), *[_t(c) for c in oc], T=T, unrotate_out=unrot)
+            ref = O.decode_attn(qq, *oc, T=T, unrotate=unrot)
+        assert O.rel_fro(out.cpu().numpy(), ref) <= OUT_TOL
+        _check_per_head(out.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("G", [1, 4, 8])
 @pytest.mark.parametrize("T", [1, 17, 300, 1000])
 def test_decode_asym_parity(q, G, T):
